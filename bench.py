@@ -1,0 +1,556 @@
+"""Benchmark of the MX hot path on GB300 (one JSON line on stdout).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl mx|reference]
+                    [--workload all|sweep|gemm|fp4|fused|pipeline256]
+
+A step is one pass of the whole hot path over its synthetic inputs:
+  sweep  QuantizeMX on [8192, 8192] for {bf16, f16} x {e4m3fn, e5m2} x
+         {plain, interleaved} scales, 8x4 blocks along dim=-2 (8 launches);
+  gemm   for e4m3fn -> bf16 and e5m2 -> f32: QuantizeMX of A and Bt
+         ([8192, 8192] bf16, 1x32 blocks along K), repack of both scale
+         tensors to the tensor-core layout, ScaledMatmul 8192^3;
+  fp4    QuantizeMX [16384, 16384] bf16 -> e2m1, 8x4, packed, interleaved;
+  fused  activation quantize + ScaledMatmul, X [16384, 8192] bf16 times a
+         pre-quantized e4m3fn weight W [8192, 28672] -> bf16.
+The headline `value` is QuantizeMX GB/s over the sweep (algorithmic bytes:
+2 read + 1 written + 1/32 scale written per element); `scaled_matmul`,
+`fp4_quantize` and `fused` carry the other workloads with their own rooflines.
+Inputs are larger than L2 and rotated so no launch re-reads the previous
+launch's input from L2.  Kernel times come from CUDA events on the launching
+stream; the whole step is bracketed by a barrier and a synchronize.
+
+--impl reference times the CPU oracle (plain C, one core) on a bounded
+sample of the sweep workload, with the same metric and unit.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import mx_synth as syn  # noqa: E402
+
+METRIC = "QuantizeMX GB/s & ScaledMatmul TFLOP/s on 1 GB300, % of HBM/MXFP8 peak"
+SWEEP = (8192, 8192)
+SWEEP_VARIANTS = [(i, f) for i in ("bf16", "f16") for f in ("e4m3fn", "e5m2")]
+SWEEP_BYTES = 2 * 8192 * 8192 + 8192 * 8192 + 1024 * 2048          # 203,423,744 per launch
+FP4_SHAPE = (16384, 16384)
+FP4_BYTES = 2 * 16384 * 16384 + 16384 * 16384 // 2 + 2048 * 4096  # 679,477,248
+GEMM_N = 8192
+GEMM_FLOP = 2 * GEMM_N ** 3
+FUSED = (16384, 28672, 8192)
+FUSED_FLOP = 2 * FUSED[0] * FUSED[1] * FUSED[2]
+# nominal dense MXFP8 : bf16 tensor ratio (4.5 : 2.25 PFLOP/s)
+FP8_OVER_BF16 = 2.0
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        p = json.load(open(path))
+        return {"hbm": p["hbm_gbs"], "bf16": p["bf16_tflops"], "bf16_sust": p.get("bf16_tflops_sustained"),
+                "src": "of measured"}
+    return {"hbm": 6800.0, "bf16": 1900.0, "bf16_sust": 1700.0, "src": "of fallback"}
+
+
+def source_hash(*names):
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "mx_fp8_microscaling_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel_key, src_hash):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    try:
+        entry = json.load(open(path)).get(kernel_key)
+    except (ValueError, OSError):
+        return None
+    if not entry or entry.get("source_hash") != src_hash:
+        return None
+    return entry.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.proc = None
+        self.gpu = gpu_index
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        rows = [[c.strip() for c in line.split(",")] for line in out.strip().splitlines() if line.strip()]
+        sm = [float(r[1]) for r in rows if len(r) >= 9 and r[1].replace(".", "").isdigit()]
+        mx_ = [float(r[2]) for r in rows if len(r) >= 9 and r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in rows:
+            if len(r) < 9:
+                continue
+            for name, v in zip(names, r[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        load = [s for s in sm if mx_ and s >= 0.5 * max(mx_)] or sm
+        return {"sm_mhz": statistics.median(load) if load else None,
+                "sm_max_mhz": max(mx_) if mx_ else None, "reasons": sorted(reasons),
+                "samples": len(rows)}
+
+
+# ---------------------------------------------------------------- workloads
+
+class Timer:
+    """Accumulates CUDA-event durations per label on the current stream."""
+
+    def __init__(self, torch):
+        self.torch = torch
+        self.pending = []
+        self.totals = {}
+        self.counts = {}
+
+    def span(self, label):
+        torch = self.torch
+        timer = self
+
+        class _Span:
+            def __enter__(self_inner):
+                self_inner.a = torch.cuda.Event(enable_timing=True)
+                self_inner.b = torch.cuda.Event(enable_timing=True)
+                self_inner.a.record()
+
+            def __exit__(self_inner, *exc):
+                self_inner.b.record()
+                timer.pending.append((label, self_inner.a, self_inner.b))
+        return _Span()
+
+    def collect(self):
+        for label, a, b in self.pending:
+            ms = a.elapsed_time(b)
+            self.totals[label] = self.totals.get(label, 0.0) + ms
+            self.counts[label] = self.counts.get(label, 0) + 1
+        self.pending = []
+
+    def avg_ms(self, label):
+        return self.totals[label] / self.counts[label]
+
+    def reset(self):
+        self.pending, self.totals, self.counts = [], {}, {}
+
+
+def dev_bits(torch, bits, in_dtype):
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16))
+    return t.view(torch.bfloat16 if in_dtype == "bf16" else torch.float16).cuda()
+
+
+class Sweep:
+    def __init__(self, torch, mx):
+        self.mx, self.torch = mx, torch
+        self.host, self.x, self.out = {}, {}, {}
+        for in_dtype, fmt in SWEEP_VARIANTS:
+            bits = syn.sweep_input(*SWEEP, in_dtype, fmt, seed=0)
+            self.host[(in_dtype, fmt)] = bits
+            self.x[(in_dtype, fmt)] = dev_bits(torch, bits, in_dtype)
+        for layout in ("plain", "interleave"):
+            for in_dtype, fmt in SWEEP_VARIANTS:
+                cfg = mx.make_cfg("8x4", -2, layout)
+                _, sr, sc = mx.mx_quantize_sizes(*SWEEP, in_dtype, fmt, cfg)
+                self.out[(layout, in_dtype, fmt)] = (
+                    torch.empty(SWEEP[0] * SWEEP[1], dtype=torch.uint8, device="cuda"),
+                    torch.empty(sr * sc, dtype=torch.uint8, device="cuda"))
+        self.launches = 8
+
+    def step(self, timer):
+        # layouts outermost: consecutive launches read different 128 MiB inputs
+        for layout in ("plain", "interleave"):
+            for in_dtype, fmt in SWEEP_VARIANTS:
+                d, s = self.out[(layout, in_dtype, fmt)]
+                with timer.span("sweep"):
+                    self.mx.mx_quantize(self.x[(in_dtype, fmt)], fmt, geometry="8x4", dim=-2,
+                                        scale_layout=layout, out_data=d, out_scale=s)
+
+
+class Gemm:
+    CASES = [("e4m3fn", "bf16"), ("e5m2", "f32")]
+
+    def __init__(self, torch, mx):
+        self.mx, self.torch = mx, torch
+        a_bits, b_bits = syn.gemm_operands(GEMM_N, GEMM_N, GEMM_N, seed=0)
+        self.a = dev_bits(torch, a_bits, "bf16")
+        self.b = dev_bits(torch, b_bits, "bf16")
+        n = GEMM_N
+        self.qa = torch.empty((n, n), dtype=torch.uint8, device="cuda")
+        self.qb = torch.empty((n, n), dtype=torch.uint8, device="cuda")
+        self.sa = torch.empty((n, n // 32), dtype=torch.uint8, device="cuda")
+        self.sb = torch.empty((n, n // 32), dtype=torch.uint8, device="cuda")
+        sfb = mx.mx_sf_layout_bytes(n, n)
+        self.sfa = torch.empty(sfb, dtype=torch.uint8, device="cuda")
+        self.sfb = torch.empty(sfb, dtype=torch.uint8, device="cuda")
+        self.c = {"bf16": torch.empty((n, n), dtype=torch.bfloat16, device="cuda"),
+                  "f32": torch.empty((n, n), dtype=torch.float32, device="cuda")}
+        self.launches = 2 * (2 + 2 + 1)
+
+    def step(self, timer):
+        mx = self.mx
+        for fmt, out in self.CASES:
+            with timer.span("gemm_quantize"):
+                mx.mx_quantize(self.a, fmt, geometry="1x32", dim=-1, out_data=self.qa, out_scale=self.sa)
+                mx.mx_quantize(self.b, fmt, geometry="1x32", dim=-1, out_data=self.qb, out_scale=self.sb)
+            with timer.span("gemm_repack"):
+                mx.mx_repack_scales(self.sa, GEMM_N, out=self.sfa)
+                mx.mx_repack_scales(self.sb, GEMM_N, out=self.sfb)
+            with timer.span(f"gemm_{fmt}_{out}"):
+                mx.mx_scaled_matmul(self.qa, self.qb, self.sfa, self.sfb, fmt, out, scales_are_sf_layout=True,
+                                    out=self.c[out], K=GEMM_N)
+
+
+class Fp4:
+    def __init__(self, torch, mx):
+        self.mx = mx
+        self.x = dev_bits(torch, syn.fp4_input(*FP4_SHAPE, seed=0), "bf16")
+        cfg = mx.make_cfg("8x4", -2, "interleave")
+        db, sr, sc = mx.mx_quantize_sizes(*FP4_SHAPE, "bf16", "e2m1", cfg)
+        self.d = torch.empty(db, dtype=torch.uint8, device="cuda")
+        self.s = torch.empty(sr * sc, dtype=torch.uint8, device="cuda")
+        self.launches = 1
+
+    def step(self, timer):
+        with timer.span("fp4"):
+            self.mx.mx_quantize(self.x, "e2m1", geometry="8x4", dim=-2, scale_layout="interleave",
+                                out_data=self.d, out_scale=self.s)
+
+
+class Fused:
+    def __init__(self, torch, mx):
+        self.mx = mx
+        M, N, K = FUSED
+        x_bits, w_bits = syn.fused_operands(M, N, K, seed=0)
+        self.x = dev_bits(torch, x_bits, "bf16")
+        wt = dev_bits(torch, w_bits, "bf16")
+        del w_bits
+        # offline weight preparation (not timed): QuantizeMX of W along K,
+        # stored K-contiguous with tensor-core layout scales
+        self.wq, self.ws = mx.mx_quantize(wt, "e4m3fn", geometry="1x32", dim=-1, scale_layout="sf")
+        del wt
+        self.c = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        self.work = torch.empty(mx.mx_fused_quantize_matmul_workspace(M, N, K), dtype=torch.uint8, device="cuda")
+        self.launches = 2
+
+    def step(self, timer):
+        with timer.span("fused"):
+            self.mx.mx_fused_quantize_matmul(self.x, self.wq, self.ws, "e4m3fn", "bf16", out=self.c,
+                                             workspace=self.work)
+
+
+# ------------------------------------------------------------- CPU oracle
+
+def oracle_sweep_sample(rows=2048, repeats=1):
+    """The oracle on [rows, 8192] slices of the four sweep inputs, plain and
+    interleaved layouts.  Returns (GB/s over algorithmic bytes, seconds,
+    elements, description)."""
+    import oracle as orc
+    samples = [(i, f, syn.sweep_input(rows, 8192, i, f, seed=0)) for i, f in SWEEP_VARIANTS]
+    t0 = time.perf_counter()
+    nbytes = 0
+    for _ in range(repeats):
+        for layout in ("plain", "interleave"):
+            for in_dtype, fmt, bits in samples:
+                orc.quantize(bits, in_dtype, fmt, geometry="8x4", dim=-2, scale_layout=layout)
+                nbytes += 3 * bits.size + bits.size // 32
+    dt = time.perf_counter() - t0
+    return nbytes / dt / 1e9, dt, 8 * repeats * rows * 8192, \
+        f"8 sweep variants on [{rows}, 8192] slices x {repeats}, single-threaded C oracle"
+
+
+def oracle_gemm_sample(rows=2):
+    """The oracle's binary64 scaled dot on `rows` full output rows of the
+    8192^3 ScaledMatmul (k-ordered sums in C).  Returns TFLOP/s."""
+    import oracle as orc
+    rng = np.random.default_rng(0)
+    K = GEMM_N
+    a = rng.integers(0, 0x7E, size=(rows, K)).astype(np.uint8)
+    bt = rng.integers(0, 0x7E, size=(GEMM_N, K)).astype(np.uint8)
+    sa = np.full((rows, K // 32), 127, np.uint8)
+    sb = np.full((GEMM_N, K // 32), 127, np.uint8)
+    ms, ns = [v.reshape(-1) for v in np.meshgrid(np.arange(rows), np.arange(GEMM_N), indexing="ij")]
+    t0 = time.perf_counter()
+    orc.scaled_matmul_entries(a, bt, sa, sb, "e4m3fn", "e4m3fn", ms, ns)
+    dt = time.perf_counter() - t0
+    return 2.0 * rows * GEMM_N * K / dt / 1e12, dt
+
+
+# ------------------------------------------------------------------- main
+
+def dist_setup():
+    import torch
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(ws, value):
+    if ws == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(ws, value):
+    if ws == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def run_reference(args):
+    ws, rank, _ = int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")), 0
+    if rank != 0:
+        return
+    rows = 1024
+    vals = []
+    for _ in range(args.warmup):
+        oracle_sweep_sample(rows=rows)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        v, dt, n, desc = oracle_sweep_sample(rows=rows)
+        vals.append(v)
+    total = time.perf_counter() - t0
+    value = statistics.median(vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * total / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
+        "config": {"workload": "QuantizeMX sweep [8192,8192] {bf16,f16}x{e4m3fn,e5m2}x{plain,interleave}, 8x4 "
+                               "blocks, dim=-2", "sample": f"[{rows}, 8192] slice per variant"},
+        "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="mx", choices=["mx", "reference"])
+    ap.add_argument("--workload", default="all", choices=["all", "sweep", "gemm", "fp4", "fused"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    if args.impl == "reference":
+        run_reference(args)
+        return
+
+    import torch
+    ws, rank, local = dist_setup()
+    torch.cuda.set_device(local)
+    import mx_fp8_microscaling_gb300 as mx
+
+    peaks = load_peaks()
+    parts = {}
+    want = ["sweep", "gemm", "fp4", "fused"] if args.workload == "all" else [args.workload]
+    builders = {"sweep": Sweep, "gemm": Gemm, "fp4": Fp4, "fused": Fused}
+    for name in want:
+        parts[name] = builders[name](torch, mx)
+    torch.cuda.synchronize()
+    launches_per_step = sum(p.launches for p in parts.values())
+
+    timer = Timer(torch)
+    for _ in range(args.warmup):
+        for p in parts.values():
+            p.step(timer)
+    torch.cuda.synchronize()
+    timer.collect()
+    timer.reset()
+    assert mx.mx_get_device_status() == 0
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.4)
+    barrier(ws)
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record()
+    for _ in range(args.steps):
+        for p in parts.values():
+            p.step(timer)
+    t_end.record()
+    torch.cuda.synchronize()
+    barrier(ws)
+    clocks = sampler.stop()
+    timer.collect()
+    status = mx.mx_get_device_status()
+    if status != 0:
+        raise SystemExit(f"device status {status} after the timed region")
+    total_ms = max_over_ranks(ws, t_start.elapsed_time(t_end))
+
+    line = {"metric": METRIC, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "u8", "data": "synthetic (seeded; distributions of the workload "
+            "descriptions)", "gpu_launches": launches_per_step * args.steps, "clocks": clocks}
+
+    if "sweep" in parts:
+        sweep_ms = max_over_ranks(ws, timer.totals["sweep"])
+        n_launch = timer.counts["sweep"]
+        value = sum_over_ranks(ws, SWEEP_BYTES * n_launch) / (sweep_ms * 1e-3) / 1e9
+        achieved = SWEEP_BYTES / (timer.avg_ms("sweep") * 1e-3) / 1e9
+        line.update({"value": round(value, 2), "unit": "GB/s",
+                     "config": {"workload": "QuantizeMX sweep [8192,8192] {bf16,f16}x{e4m3fn,e5m2}x"
+                                            "{plain,interleave}, 8x4 blocks, dim=-2",
+                                "bytes_per_launch": SWEEP_BYTES, "launches_per_step": 8,
+                                "l2": "inputs (128 MiB each, 4 distinct) larger than L2 and rotated",
+                                "parallelism": f"replicas x{ws}"},
+                     "roofline": {"bound": "hbm", "kernel": "quant_g84", "achieved": round(achieved, 1),
+                                  "peak": peaks["hbm"], "unit": "GB/s",
+                                  "frac": round(achieved / peaks["hbm"], 4), "peak_source": peaks["src"],
+                                  "traffic": profiled_traffic("quant_g84", source_hash("quantize.cu"))}})
+    else:
+        line.update({"value": None, "unit": None, "config": {"workload": args.workload}})
+
+    if "gemm" in parts:
+        g = {}
+        peak_fp8 = peaks["bf16"] * FP8_OVER_BF16
+        for fmt, out in Gemm.CASES:
+            ms = timer.avg_ms(f"gemm_{fmt}_{out}")
+            tf = GEMM_FLOP / (ms * 1e-3) / 1e12
+            g[f"{fmt}_{out}"] = {"tflops": round(tf, 1), "ms": round(ms, 4)}
+        avg = statistics.mean(v["tflops"] for v in g.values())
+        pipe_ms = (timer.totals["gemm_quantize"] + timer.totals["gemm_repack"]
+                   + sum(timer.totals[f"gemm_{f}_{o}"] for f, o in Gemm.CASES)) / args.steps / 2
+        line["scaled_matmul"] = {
+            "value": round(avg, 1), "unit": "TFLOP/s", "config": "M=N=K=8192, E8M0 per 32 along K",
+            "cases": g, "pipeline_tflops_incl_quantize_repack": round(GEMM_FLOP / (pipe_ms * 1e-3) / 1e12, 1),
+            "quantize_operands_ms": round(timer.totals["gemm_quantize"] / timer.counts["gemm_quantize"], 4),
+            "repack_ms": round(timer.totals["gemm_repack"] / timer.counts["gemm_repack"], 4),
+            "roofline": {"bound": "tensor", "kernel": "mx_gemm_kernel", "achieved": round(avg, 1),
+                         "peak": round(peak_fp8, 1), "unit": "TFLOP/s", "frac": round(avg / peak_fp8, 4),
+                         "peak_source": f"{peaks['src']} bf16 burst x {FP8_OVER_BF16} (nominal MXFP8/bf16)",
+                         "traffic": profiled_traffic("mx_gemm_kernel", source_hash("gemm.cu"))}}
+    if "fp4" in parts:
+        ms = timer.avg_ms("fp4")
+        gbs = FP4_BYTES / (ms * 1e-3) / 1e9
+        line["fp4_quantize"] = {"value": round(gbs, 1), "unit": "GB/s", "ms": round(ms, 4),
+                                "config": "[16384,16384] bf16 -> e2m1, 8x4, interleaved scales",
+                                "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm"],
+                                             "unit": "GB/s", "frac": round(gbs / peaks["hbm"], 4),
+                                             "peak_source": peaks["src"]}}
+    if "fused" in parts:
+        ms = timer.avg_ms("fused")
+        tf = FUSED_FLOP / (ms * 1e-3) / 1e12
+        peak_fp8 = peaks["bf16"] * FP8_OVER_BF16
+        line["fused"] = {"value": round(tf, 1), "unit": "TFLOP/s", "ms": round(ms, 4),
+                         "config": "X[16384,8192] bf16 -> e4m3fn (1x32 along K) x W[8192,28672] e4m3fn -> bf16",
+                         "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": round(peak_fp8, 1),
+                                      "unit": "TFLOP/s", "frac": round(tf / peak_fp8, 4),
+                                      "peak_source": f"{peaks['src']} bf16 burst x {FP8_OVER_BF16}"}}
+
+    # end to end through the public API with host buffers: pinned host input
+    # -> device, QuantizeMX, data and scales -> pinned host, every step
+    if "sweep" in parts:
+        sw = parts["sweep"]
+        host_in = {k: torch.from_numpy(v.view(np.int16)).pin_memory() for k, v in sw.host.items()}
+        host_out = {k: (torch.empty(d.numel(), dtype=torch.uint8).pin_memory(),
+                        torch.empty(s.numel(), dtype=torch.uint8).pin_memory()) for k, (d, s) in sw.out.items()}
+        h2d = d2h = 0
+
+        def e2e_step():
+            nonlocal h2d, d2h
+            for layout in ("plain", "interleave"):
+                for in_dtype, fmt in SWEEP_VARIANTS:
+                    xin = sw.x[(in_dtype, fmt)]
+                    xin.view(torch.int16).copy_(host_in[(in_dtype, fmt)], non_blocking=True)
+                    d, s = sw.out[(layout, in_dtype, fmt)]
+                    mx.mx_quantize(xin, fmt, geometry="8x4", dim=-2, scale_layout=layout, out_data=d,
+                                   out_scale=s)
+                    hd, hs = host_out[(layout, in_dtype, fmt)]
+                    hd.copy_(d, non_blocking=True)
+                    hs.copy_(s, non_blocking=True)
+                    h2d += xin.numel() * 2
+                    d2h += d.numel() + s.numel()
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        h2d = d2h = 0
+        barrier(ws)
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            e2e_step()
+        torch.cuda.synchronize()
+        dt = max_over_ranks(ws, time.perf_counter() - t0)
+        e2e_value = sum_over_ranks(ws, SWEEP_BYTES * 8 * args.steps) / dt / 1e9
+        line["e2e"] = {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d // args.steps,
+                       "d2h_bytes_per_step": d2h // args.steps,
+                       "note": "pinned host -> device copy, QuantizeMX, data+scales -> pinned host, per launch"}
+
+    if rank == 0 and not args.no_cpu_baseline:
+        v, dt, n, desc = oracle_sweep_sample(rows=2048)
+        line["cpu_baseline"] = {"value": round(v, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                                "sample": desc, "seconds": round(dt, 2)}
+        if "gemm" in parts:
+            tf, dtg = oracle_gemm_sample(rows=2)
+            line["cpu_baseline"]["scaled_matmul"] = {"value": round(tf, 6), "unit": "TFLOP/s", "cores": 1,
+                                                     "sample": "2 full output rows of the 8192^3 product, "
+                                                               "binary64 k-ordered sums",
+                                                     "seconds": round(dtg, 2)}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

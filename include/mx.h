@@ -1,0 +1,268 @@
+/*
+ * mx.h -- libmx: OCP-MX microscaling on one GB300 GPU (sm_103a).
+ *
+ * Two operations, as the pages "MX-FP8 Microscaling Legalization" (sections 2-4,
+ * the QuantizeMX and ScaledMatmul custom-call contracts) and "MX Microscaling:
+ * Quantize, Block-Scaling and E8M0" (the numeric model) define them:
+ *
+ *   QuantizeMX    bf16/f16 tensor -> {FP8 e4m3fn/e5m2 or FP4 e2m1 data,
+ *                 one E8M0 scale per 32-element block}, scale method EMAX.
+ *   ScaledMatmul  block_scaled_dot(lhs, rhs, lhs_scale, rhs_scale) -> f32/bf16.
+ *
+ * Conventions for every call below:
+ *   - Pointers named `in`, `out`, `a`, `bt`, `c`, `*_scale`, `workspace` are
+ *     DEVICE pointers (memory of the current CUDA device).  The caller owns and
+ *     allocates every buffer; the library allocates nothing.
+ *   - 2-D tensors are row-major.  `ld_*` is the row pitch in elements of the
+ *     tensor's own type.  Each call states its alignment needs; where a pointer
+ *     only needs element alignment, 16-byte aligned rows select the faster
+ *     vectorised kernels.
+ *   - All calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *     default stream).  Argument errors are returned synchronously and launch
+ *     nothing.  Errors inside a kernel (a bounded wait that gave up) are
+ *     recorded in a per-device status word, read by mx_get_device_status().
+ *   - The current device must be compute capability 10.3 (sm_103a);
+ *     otherwise calls return MX_ERR_DEVICE.
+ *   - Calls are thread-safe with respect to each other; concurrent calls that
+ *     write the same output buffer race, as any two kernels would.
+ */
+#ifndef MX_H_
+#define MX_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t, declared here so C callers need no CUDA header. */
+typedef struct CUstream_st* mx_stream;
+
+typedef enum mx_status {
+    MX_OK = 0,
+    MX_ERR_INVALID_ARG = 1,       /* NULL pointer, negative size, unknown enum value, pitch < width */
+    MX_ERR_UNSUPPORTED_DTYPE = 2, /* dtype combination outside the dispatch matrix */
+    MX_ERR_BLOCK_SIZE = 3,        /* block_size other than 32 (0 selects 32) */
+    MX_ERR_DIM = 4,               /* dim other than -1 / -2 (or 1 / 0 for a 2-D tensor) */
+    MX_ERR_SHAPE = 5,             /* extents not divisible by the block / the x4 container */
+    MX_ERR_ALIGNMENT = 6,         /* pointer or pitch not 16-byte aligned */
+    MX_ERR_WORKSPACE = 7,         /* workspace missing or too small */
+    MX_ERR_CUDA = 8,              /* a CUDA runtime call or launch failed */
+    MX_ERR_TIMEOUT = 9,           /* a bounded device-side wait gave up (device status word) */
+    MX_ERR_DEVICE = 10,           /* current device is not sm_103a */
+    MX_ERR_SCALE_METHOD = 11      /* scale_method other than EMAX */
+} mx_status;
+
+typedef enum mx_dtype {
+    MX_BF16 = 1,
+    MX_F16 = 2,
+    MX_F32 = 3,
+    MX_E4M3FN = 4, /* OCP float8_e4m3fn: 1.4.3, bias 7, max 448, no Inf */
+    MX_E5M2 = 5,   /* OCP float8_e5m2: 1.5.2, bias 15, max 57344 */
+    MX_E2M1 = 6,   /* OCP float4_e2m1fn: 1.2.1, bias 1, max 6, finite only */
+    MX_E8M0 = 7    /* OCP float8_e8m0fnu: 2^(E-127), 0xFF = NaN */
+} mx_dtype;
+
+/* Block geometry of QuantizeMX (32 elements per block either way). */
+enum {
+    MX_GEOM_8X4 = 0,  /* 8 along the `dim` axis x 4 along the other axis: the
+                         page's 8-partition x 4-column block ("Block geometry",
+                         scale [P//8, F//4]) */
+    MX_GEOM_1X32 = 1  /* 32 consecutive elements along `dim` (HLO block_size
+                         along dim, QuantizeMX backend_config) */
+};
+
+/* Scale tensor layout. */
+enum {
+    MX_SCALE_PLAIN = 0,        /* row-major [scale_rows, scale_cols] */
+    MX_SCALE_INTERLEAVE32 = 1, /* scale row i stored at buffer row (i & 3) + 32 * (i >> 2)
+                                  (page "MX Microscaling", section "E8M0 Scale-Tensor
+                                  Layout"); buffer rows = 32 * ceil(scale_rows / 4);
+                                  rows never addressed are not written */
+    MX_SCALE_TC_SF = 2         /* the tensor-core scale-factor layout of mx_repack_scales,
+                                  written directly (1x32 blocks along dim=-1 only); the
+                                  buffer holds mx_sf_layout_bytes(rows, cols) bytes and its
+                                  padding is written as 0.  No counterpart on the pages:
+                                  it lets an activation feed mx_scaled_matmul with no
+                                  repack */
+};
+
+enum { MX_SCALE_METHOD_EMAX = 0 };
+
+/*
+ * QuantizeMX configuration: the backend_config fields {dtype, dim,
+ * block_size, scale_method} of the page "MX-FP8 Microscaling Legalization",
+ * section 4.1, plus the layout choices of the numeric page.
+ */
+typedef struct mx_quant_cfg {
+    int32_t geometry;          /* MX_GEOM_8X4 | MX_GEOM_1X32 */
+    int32_t scale_layout;      /* MX_SCALE_PLAIN | MX_SCALE_INTERLEAVE32 | MX_SCALE_TC_SF */
+    int32_t block_size;        /* must be 32; 0 selects the default 32 (section 2.2) */
+    int32_t dim;               /* -1 (last) or -2 (second-to-last); 1 / 0 are folded to
+                                  -1 / -2 for the 2-D view (section 2.3) */
+    int32_t scale_method;      /* MX_SCALE_METHOD_EMAX only */
+    int32_t fp4_lane_stride;   /* e2m1 packing: 0 (no lane permutation), 1, 2 or 4.
+                                  The page's lane_remap reverses each window of
+                                  2*stride nibbles.  Default 2. */
+    int32_t fp4_nibble_parity; /* e2m1 packing: 0 puts even permuted indices in the
+                                  high nibble (default), 1 the low nibble */
+    int32_t emax_alt;          /* 0: E8M0 measured against EMAX (default);
+                                  1: against EMAX-1 (the page's alternative mode) */
+} mx_quant_cfg;
+
+/* Fill `cfg` with the defaults: 8x4, plain scales, block 32, dim -2, EMAX,
+ * FP4 stride 2 / parity 0, emax_alt 0.  Returns MX_ERR_INVALID_ARG on NULL. */
+mx_status mx_quant_cfg_default(mx_quant_cfg* cfg);
+
+/*
+ * Sizes of QuantizeMX outputs for a [rows, cols] input.
+ *   data_bytes   dense row-major data: rows*cols bytes (FP8, one byte per
+ *                element; four consecutive bytes form the page's x4 U32
+ *                container) or rows*cols/2 bytes (e2m1, two nibbles per byte).
+ *   scale_rows   rows of the scale BUFFER (interleaved layout: 32*ceil(r/4);
+ *                MX_SCALE_TC_SF: rows rounded up to 128).
+ *   scale_cols   columns of the scale tensor (MX_SCALE_TC_SF: rounded up to 4).
+ *   scale_bytes  scale_rows * scale_cols.
+ * Scale tensor shape: the data shape with each axis divided by the block's
+ * extent along it (8x4 dim=-2: [rows/8, cols/4]; 8x4 dim=-1: [rows/4, cols/8];
+ * 1x32 dim=-1: [rows, cols/32]; 1x32 dim=-2: [rows/32, cols]).
+ * Any output pointer may be NULL.  Same argument checks as mx_quantize.
+ */
+mx_status mx_quantize_sizes(mx_dtype in_dtype, mx_dtype out_dtype, int64_t rows, int64_t cols,
+                            const mx_quant_cfg* cfg, size_t* data_bytes, int64_t* scale_rows,
+                            int64_t* scale_cols, size_t* scale_bytes);
+
+/*
+ * QuantizeMX (page "MX Microscaling: Quantize, Block-Scaling and E8M0",
+ * sections "Block-Scale Computation" and "Round-to-Grid"): for each 32-element
+ * block, E8M0 = max(1, max(0, maxExp - EMAX)) where maxExp is the largest
+ * binary32 exponent byte in the block (EMAX: e2m1 2, e4m3fn 8, e5m2 15); each
+ * element is multiplied by 2^(127 - E8M0) in binary32 and rounded to nearest
+ * (ties to even), saturating at the format maximum.  NaN inputs become
+ * 0x7F|sign (FP8) or a signed zero nibble (e2m1); Inf saturates.
+ *
+ *   in         device, [rows, ld_in] bf16/f16, 2-byte aligned, ld_in >= cols
+ *              (16-byte aligned rows with cols % 8 == 0 take the vectorised
+ *              kernels; anything else a scalar kernel with the same results)
+ *   in_dtype   MX_BF16 | MX_F16
+ *   rows, cols logical extents (>= 0); cols % 4 == 0 (x4 container); rows and
+ *              cols divisible by the block extents
+ *   out_dtype  MX_E4M3FN | MX_E5M2 | MX_E2M1
+ *   cfg        NULL selects the defaults of mx_quant_cfg_default
+ *   out_data   device, data_bytes (see mx_quantize_sizes), dense, 2-byte aligned
+ *   out_scale  device, scale_bytes; interleaved layout leaves unaddressed rows
+ *              untouched
+ * e2m1 with lane stride s > 1 also needs cols % (2*s) == 0.
+ * Returns MX_OK after the launch (asynchronous) or an argument error.
+ */
+mx_status mx_quantize(const void* in, mx_dtype in_dtype, int64_t rows, int64_t cols, int64_t ld_in,
+                      mx_dtype out_dtype, const mx_quant_cfg* cfg, void* out_data, void* out_scale,
+                      mx_stream stream);
+
+/*
+ * Bytes of the tensor-core scale-factor ("SF") layout for an operand of `mn`
+ * rows and K = `k` elements per row (k % 32 == 0): the E8M0 matrix
+ * [mn, k/32] padded to 128-row x 4-column tiles of 512 bytes,
+ * ceil(mn/128) * ceil(k/128) * 512.  The layout is that of the block-scaled
+ * tcgen05 MMA (PTX ISA, tcgen05 "scale factor" matrices; also cuBLASLt's
+ * 1-D block-scaling layout); the pages have no counterpart.
+ */
+mx_status mx_sf_layout_bytes(int64_t mn, int64_t k, size_t* bytes);
+
+/*
+ * Repack plain E8M0 scales [mn, k/32] (row pitch ld_plain bytes) into the SF
+ * layout: tile (t_mn, t_k) = rows 128*t_mn.., scale columns 4*t_k.. is 512
+ * contiguous bytes at ((t_mn * ceil(k/128)) + t_k) * 512, and inside a tile
+ * scale (r, c) sits at byte (r % 32) * 16 + (r / 32) * 4 + c.  Padding bytes
+ * are written as 0 (2^-127).  `plain` and `sf` are device pointers; `sf`
+ * holds mx_sf_layout_bytes bytes.
+ */
+mx_status mx_repack_scales(const uint8_t* plain, int64_t mn, int64_t k, int64_t ld_plain,
+                           uint8_t* sf, mx_stream stream);
+
+/*
+ * Workspace bytes mx_scaled_matmul needs: with plain scales, room for both
+ * operands' SF-layout scales (16-byte aligned); with SF-layout scales, 0.
+ */
+mx_status mx_scaled_matmul_workspace(int64_t M, int64_t N, int64_t K, int scales_are_sf_layout,
+                                     size_t* bytes);
+
+/*
+ * ScaledMatmul, block_scaled_dot(lhs, rhs, lhs_scale, rhs_scale) of the page
+ * "MX-FP8 Microscaling Legalization" (sections 3 and 4.2; the scales are
+ * bound by position), for the 2-D case with both operands contiguous along K:
+ *
+ *   C[m,n] = sum_k dec(A[m,k]) 2^(sA[m,k/32]-127) * dec(Bt[n,k]) 2^(sB[n,k/32]-127)
+ *
+ * accumulated in f32 on the tensor cores, written as f32 or bf16
+ * (round to nearest even).
+ *   a, bt        device FP8 codes, A [M, K] and Bt [N, K] (= rhs^T), dense,
+ *                16-byte aligned; both of `elem_dtype`
+ *   a_scale,     device E8M0: plain [M, K/32] / [N, K/32] dense row-major
+ *   b_scale      (scales_are_sf_layout = 0), or already in the SF layout of
+ *                mx_repack_scales (scales_are_sf_layout = 1)
+ *   elem_dtype   MX_E4M3FN | MX_E5M2 (ScaledMatmul_e4m3fn_e4m3fn_* /
+ *                ScaledMatmul_e5m2_e5m2_*)
+ *   M, N, K      M, N >= 1; K >= 32 and K % 32 == 0
+ *   out_dtype    MX_F32 | MX_BF16
+ *   c, ldc       device [M, ldc] output, ldc >= N, element aligned (16-byte
+ *                aligned rows use vector stores)
+ *   workspace    device scratch of mx_scaled_matmul_workspace bytes (may be
+ *                NULL when that is 0); contents are overwritten
+ */
+mx_status mx_scaled_matmul(const void* a, const void* bt, const uint8_t* a_scale,
+                           const uint8_t* b_scale, int scales_are_sf_layout, mx_dtype elem_dtype,
+                           int64_t M, int64_t N, int64_t K, mx_dtype out_dtype, void* c,
+                           int64_t ldc, void* workspace, size_t workspace_bytes, mx_stream stream);
+
+/*
+ * Workspace bytes of mx_fused_quantize_matmul: the quantized activation
+ * (M*K bytes) and its SF-layout scales, each 16-byte aligned.
+ */
+mx_status mx_fused_quantize_matmul_workspace(int64_t M, int64_t N, int64_t K, size_t* bytes);
+
+/*
+ * Activation quantize fused with ScaledMatmul (page "MX-FP8 Microscaling
+ * Legalization", section 4.3: QuantizeMX feeds ScaledMatmul by dataflow):
+ * X [M, K] bf16/f16 is quantized along K (1x32 blocks, EMAX) to `elem_dtype`
+ * and multiplied by a pre-quantized weight given K-contiguous as
+ * Wt [N, K] with SF-layout scales.  The result equals QuantizeMX(X) followed
+ * by mx_scaled_matmul bit for bit in the quantized operand.
+ *   x, x_dtype   device [M, ld_x] MX_BF16 | MX_F16
+ *   wt, w_scale_sf  device FP8 [N, K] and SF-layout scales (mx_repack_scales)
+ *   other arguments as mx_scaled_matmul; workspace per
+ *   mx_fused_quantize_matmul_workspace.
+ */
+mx_status mx_fused_quantize_matmul(const void* x, mx_dtype x_dtype, int64_t ld_x, const void* wt,
+                                   const uint8_t* w_scale_sf, mx_dtype elem_dtype, int64_t M,
+                                   int64_t N, int64_t K, mx_dtype out_dtype, void* c, int64_t ldc,
+                                   void* workspace, size_t workspace_bytes, mx_stream stream);
+
+/*
+ * Read and clear the current device's status word (synchronises the device).
+ * *status receives MX_OK or the first device-side error recorded since the
+ * last read (MX_ERR_TIMEOUT when a bounded wait gave up).
+ */
+mx_status mx_get_device_status(int* status);
+
+/* Static description of a status code; never NULL. */
+const char* mx_status_string(mx_status status);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int mx_version(void);
+
+/*
+ * Testing hook for the bounded-wait path (no counterpart on the pages).
+ * skip_producer = 1 makes later mx_scaled_matmul launches issue no loads, so
+ * their waits run out after `timeout_ns` (0 = the default of 2 s) and record
+ * MX_ERR_TIMEOUT in the device status word, with no fault and no hang.
+ * skip_producer = 0 restores normal operation.  Not thread-safe; host only.
+ */
+mx_status mx_debug_gemm_fault_injection(int skip_producer, uint64_t timeout_ns);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MX_H_ */

@@ -1,0 +1,269 @@
+"""Python binding of libmx (OCP-MX microscaling on sm_103a).
+
+Argument marshalling only: every computation runs in the CUDA kernels of
+``libmx.so`` (built in-tree by ``build.py``).  Tensors are PyTorch CUDA
+tensors; PyTorch supplies device memory and the current stream.  Importing
+this package raises if the library has not been built: there is no fallback.
+
+The functions carry the C-ABI names of ``include/mx.h``:
+
+    mx_quantize(x, out_dtype, ...)            -> (data, scale)
+    mx_quantize_sizes(...)                    -> (data_bytes, scale_rows, scale_cols)
+    mx_repack_scales(plain, k)                -> sf
+    mx_sf_layout_bytes(mn, k)                 -> int
+    mx_scaled_matmul(a, bt, a_scale, b_scale, ...) -> c
+    mx_fused_quantize_matmul(x, wt, w_scale_sf, ...) -> c
+    mx_get_device_status()                    -> int
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_build", "libmx.so")
+
+# enum values of include/mx.h
+MX_OK = 0
+MX_ERR_TIMEOUT = 9
+DTYPES = {"bf16": 1, "f16": 2, "f32": 3, "e4m3fn": 4, "e5m2": 5, "e2m1": 6, "e8m0": 7}
+GEOMETRIES = {"8x4": 0, "1x32": 1}
+LAYOUTS = {"plain": 0, "interleave": 1, "sf": 2}
+STATUS_NAMES = {0: "MX_OK", 1: "MX_ERR_INVALID_ARG", 2: "MX_ERR_UNSUPPORTED_DTYPE", 3: "MX_ERR_BLOCK_SIZE",
+                4: "MX_ERR_DIM", 5: "MX_ERR_SHAPE", 6: "MX_ERR_ALIGNMENT", 7: "MX_ERR_WORKSPACE",
+                8: "MX_ERR_CUDA", 9: "MX_ERR_TIMEOUT", 10: "MX_ERR_DEVICE", 11: "MX_ERR_SCALE_METHOD"}
+
+
+class MxError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {STATUS_NAMES.get(status, status)}")
+        self.status = status
+
+
+class QuantCfg(ctypes.Structure):
+    _fields_ = [("geometry", ctypes.c_int32), ("scale_layout", ctypes.c_int32),
+                ("block_size", ctypes.c_int32), ("dim", ctypes.c_int32),
+                ("scale_method", ctypes.c_int32), ("fp4_lane_stride", ctypes.c_int32),
+                ("fp4_nibble_parity", ctypes.c_int32), ("emax_alt", ctypes.c_int32)]
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"libmx is not built ({LIB_PATH} missing); run "
+                          "`python -c 'import __graft_entry__ as g; g.build()'`")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I64, I, SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
+    PS = ctypes.POINTER(SZ)
+    PI64 = ctypes.POINTER(I64)
+    sigs = {
+        "mx_quant_cfg_default": [ctypes.POINTER(QuantCfg)],
+        "mx_quantize_sizes": [I, I, I64, I64, ctypes.POINTER(QuantCfg), PS, PI64, PI64, PS],
+        "mx_quantize": [P, I, I64, I64, I64, I, ctypes.POINTER(QuantCfg), P, P, P],
+        "mx_sf_layout_bytes": [I64, I64, PS],
+        "mx_repack_scales": [P, I64, I64, I64, P, P],
+        "mx_scaled_matmul_workspace": [I64, I64, I64, I, PS],
+        "mx_scaled_matmul": [P, P, P, P, I, I, I64, I64, I64, I, P, I64, P, SZ, P],
+        "mx_fused_quantize_matmul_workspace": [I64, I64, I64, PS],
+        "mx_fused_quantize_matmul": [P, I, I64, P, P, I, I64, I64, I64, I, P, I64, P, SZ, P],
+        "mx_get_device_status": [ctypes.POINTER(I)],
+        "mx_status_string": [I],
+        "mx_version": [],
+        "mx_debug_gemm_fault_injection": [I, ctypes.c_uint64],
+    }
+    for name, args in sigs.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = ctypes.c_char_p if name == "mx_status_string" else I
+    return lib
+
+
+_lib = _load()
+
+
+def _check(status: int, what: str):
+    if status != MX_OK:
+        raise MxError(status, what)
+
+
+def _stream(stream=None) -> ctypes.c_void_p:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dev_ptr(t: torch.Tensor | None):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("libmx takes CUDA tensors")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _in_dtype(t: torch.Tensor) -> str:
+    if t.dtype == torch.bfloat16:
+        return "bf16"
+    if t.dtype == torch.float16:
+        return "f16"
+    raise ValueError(f"QuantizeMX input must be bf16 or f16, got {t.dtype}")
+
+
+def make_cfg(geometry="8x4", dim=-2, scale_layout="plain", fp4_lane_stride=2, fp4_nibble_parity=0,
+             emax_alt=False, block_size=32, scale_method=0) -> QuantCfg:
+    cfg = QuantCfg()
+    _lib.mx_quant_cfg_default(ctypes.byref(cfg))
+    cfg.geometry = GEOMETRIES[geometry] if isinstance(geometry, str) else geometry
+    cfg.scale_layout = LAYOUTS[scale_layout] if isinstance(scale_layout, str) else scale_layout
+    cfg.block_size = block_size
+    cfg.dim = dim
+    cfg.scale_method = scale_method
+    cfg.fp4_lane_stride = fp4_lane_stride
+    cfg.fp4_nibble_parity = fp4_nibble_parity
+    cfg.emax_alt = int(emax_alt)
+    return cfg
+
+
+def _view2d(x: torch.Tensor, dim: int) -> tuple[int, int, int]:
+    """Rows, cols and row pitch of the 2-D view of x: leading dimensions fold
+    into rows (the last dimension must be contiguous)."""
+    if x.dim() < 2:
+        raise ValueError("QuantizeMX needs rank >= 2")
+    if x.stride(-1) != 1:
+        raise ValueError("the last dimension must be contiguous")
+    cols = x.shape[-1]
+    rows = 1
+    for s in x.shape[:-1]:
+        rows *= s
+    ld = x.stride(-2) if x.dim() >= 2 else cols
+    # leading dims must be dense over rows for the folded view
+    expect = ld * x.shape[-2]
+    for i in range(x.dim() - 3, -1, -1):
+        if x.shape[i] > 1 and x.stride(i) != expect:
+            raise ValueError("leading dimensions must fold into rows with a single pitch")
+        expect *= x.shape[i]
+    return rows, cols, ld
+
+
+def mx_quantize_sizes(rows: int, cols: int, in_dtype="bf16", out_dtype="e4m3fn", cfg: QuantCfg | None = None):
+    db, sr, sc, sbytes = ctypes.c_size_t(), ctypes.c_int64(), ctypes.c_int64(), ctypes.c_size_t()
+    _check(_lib.mx_quantize_sizes(DTYPES[in_dtype], DTYPES[out_dtype], rows, cols,
+                                  ctypes.byref(cfg) if cfg is not None else None, ctypes.byref(db),
+                                  ctypes.byref(sr), ctypes.byref(sc), ctypes.byref(sbytes)),
+           "mx_quantize_sizes")
+    return db.value, sr.value, sc.value
+
+
+def mx_quantize(x: torch.Tensor, out_dtype: str = "e4m3fn", *, geometry="8x4", dim=-2, scale_layout="plain",
+                fp4_lane_stride=2, fp4_nibble_parity=0, emax_alt=False, block_size=32, scale_method=0,
+                out_data: torch.Tensor | None = None, out_scale: torch.Tensor | None = None, stream=None):
+    """QuantizeMX of x (bf16/f16, CUDA).  Returns (data, scale) uint8 tensors:
+    data [rows, cols] (FP8) or [rows, cols/2] (e2m1) over the folded 2-D view,
+    scale [buffer rows, scale cols].  Pre-allocated outputs may be passed."""
+    in_dtype = _in_dtype(x)
+    rows, cols, ld = _view2d(x, dim)
+    cfg = make_cfg(geometry, dim, scale_layout, fp4_lane_stride, fp4_nibble_parity, emax_alt, block_size,
+                   scale_method)
+    data_bytes, srows, scols = mx_quantize_sizes(rows, cols, in_dtype, out_dtype, cfg)
+    if out_data is None:
+        out_data = torch.empty((rows, cols // 2 if out_dtype == "e2m1" else cols), dtype=torch.uint8,
+                               device=x.device)
+    if out_scale is None:
+        out_scale = torch.empty((srows, scols), dtype=torch.uint8, device=x.device)
+    if out_data.numel() < data_bytes or out_scale.numel() < srows * scols:
+        raise ValueError("output buffer too small")
+    _check(_lib.mx_quantize(_dev_ptr(x), DTYPES[in_dtype], rows, cols, ld, DTYPES[out_dtype],
+                            ctypes.byref(cfg), _dev_ptr(out_data), _dev_ptr(out_scale), _stream(stream)),
+           "mx_quantize")
+    return out_data, out_scale
+
+
+def mx_sf_layout_bytes(mn: int, k: int) -> int:
+    n = ctypes.c_size_t()
+    _check(_lib.mx_sf_layout_bytes(mn, k, ctypes.byref(n)), "mx_sf_layout_bytes")
+    return n.value
+
+
+def mx_repack_scales(plain: torch.Tensor, k: int, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Plain E8M0 scales [mn, k/32] -> tensor-core SF layout (uint8, flat)."""
+    mn = plain.shape[0]
+    if out is None:
+        out = torch.empty(mx_sf_layout_bytes(mn, k), dtype=torch.uint8, device=plain.device)
+    _check(_lib.mx_repack_scales(_dev_ptr(plain), mn, k, plain.stride(0), _dev_ptr(out), _stream(stream)),
+           "mx_repack_scales")
+    return out
+
+
+def mx_scaled_matmul_workspace(M: int, N: int, K: int, scales_are_sf_layout: bool = False) -> int:
+    n = ctypes.c_size_t()
+    _check(_lib.mx_scaled_matmul_workspace(M, N, K, int(scales_are_sf_layout), ctypes.byref(n)),
+           "mx_scaled_matmul_workspace")
+    return n.value
+
+
+def mx_scaled_matmul(a: torch.Tensor, bt: torch.Tensor, a_scale: torch.Tensor, b_scale: torch.Tensor,
+                     elem_dtype: str = "e4m3fn", out_dtype: str = "f32", *, scales_are_sf_layout: bool = False,
+                     out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                     K: int | None = None, stream=None) -> torch.Tensor:
+    """C = ScaledMatmul(A [M,K], Bt [N,K]) with E8M0 scales, f32 or bf16 out."""
+    M, Kb = a.shape
+    N = bt.shape[0]
+    K = Kb if K is None else K
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32 if out_dtype == "f32" else torch.bfloat16, device=a.device)
+    ws_bytes = mx_scaled_matmul_workspace(M, N, K, scales_are_sf_layout)
+    if ws_bytes and workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=a.device)
+    _check(_lib.mx_scaled_matmul(_dev_ptr(a), _dev_ptr(bt), _dev_ptr(a_scale), _dev_ptr(b_scale),
+                                 int(scales_are_sf_layout), DTYPES[elem_dtype], M, N, K, DTYPES[out_dtype],
+                                 _dev_ptr(out), out.stride(0), _dev_ptr(workspace),
+                                 workspace.numel() if workspace is not None else 0, _stream(stream)),
+           "mx_scaled_matmul")
+    return out
+
+
+def mx_fused_quantize_matmul_workspace(M: int, N: int, K: int) -> int:
+    n = ctypes.c_size_t()
+    _check(_lib.mx_fused_quantize_matmul_workspace(M, N, K, ctypes.byref(n)), "mx_fused_quantize_matmul_workspace")
+    return n.value
+
+
+def mx_fused_quantize_matmul(x: torch.Tensor, wt: torch.Tensor, w_scale_sf: torch.Tensor,
+                             elem_dtype: str = "e4m3fn", out_dtype: str = "bf16", *,
+                             out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                             stream=None) -> torch.Tensor:
+    """QuantizeMX(x along K) fused with ScaledMatmul against Wt [N,K]."""
+    M, K = x.shape
+    N = wt.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32 if out_dtype == "f32" else torch.bfloat16, device=x.device)
+    if workspace is None:
+        workspace = torch.empty(mx_fused_quantize_matmul_workspace(M, N, K), dtype=torch.uint8, device=x.device)
+    _check(_lib.mx_fused_quantize_matmul(_dev_ptr(x), DTYPES[_in_dtype(x)], x.stride(0), _dev_ptr(wt),
+                                         _dev_ptr(w_scale_sf), DTYPES[elem_dtype], M, N, K, DTYPES[out_dtype],
+                                         _dev_ptr(out), out.stride(0), _dev_ptr(workspace), workspace.numel(),
+                                         _stream(stream)),
+           "mx_fused_quantize_matmul")
+    return out
+
+
+def mx_get_device_status() -> int:
+    s = ctypes.c_int()
+    _check(_lib.mx_get_device_status(ctypes.byref(s)), "mx_get_device_status")
+    return s.value
+
+
+def mx_status_string(status: int) -> str:
+    return _lib.mx_status_string(status).decode()
+
+
+def mx_version() -> int:
+    return _lib.mx_version()
+
+
+def mx_debug_gemm_fault_injection(skip_producer: bool, timeout_ns: int = 0):
+    _check(_lib.mx_debug_gemm_fault_injection(int(skip_producer), timeout_ns), "mx_debug_gemm_fault_injection")
+
+
+def raw_library() -> ctypes.CDLL:
+    """The loaded ctypes handle (for callers that want the C-ABI directly)."""
+    return _lib

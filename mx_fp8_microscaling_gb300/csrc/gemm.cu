@@ -1,0 +1,390 @@
+// Block-scaled FP8 GEMM (ScaledMatmul) on the sm_103a tensor cores.
+//
+//   C[m,n] = sum_k dec(A[m,k]) 2^(sA[m,k/32]-127) * dec(Bt[n,k]) 2^(sB[n,k/32]-127)
+//
+// (ScaledMatmul of the page "MX-FP8 Microscaling Legalization", sections 3-4;
+// the scale is applied as 2^(E8M0 - 127), the inverse of the quantizer's
+// prescale, page "MX Microscaling", quantizeDataApplyingMxScales NOTE.)
+//
+// Design (one CTA per SM, persistent over 128 x 256 output tiles):
+//   warp 0      TMA producer: per 128-wide K block, one 2-D TMA load of the
+//               A tile (128 x 128 B) and of the B tile (256 x 128 B), both
+//               128-byte swizzled, plus three 512-byte bulk copies of the
+//               scale-factor tiles, into a 4-stage shared-memory ring.
+//   warp 1      MMA issuer (one thread): tcgen05.cp moves the stage's scale
+//               tiles into tensor memory, then four
+//               tcgen05.mma.kind::mxf8f6f4.block_scale (M=128, N=256, K=32)
+//               accumulate into a 128 x 256 f32 tile in tensor memory;
+//               tcgen05.commit frees the stage / hands the tile over.
+//   warps 2-9   epilogue: tcgen05.ld the accumulator (each warp its TMEM lane
+//               quarter and one 128-column half), release tensor memory to the
+//               MMA warp, then convert (f32 or bf16, round to nearest even) and
+//               store rows straight to global memory while the next tile's
+//               main loop runs.
+// Tensor memory (512 columns): accumulator in columns 0..255, scale factors
+// of pipeline stage s at 256 + 16 s (A: 4 columns, B: 8 columns).
+// Every mbarrier wait is bounded (2 s of wall clock by default); a wait that
+// gives up records MX_ERR_TIMEOUT in the device status word and all roles
+// leave their loops, wait for their own asynchronous work, free tensor memory
+// and return.
+
+#include <cstdint>
+#include <mutex>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "mx_device.cuh"
+#include "mx_internal.h"
+#include "tcgen05.cuh"
+
+namespace mx {
+
+// First device-side error since the last read (an mx_status value).
+__device__ int g_mx_status = 0;
+
+namespace {
+
+using namespace dev;
+
+constexpr int BM = 128, BN = 256, BK = 128;
+constexpr int STAGES = 4;
+constexpr int NUM_EPI_WARPS = 8;
+constexpr int NUM_THREADS = 64 + NUM_EPI_WARPS * 32;
+constexpr uint32_t A_STAGE = BM * BK;   // 16 KB
+constexpr uint32_t B_STAGE = BN * BK;   // 32 KB
+constexpr uint32_t SFA_STAGE = 512;
+constexpr uint32_t SFB_STAGE = 1024;
+constexpr uint32_t OFF_A = 0;
+constexpr uint32_t OFF_B = OFF_A + STAGES * A_STAGE;
+constexpr uint32_t OFF_SFA = OFF_B + STAGES * B_STAGE;
+constexpr uint32_t OFF_SFB = OFF_SFA + STAGES * SFA_STAGE;
+constexpr uint32_t OFF_BAR = OFF_SFB + STAGES * SFB_STAGE;
+constexpr int NUM_BARS = 2 * STAGES + 3;  // full[S], empty[S], tmem_full, tmem_empty, mma_done
+constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
+constexpr uint32_t SMEM_BYTES = OFF_MISC + 16;
+constexpr uint32_t SMEM_ALLOC = SMEM_BYTES + 1024;  // slack to align the base to 1024
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t TMEM_SF = 256;
+constexpr uint32_t STAGE_TX = A_STAGE + B_STAGE + SFA_STAGE + SFB_STAGE;
+
+struct KParams {
+    const uint8_t* sfa;
+    const uint8_t* sfb;
+    void* c;
+    int64_t ldc;
+    int M, N, K;
+    int out_bf16;
+    int vec_store;       // 16-byte row stores allowed (aligned c and pitch)
+    int num_m_tiles, num_n_tiles, num_kb;
+    int num_sf_n_tiles;  // 128-row scale tiles of B
+    int group_m;
+    uint32_t idesc;
+    uint64_t timeout_ns;
+    int skip_producer;   // fault injection: never issue loads (waits must time out)
+};
+
+__device__ __forceinline__ void tile_coords(int t, const KParams& p, int& mt, int& nt) {
+    const int group = p.group_m * p.num_n_tiles;
+    const int g = t / group;
+    const int first_m = g * p.group_m;
+    const int gm = min(p.num_m_tiles - first_m, p.group_m);
+    const int idx = t - g * group;
+    mt = first_m + idx % gm;
+    nt = idx / gm;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    mx_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                   const KParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sb = smem_u32(smem);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    auto full_bar = [&](int s) { return sb + OFF_BAR + 8u * s; };
+    auto empty_bar = [&](int s) { return sb + OFF_BAR + 8u * (STAGES + s); };
+    const uint32_t tmem_full = sb + OFF_BAR + 8u * (2 * STAGES);
+    const uint32_t tmem_empty = tmem_full + 8;
+    const uint32_t mma_done = tmem_full + 16;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        mbar_init(tmem_full, 1);
+        mbar_init(tmem_empty, NUM_EPI_WARPS);
+        mbar_init(mma_done, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        prefetch_tmap(&tmap_a);
+        prefetch_tmap(&tmap_b);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const int num_tiles = p.num_m_tiles * p.num_n_tiles;
+
+    if (warp == 0) {
+        if (lane == 0 && !p.skip_producer) {
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+                int mt, nt;
+                tile_coords(t, p, mt, nt);
+                const int nsf0 = 2 * nt;
+                const int nsf1 = (2 * nt + 1 < p.num_sf_n_tiles) ? 2 * nt + 1 : 2 * nt;
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, p.timeout_ns, &g_mx_status)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = full_bar(stage);
+                    mbar_arrive_expect_tx(fb, STAGE_TX);
+                    tma_load_2d(sb + OFF_A + stage * A_STAGE, &tmap_a, fb, kb * BK, mt * BM);
+                    tma_load_2d(sb + OFF_B + stage * B_STAGE, &tmap_b, fb, kb * BK, nt * BN);
+                    bulk_load(sb + OFF_SFA + stage * SFA_STAGE,
+                              p.sfa + (static_cast<size_t>(mt) * p.num_kb + kb) * 512u, 512u, fb);
+                    bulk_load(sb + OFF_SFB + stage * SFB_STAGE,
+                              p.sfb + (static_cast<size_t>(nsf0) * p.num_kb + kb) * 512u, 512u, fb);
+                    bulk_load(sb + OFF_SFB + stage * SFB_STAGE + 512u,
+                              p.sfb + (static_cast<size_t>(nsf1) * p.num_kb + kb) * 512u, 512u, fb);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            // Wait (bounded) until the loads of the last STAGES issued stages
+            // have landed, so no copy is in flight when the CTA exits.  A stage
+            // the MMA warp already consumed reads as complete at once.
+            for (int i = 0; i < STAGES; ++i) {
+                if (--stage < 0) {
+                    stage = STAGES - 1;
+                    phase ^= 1u;
+                }
+                volatile int no_abort = 0;
+                (void)mbar_wait_bounded(full_bar(stage), phase, &no_abort, 100000000ull, &g_mx_status);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0, acc_phase = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+                if (!mbar_wait_bounded(tmem_empty, acc_phase ^ 1u, abort_flag, p.timeout_ns, &g_mx_status)) break;
+                tc_fence_after();
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    if (!mbar_wait_bounded(full_bar(stage), phase, abort_flag, p.timeout_ns, &g_mx_status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sfa_t = tmem_base + TMEM_SF + 16u * stage;
+                    const uint32_t sfb_t = sfa_t + 4u;
+                    const uint32_t s_sfa = sb + OFF_SFA + stage * SFA_STAGE;
+                    const uint32_t s_sfb = sb + OFF_SFB + stage * SFB_STAGE;
+                    tc_cp_32x128b_warpx4(sfa_t, sdesc_sf_tile(s_sfa));
+                    tc_cp_32x128b_warpx4(sfb_t, sdesc_sf_tile(s_sfb));
+                    tc_cp_32x128b_warpx4(sfb_t + 4u, sdesc_sf_tile(s_sfb + 512u));
+                    const uint32_t sa = sb + OFF_A + stage * A_STAGE;
+                    const uint32_t sbb = sb + OFF_B + stage * B_STAGE;
+#pragma unroll
+                    for (int kk = 0; kk < BK / 32; ++kk) {
+                        const uint32_t idesc = p.idesc | (static_cast<uint32_t>(kk) << 4) |
+                                               (static_cast<uint32_t>(kk) << 29);
+                        tc_mma_mxf8(tmem_base, sdesc_kmajor_sw128(sa + kk * 32), sdesc_kmajor_sw128(sbb + kk * 32),
+                                    idesc, sfa_t, sfb_t, (kb | kk) != 0);
+                    }
+                    tc_commit(empty_bar(stage));
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                tc_commit(tmem_full);
+                acc_phase ^= 1u;
+            }
+            // Everything this thread issued must finish before tensor memory is freed.
+            tc_commit(mma_done);
+            volatile int no_abort = 0;
+            (void)mbar_wait_bounded(mma_done, 0, &no_abort, 100000000ull, &g_mx_status);
+        }
+    } else {
+        const int quarter = warp & 3;          // TMEM lanes this warp may access
+        const int half = (warp - 2) >> 2;      // accumulator columns [128*half, +128)
+        uint32_t acc_phase = 0;
+        for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+            int mt, nt;
+            tile_coords(t, p, mt, nt);
+            // one lane waits; the warp follows its verdict so it never diverges
+            bool ok = true;
+            if (lane == 0) ok = mbar_wait_bounded(tmem_full, acc_phase, abort_flag, p.timeout_ns, &g_mx_status);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            tc_fence_after();
+            uint32_t v[4][32];
+            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + half * 128;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) tmem_ld_32x32b_x32(taddr + 32u * j, v[j]);
+            tmem_wait_ld();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tmem_empty);
+            acc_phase ^= 1u;
+
+            const int64_t m = static_cast<int64_t>(mt) * BM + quarter * 32 + lane;
+            const int64_t n0 = static_cast<int64_t>(nt) * BN + half * 128;
+            if (m >= p.M || n0 >= p.N) continue;
+            if (p.out_bf16) {
+                uint16_t* crow = reinterpret_cast<uint16_t*>(p.c) + m * p.ldc + n0;
+                if (p.vec_store && n0 + 128 <= p.N) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            uint4 w;
+                            w.x = pack_bf16x2(__uint_as_float(v[j][8 * q + 0]), __uint_as_float(v[j][8 * q + 1]));
+                            w.y = pack_bf16x2(__uint_as_float(v[j][8 * q + 2]), __uint_as_float(v[j][8 * q + 3]));
+                            w.z = pack_bf16x2(__uint_as_float(v[j][8 * q + 4]), __uint_as_float(v[j][8 * q + 5]));
+                            w.w = pack_bf16x2(__uint_as_float(v[j][8 * q + 6]), __uint_as_float(v[j][8 * q + 7]));
+                            *reinterpret_cast<uint4*>(crow + 32 * j + 8 * q) = w;
+                        }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            if (n0 + 32 * j + i < p.N)
+                                crow[32 * j + i] = static_cast<uint16_t>(
+                                    pack_bf16x2(__uint_as_float(v[j][i]), 0.0f) & 0xFFFFu);
+                }
+            } else {
+                float* crow = reinterpret_cast<float*>(p.c) + m * p.ldc + n0;
+                if (p.vec_store && n0 + 128 <= p.N) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+#pragma unroll
+                        for (int q = 0; q < 8; ++q)
+                            *reinterpret_cast<uint4*>(crow + 32 * j + 4 * q) =
+                                make_uint4(v[j][4 * q], v[j][4 * q + 1], v[j][4 * q + 2], v[j][4 * q + 3]);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            if (n0 + 32 * j + i < p.N) crow[32 * j + i] = __uint_as_float(v[j][i]);
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
+}
+
+// ------------------------------------------------------------------- host
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+// K-major FP8 operand [rows, k] as a 2-D tensor map with a (128 B x box_rows) box, 128B swizzle.
+bool make_operand_map(CUtensorMap* map, const void* base, int64_t rows, int64_t k, uint32_t box_rows) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(k), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(k)};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+uint64_t g_timeout_ns = 2000000000ull;
+int g_fault_skip_producer = 0;
+
+}  // namespace
+
+void set_gemm_fault_injection(int skip_producer, uint64_t timeout_ns) {
+    g_fault_skip_producer = skip_producer;
+    g_timeout_ns = timeout_ns ? timeout_ns : 2000000000ull;
+}
+
+cudaError_t launch_scaled_matmul(const GemmArgs& g, cudaStream_t stream) {
+    static std::once_flag attr_once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(attr_once, [] {
+        attr_err = cudaFuncSetAttribute(mx_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+
+    CUtensorMap ma, mb;
+    if (!make_operand_map(&ma, g.a, g.M, g.K, BM) || !make_operand_map(&mb, g.bt, g.N, g.K, BN))
+        return cudaErrorInvalidValue;
+
+    KParams p{};
+    p.sfa = g.sfa;
+    p.sfb = g.sfb;
+    p.c = g.c;
+    p.ldc = g.ldc;
+    p.M = static_cast<int>(g.M);
+    p.N = static_cast<int>(g.N);
+    p.K = static_cast<int>(g.K);
+    p.out_bf16 = g.out_bf16;
+    p.vec_store = g.vec_store;
+    p.num_m_tiles = static_cast<int>((g.M + BM - 1) / BM);
+    p.num_n_tiles = static_cast<int>((g.N + BN - 1) / BN);
+    p.num_kb = static_cast<int>((g.K + BK - 1) / BK);
+    p.num_sf_n_tiles = static_cast<int>((g.N + 127) / 128);
+    p.group_m = 16;
+    p.idesc = make_idesc_mxf8(g.elem_fmt, g.elem_fmt, BM, BN);
+    p.timeout_ns = g_timeout_ns;
+    p.skip_producer = g_fault_skip_producer;
+
+    const int tiles = p.num_m_tiles * p.num_n_tiles;
+    const int sms = device_sm_count();
+    const int grid = tiles < sms ? tiles : sms;
+    mx_gemm_kernel<<<grid, NUM_THREADS, SMEM_ALLOC, stream>>>(ma, mb, p);
+    return cudaGetLastError();
+}
+
+cudaError_t read_and_clear_device_status(int* status) {
+    int zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(status, g_mx_status, sizeof(int));
+    if (e != cudaSuccess) return e;
+    return cudaMemcpyToSymbol(g_mx_status, &zero, sizeof(int));
+}
+
+}  // namespace mx

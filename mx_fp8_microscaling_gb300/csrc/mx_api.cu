@@ -1,0 +1,383 @@
+// libmx C-ABI: argument validation, normalisation and dispatch.
+//
+// Every entry point validates its arguments on the host and returns an
+// mx_status without launching anything when they are wrong; otherwise it
+// launches on the caller's stream and returns at once.  The contract checks
+// mirror the QuantizeMX / ScaledMatmul validators the page "MX-FP8
+// Microscaling Legalization" lists (section 6 GOTCHA and section 7: block_size
+// 32, the dtype sets, dim -1 / -2, divisibility by 4 for the x4 container, the
+// operand and output types).
+
+#include <cstdint>
+#include <mutex>
+
+#include <cuda_runtime.h>
+
+#include "mx.h"
+#include "mx_internal.h"
+
+namespace mx {
+
+void set_gemm_fault_injection(int skip_producer, uint64_t timeout_ns);
+
+namespace {
+
+struct DeviceInfo {
+    bool ready = false;
+    bool sm103 = false;
+    int sms = 0;
+};
+
+std::mutex g_dev_mutex;
+DeviceInfo g_dev[64];
+
+const DeviceInfo& current_device() {
+    static DeviceInfo none;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return none;
+    std::lock_guard<std::mutex> lock(g_dev_mutex);
+    DeviceInfo& d = g_dev[dev];
+    if (!d.ready) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return none;
+        d.sm103 = (major == 10 && minor == 3);
+        d.sms = sms;
+        d.ready = true;
+    }
+    return d;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Normalised QuantizeMX configuration.
+struct QuantPlan {
+    int fmt = 0;
+    bool in_f16 = false;
+    int br = 0, bc = 0;
+    int scale_mode = 0;
+    int emax_bias = 0;
+    int stride = 0, parity = 0;
+    int64_t scale_rows = 0, scale_cols = 0, scale_buf_rows = 0;
+    size_t data_bytes = 0;
+};
+
+int emax_of(int fmt) { return fmt == kE2M1 ? 2 : (fmt == kE4M3 ? 8 : 15); }
+
+mx_status plan_quantize(mx_dtype in_dtype, mx_dtype out_dtype, int64_t rows, int64_t cols,
+                        const mx_quant_cfg* user_cfg, QuantPlan* plan) {
+    mx_quant_cfg cfg;
+    mx_quant_cfg_default(&cfg);
+    if (user_cfg) cfg = *user_cfg;
+
+    if (in_dtype != MX_BF16 && in_dtype != MX_F16) return MX_ERR_UNSUPPORTED_DTYPE;
+    switch (out_dtype) {
+    case MX_E4M3FN: plan->fmt = kE4M3; break;
+    case MX_E5M2: plan->fmt = kE5M2; break;
+    case MX_E2M1: plan->fmt = kE2M1; break;
+    default: return MX_ERR_UNSUPPORTED_DTYPE;
+    }
+    plan->in_f16 = (in_dtype == MX_F16);
+    if (cfg.block_size != 0 && cfg.block_size != 32) return MX_ERR_BLOCK_SIZE;
+    if (cfg.scale_method != MX_SCALE_METHOD_EMAX) return MX_ERR_SCALE_METHOD;
+    int dim = cfg.dim;
+    if (dim == 1) dim = -1;
+    if (dim == 0) dim = -2;
+    if (dim != -1 && dim != -2) return MX_ERR_DIM;
+    if (cfg.geometry == MX_GEOM_8X4) {
+        plan->br = dim == -2 ? 8 : 4;
+        plan->bc = dim == -2 ? 4 : 8;
+    } else if (cfg.geometry == MX_GEOM_1X32) {
+        plan->br = dim == -2 ? 32 : 1;
+        plan->bc = dim == -2 ? 1 : 32;
+    } else {
+        return MX_ERR_INVALID_ARG;
+    }
+    if (cfg.scale_layout != MX_SCALE_PLAIN && cfg.scale_layout != MX_SCALE_INTERLEAVE32 &&
+        cfg.scale_layout != MX_SCALE_TC_SF)
+        return MX_ERR_INVALID_ARG;
+    if (cfg.scale_layout == MX_SCALE_TC_SF && (cfg.geometry != MX_GEOM_1X32 || dim != -1))
+        return MX_ERR_INVALID_ARG;
+    plan->scale_mode = cfg.scale_layout;
+    if (cfg.emax_alt != 0 && cfg.emax_alt != 1) return MX_ERR_INVALID_ARG;
+    plan->emax_bias = emax_of(plan->fmt) - cfg.emax_alt;
+    const int s = cfg.fp4_lane_stride;
+    if (s != 0 && s != 1 && s != 2 && s != 4) return MX_ERR_INVALID_ARG;
+    if (cfg.fp4_nibble_parity != 0 && cfg.fp4_nibble_parity != 1) return MX_ERR_INVALID_ARG;
+    plan->stride = s;
+    plan->parity = cfg.fp4_nibble_parity;
+
+    if (rows < 0 || cols < 0) return MX_ERR_INVALID_ARG;
+    if (cols % 4 != 0 || rows % plan->br != 0 || cols % plan->bc != 0) return MX_ERR_SHAPE;
+    if (plan->fmt == kE2M1 && s > 1 && cols % (2 * s) != 0) return MX_ERR_SHAPE;
+
+    plan->scale_rows = rows / plan->br;
+    plan->scale_cols = cols / plan->bc;
+    if (plan->scale_mode == MX_SCALE_INTERLEAVE32) {
+        plan->scale_buf_rows = 32 * ((plan->scale_rows + 3) / 4);
+    } else if (plan->scale_mode == MX_SCALE_TC_SF) {
+        plan->scale_buf_rows = (plan->scale_rows + 127) / 128 * 128;
+        plan->scale_cols = (plan->scale_cols + 3) / 4 * 4;
+    } else {
+        plan->scale_buf_rows = plan->scale_rows;
+    }
+    plan->data_bytes = static_cast<size_t>(plan->fmt == kE2M1 ? rows * cols / 2 : rows * cols);
+    return MX_OK;
+}
+
+// __byte_perm selector that moves pair-byte p of an 8-element chunk to the
+// byte the page's lane_remap gives element 2p: byte (remap(2p) >> 1).
+uint32_t fp4_pair_perm(int stride) {
+    int dest[4];
+    for (int p = 0; p < 4; ++p) {
+        int64_t n = 2 * p, r = n;
+        if (stride) {
+            const int64_t w = 2 * stride, q = n / w, rr = n % w;
+            r = w * (q + 1) - rr;
+            if ((n & 1) == 0) r -= 2;
+        }
+        dest[p] = static_cast<int>(r >> 1);
+    }
+    uint32_t sel = 0;
+    for (int p = 0; p < 4; ++p) sel |= static_cast<uint32_t>(p) << (4 * dest[p]);
+    return sel;
+}
+
+mx_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MX_OK : MX_ERR_CUDA; }
+
+size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
+
+}  // namespace
+
+int device_sm_count() { return current_device().sms; }
+bool device_is_sm103() { return current_device().sm103; }
+
+}  // namespace mx
+
+using namespace mx;
+
+extern "C" {
+
+mx_status mx_quant_cfg_default(mx_quant_cfg* cfg) {
+    if (!cfg) return MX_ERR_INVALID_ARG;
+    cfg->geometry = MX_GEOM_8X4;
+    cfg->scale_layout = MX_SCALE_PLAIN;
+    cfg->block_size = 32;
+    cfg->dim = -2;
+    cfg->scale_method = MX_SCALE_METHOD_EMAX;
+    cfg->fp4_lane_stride = 2;
+    cfg->fp4_nibble_parity = 0;
+    cfg->emax_alt = 0;
+    return MX_OK;
+}
+
+mx_status mx_quantize_sizes(mx_dtype in_dtype, mx_dtype out_dtype, int64_t rows, int64_t cols,
+                            const mx_quant_cfg* cfg, size_t* data_bytes, int64_t* scale_rows,
+                            int64_t* scale_cols, size_t* scale_bytes) {
+    QuantPlan plan;
+    mx_status st = plan_quantize(in_dtype, out_dtype, rows, cols, cfg, &plan);
+    if (st != MX_OK) return st;
+    if (data_bytes) *data_bytes = plan.data_bytes;
+    if (scale_rows) *scale_rows = plan.scale_buf_rows;
+    if (scale_cols) *scale_cols = plan.scale_cols;
+    if (scale_bytes) *scale_bytes = static_cast<size_t>(plan.scale_buf_rows * plan.scale_cols);
+    return MX_OK;
+}
+
+mx_status mx_quantize(const void* in, mx_dtype in_dtype, int64_t rows, int64_t cols, int64_t ld_in,
+                      mx_dtype out_dtype, const mx_quant_cfg* cfg, void* out_data, void* out_scale,
+                      mx_stream stream) {
+    QuantPlan plan;
+    mx_status st = plan_quantize(in_dtype, out_dtype, rows, cols, cfg, &plan);
+    if (st != MX_OK) return st;
+    if (ld_in < cols) return MX_ERR_INVALID_ARG;
+    if (rows == 0 || cols == 0) return MX_OK;
+    if (!in || !out_data || !out_scale) return MX_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(in) & 1u) || (reinterpret_cast<uintptr_t>(out_data) & 1u))
+        return MX_ERR_ALIGNMENT;
+    if (!device_is_sm103()) return MX_ERR_DEVICE;
+
+    QuantArgs q{};
+    q.in = static_cast<const uint8_t*>(in);
+    q.rows = rows;
+    q.cols = cols;
+    q.ld_in = ld_in;
+    q.data = static_cast<uint8_t*>(out_data);
+    q.ld_data = plan.fmt == kE2M1 ? cols / 2 : cols;
+    q.scale = static_cast<uint8_t*>(out_scale);
+    q.scale_cols = plan.scale_cols;
+    q.block_rows = plan.br;
+    q.block_cols = plan.bc;
+    q.scale_mode = plan.scale_mode;
+    q.sf_ntk = plan.scale_cols / 4;
+    q.emax_bias = plan.emax_bias;
+    q.fp4_stride = plan.stride;
+    q.fp4_parity = plan.parity;
+    q.fp4_perm = fp4_pair_perm(plan.stride);
+    q.vec_ok = aligned16(in) && (ld_in * 2) % 16 == 0 && (reinterpret_cast<uintptr_t>(out_data) & 7u) == 0 &&
+               (reinterpret_cast<uintptr_t>(out_scale) & 1u) == 0;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (plan.scale_mode == MX_SCALE_TC_SF && (rows % 128 != 0 || (cols / 32) % 4 != 0)) {
+        // the kernel writes live scales only; padding of the SF tiles is 0
+        if (cudaMemsetAsync(out_scale, 0, static_cast<size_t>(plan.scale_buf_rows * plan.scale_cols), s) !=
+            cudaSuccess)
+            return MX_ERR_CUDA;
+    }
+    return from_cuda(launch_quantize(q, plan.in_f16, plan.fmt, s));
+}
+
+mx_status mx_sf_layout_bytes(int64_t mn, int64_t k, size_t* bytes) {
+    if (!bytes || mn < 0 || k < 0) return MX_ERR_INVALID_ARG;
+    if (k % 32 != 0) return MX_ERR_SHAPE;
+    *bytes = sf_layout_bytes(mn, k);
+    return MX_OK;
+}
+
+mx_status mx_repack_scales(const uint8_t* plain, int64_t mn, int64_t k, int64_t ld_plain, uint8_t* sf,
+                           mx_stream stream) {
+    if (mn < 0 || k < 0) return MX_ERR_INVALID_ARG;
+    if (k % 32 != 0) return MX_ERR_SHAPE;
+    if (ld_plain < k / 32) return MX_ERR_INVALID_ARG;
+    if (mn == 0 || k == 0) return MX_OK;
+    if (!plain || !sf) return MX_ERR_INVALID_ARG;
+    if (!aligned16(sf)) return MX_ERR_ALIGNMENT;
+    if (!device_is_sm103()) return MX_ERR_DEVICE;
+    return from_cuda(launch_repack_scales(plain, mn, k, ld_plain, sf, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+mx_status mx_scaled_matmul_workspace(int64_t M, int64_t N, int64_t K, int scales_are_sf_layout, size_t* bytes) {
+    if (!bytes || M < 0 || N < 0 || K < 0) return MX_ERR_INVALID_ARG;
+    if (K % 32 != 0) return MX_ERR_SHAPE;
+    *bytes = scales_are_sf_layout ? 0 : align16(sf_layout_bytes(M, K)) + align16(sf_layout_bytes(N, K));
+    return MX_OK;
+}
+
+static mx_status check_matmul(const void* a, const void* bt, const uint8_t* a_scale, const uint8_t* b_scale,
+                              mx_dtype elem_dtype, int64_t M, int64_t N, int64_t K, mx_dtype out_dtype, void* c,
+                              int64_t ldc) {
+    if (elem_dtype != MX_E4M3FN && elem_dtype != MX_E5M2) return MX_ERR_UNSUPPORTED_DTYPE;
+    if (out_dtype != MX_F32 && out_dtype != MX_BF16) return MX_ERR_UNSUPPORTED_DTYPE;
+    if (M < 0 || N < 0 || K < 0) return MX_ERR_INVALID_ARG;
+    if (K < 32 || K % 32 != 0) return MX_ERR_SHAPE;
+    if (M > (int64_t(1) << 30) || N > (int64_t(1) << 30) || K > (int64_t(1) << 30)) return MX_ERR_SHAPE;
+    if (ldc < N) return MX_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return MX_OK;
+    if (!a || !bt || !a_scale || !b_scale || !c) return MX_ERR_INVALID_ARG;
+    const uintptr_t esize = out_dtype == MX_F32 ? 4 : 2;
+    if (!aligned16(a) || !aligned16(bt) || (reinterpret_cast<uintptr_t>(c) & (esize - 1))) return MX_ERR_ALIGNMENT;
+    return MX_OK;
+}
+
+mx_status mx_scaled_matmul(const void* a, const void* bt, const uint8_t* a_scale, const uint8_t* b_scale,
+                           int scales_are_sf_layout, mx_dtype elem_dtype, int64_t M, int64_t N, int64_t K,
+                           mx_dtype out_dtype, void* c, int64_t ldc, void* workspace, size_t workspace_bytes,
+                           mx_stream stream) {
+    mx_status st = check_matmul(a, bt, a_scale, b_scale, elem_dtype, M, N, K, out_dtype, c, ldc);
+    if (st != MX_OK || M == 0 || N == 0) return st;
+    const uint8_t* sfa = a_scale;
+    const uint8_t* sfb = b_scale;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (scales_are_sf_layout) {
+        if (!aligned16(a_scale) || !aligned16(b_scale)) return MX_ERR_ALIGNMENT;
+    } else {
+        size_t need = 0;
+        mx_scaled_matmul_workspace(M, N, K, 0, &need);
+        if (!workspace || workspace_bytes < need) return MX_ERR_WORKSPACE;
+        if (!aligned16(workspace)) return MX_ERR_ALIGNMENT;
+    }
+    if (!device_is_sm103()) return MX_ERR_DEVICE;
+    if (!scales_are_sf_layout) {
+        uint8_t* ws = static_cast<uint8_t*>(workspace);
+        uint8_t* wa = ws;
+        uint8_t* wb = ws + align16(sf_layout_bytes(M, K));
+        cudaError_t e = launch_repack_scales(a_scale, M, K, K / 32, wa, s);
+        if (e == cudaSuccess) e = launch_repack_scales(b_scale, N, K, K / 32, wb, s);
+        if (e != cudaSuccess) return MX_ERR_CUDA;
+        sfa = wa;
+        sfb = wb;
+    }
+    GemmArgs g{};
+    g.a = static_cast<const uint8_t*>(a);
+    g.bt = static_cast<const uint8_t*>(bt);
+    g.sfa = sfa;
+    g.sfb = sfb;
+    g.M = M;
+    g.N = N;
+    g.K = K;
+    g.c = c;
+    g.ldc = ldc;
+    g.elem_fmt = elem_dtype == MX_E4M3FN ? kE4M3 : kE5M2;
+    g.out_bf16 = out_dtype == MX_BF16;
+    g.vec_store = aligned16(c) && (ldc * (out_dtype == MX_F32 ? 4 : 2)) % 16 == 0;
+    return from_cuda(launch_scaled_matmul(g, s));
+}
+
+mx_status mx_fused_quantize_matmul_workspace(int64_t M, int64_t N, int64_t K, size_t* bytes) {
+    if (!bytes || M < 0 || N < 0 || K < 0) return MX_ERR_INVALID_ARG;
+    if (K % 32 != 0) return MX_ERR_SHAPE;
+    *bytes = align16(static_cast<size_t>(M * K)) + align16(sf_layout_bytes(M, K));
+    return MX_OK;
+}
+
+mx_status mx_fused_quantize_matmul(const void* x, mx_dtype x_dtype, int64_t ld_x, const void* wt,
+                                   const uint8_t* w_scale_sf, mx_dtype elem_dtype, int64_t M, int64_t N, int64_t K,
+                                   mx_dtype out_dtype, void* c, int64_t ldc, void* workspace,
+                                   size_t workspace_bytes, mx_stream stream) {
+    if (x_dtype != MX_BF16 && x_dtype != MX_F16) return MX_ERR_UNSUPPORTED_DTYPE;
+    const void* dummy = workspace ? workspace : wt;
+    mx_status st = check_matmul(dummy, wt, w_scale_sf, w_scale_sf, elem_dtype, M, N, K, out_dtype, c, ldc);
+    if (st != MX_OK || M == 0 || N == 0) return st;
+    if (ld_x < K) return MX_ERR_INVALID_ARG;
+    if (!x) return MX_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(x) & 1u) || !aligned16(w_scale_sf)) return MX_ERR_ALIGNMENT;
+    size_t need = 0;
+    mx_fused_quantize_matmul_workspace(M, N, K, &need);
+    if (!workspace || workspace_bytes < need) return MX_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return MX_ERR_ALIGNMENT;
+    if (!device_is_sm103()) return MX_ERR_DEVICE;
+    uint8_t* xq = static_cast<uint8_t*>(workspace);
+    uint8_t* xs = xq + align16(static_cast<size_t>(M * K));
+    mx_quant_cfg cfg;
+    mx_quant_cfg_default(&cfg);
+    cfg.geometry = MX_GEOM_1X32;
+    cfg.dim = -1;
+    cfg.scale_layout = MX_SCALE_TC_SF;
+    st = mx_quantize(x, x_dtype, M, K, ld_x, elem_dtype, &cfg, xq, xs, stream);
+    if (st != MX_OK) return st;
+    return mx_scaled_matmul(xq, wt, xs, w_scale_sf, 1, elem_dtype, M, N, K, out_dtype, c, ldc, nullptr, 0, stream);
+}
+
+mx_status mx_get_device_status(int* status) {
+    if (!status) return MX_ERR_INVALID_ARG;
+    if (cudaDeviceSynchronize() != cudaSuccess) return MX_ERR_CUDA;
+    return from_cuda(read_and_clear_device_status(status));
+}
+
+const char* mx_status_string(mx_status status) {
+    switch (status) {
+    case MX_OK: return "MX_OK";
+    case MX_ERR_INVALID_ARG: return "MX_ERR_INVALID_ARG: invalid argument";
+    case MX_ERR_UNSUPPORTED_DTYPE: return "MX_ERR_UNSUPPORTED_DTYPE: dtype combination not supported";
+    case MX_ERR_BLOCK_SIZE: return "MX_ERR_BLOCK_SIZE: block_size must be 32";
+    case MX_ERR_DIM: return "MX_ERR_DIM: only the last (-1) or second-to-last (-2) dim is supported";
+    case MX_ERR_SHAPE: return "MX_ERR_SHAPE: extents not divisible by the block or the x4 container";
+    case MX_ERR_ALIGNMENT: return "MX_ERR_ALIGNMENT: pointer or pitch not 16-byte aligned";
+    case MX_ERR_WORKSPACE: return "MX_ERR_WORKSPACE: workspace missing or too small";
+    case MX_ERR_CUDA: return "MX_ERR_CUDA: CUDA runtime error";
+    case MX_ERR_TIMEOUT: return "MX_ERR_TIMEOUT: a bounded device wait gave up";
+    case MX_ERR_DEVICE: return "MX_ERR_DEVICE: current device is not sm_103a";
+    case MX_ERR_SCALE_METHOD: return "MX_ERR_SCALE_METHOD: scale_method must be EMAX";
+    }
+    return "unknown mx_status";
+}
+
+int mx_version(void) { return 100; }
+
+mx_status mx_debug_gemm_fault_injection(int skip_producer, uint64_t timeout_ns) {
+    set_gemm_fault_injection(skip_producer, timeout_ns);
+    return MX_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,65 @@
+// Internal declarations shared by the libmx translation units (host side).
+#pragma once
+
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "mx.h"
+
+namespace mx {
+
+// Element formats as the kernels see them.
+enum Fmt : int { kE4M3 = 0, kE5M2 = 1, kE2M1 = 2 };
+
+// One QuantizeMX launch, already validated and normalised by the C-ABI layer.
+struct QuantArgs {
+    const uint8_t* in;      // bf16/f16 elements, byte pointer
+    int64_t rows, cols;     // logical extents
+    int64_t ld_in;          // input pitch in elements
+    uint8_t* data;          // dense output
+    int64_t ld_data;        // output pitch in bytes (cols or cols/2)
+    uint8_t* scale;         // scale buffer
+    int64_t scale_cols;     // columns of the scale tensor
+    int32_t block_rows;     // block extent along rows (8, 4, 1, 32)
+    int32_t block_cols;     // block extent along columns (4, 8, 32, 1)
+    int32_t scale_mode;     // 0 plain, 1 interleave (row i -> (i & 3) + 32 * (i >> 2)),
+                            // 2 tensor-core SF tiles (1x32 blocks along rows only)
+    int64_t sf_ntk;         // SF mode: 128-column tiles per 128-row tile band
+    int32_t emax_bias;      // EMAX (or EMAX-1)
+    int32_t fp4_stride;     // lane_remap stride (0 = none)
+    int32_t fp4_parity;     // nibble parity
+    uint32_t fp4_perm;      // __byte_perm selector placing the 4 pair-bytes of an 8-element chunk
+    int32_t vec_ok;         // 16-byte input rows and 8-byte output rows: vectorised kernels allowed
+};
+
+cudaError_t launch_quantize(const QuantArgs& q, bool in_f16, int fmt, cudaStream_t stream);
+
+// Scale-factor repack: plain [mn, k/32] -> SF tiles (see mx_repack_scales).
+cudaError_t launch_repack_scales(const uint8_t* plain, int64_t mn, int64_t k, int64_t ld_plain,
+                                 uint8_t* sf, cudaStream_t stream);
+size_t sf_layout_bytes(int64_t mn, int64_t k);
+
+// Block-scaled GEMM on SF-layout scales.
+struct GemmArgs {
+    const uint8_t* a;        // [M, K] FP8
+    const uint8_t* bt;       // [N, K] FP8
+    const uint8_t* sfa;      // SF layout for A
+    const uint8_t* sfb;      // SF layout for Bt
+    int64_t M, N, K;
+    void* c;
+    int64_t ldc;             // elements
+    int32_t elem_fmt;        // kE4M3 | kE5M2
+    int32_t out_bf16;        // 1: bf16 output, 0: f32
+    int32_t vec_store;       // 1: c and ldc allow 16-byte row stores
+};
+cudaError_t launch_scaled_matmul(const GemmArgs& g, cudaStream_t stream);
+
+// Per-device properties, cached.
+int device_sm_count();
+bool device_is_sm103();
+
+// Device status word (first device-side error since the last read).
+cudaError_t read_and_clear_device_status(int* status);
+
+}  // namespace mx

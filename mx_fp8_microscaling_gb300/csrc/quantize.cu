@@ -1,0 +1,399 @@
+// QuantizeMX kernels for sm_103a.
+//
+// The arithmetic follows the page "MX Microscaling: Quantize, Block-Scaling
+// and E8M0":
+//   - block max of the binary32 exponent byte, sign dropped
+//     (findMaxExponentPerInputBlock);
+//   - E8M0 = max(1, max(0, maxExp - EMAX)) (generateMxScales);
+//   - y = x * 2^(127 - E8M0), one binary32 multiply (quantizeDataApplyingMxScales);
+//   - round to nearest even with saturation (Round-to-Grid), NaN -> 0x7F|sign
+//     for FP8 and a signed zero nibble for e2m1, Inf -> the format maximum;
+//   - x4 packing: FP8 bytes in element order; e2m1 nibbles placed by the
+//     page's lane_remap (x4-Pack), scale rows optionally interleaved
+//     (E8M0 Scale-Tensor Layout).
+//
+// The quantizer is bound by HBM bandwidth (2 bytes in, 1 or 0.5 byte out per
+// element).  The fast kernels give each thread 8 contiguous elements per row
+// (one 16-byte load), so a warp reads 512 contiguous bytes per row:
+//   quant_g84   8x4 blocks, dim=-2: a thread owns 8 rows x 8 columns = two
+//               whole blocks, so the block max needs no communication.
+//   quant_g1x32 1x32 blocks along rows: a block spans 4 lanes; two xor
+//               shuffles finish the max.  Each thread handles 4 rows.
+// Block maxima are taken on 16-bit magnitudes (exponent field on top, so the
+// magnitude order is the exponent order) with max.u16x2, two elements per op.
+// Blocks that contain Inf/NaN (exponent byte 255) take a per-element path
+// that encodes the special values explicitly.
+//
+// quant_generic covers every geometry, any width with cols % 4 == 0 and any
+// element-aligned pitch, one thread per tile of whole blocks, scalar loads.
+
+#include <cstdint>
+
+#include "mx_device.cuh"
+#include "mx_internal.h"
+
+namespace mx {
+namespace {
+
+using namespace dev;
+
+constexpr int kThreads = 256;
+
+// --------------------------------------------------------------- helpers
+
+template <bool F16>
+__device__ __forceinline__ float widen_lo(uint32_t w) {
+    if constexpr (F16) return f16_bits_to_f32(w & 0xFFFFu);
+    else return __uint_as_float(w << 16);
+}
+template <bool F16>
+__device__ __forceinline__ float widen_hi(uint32_t w) {
+    if constexpr (F16) return f16_bits_to_f32(w >> 16);
+    else return __uint_as_float(w & 0xFFFF0000u);
+}
+template <bool F16>
+__device__ __forceinline__ float widen1(uint32_t h) {
+    if constexpr (F16) return f16_bits_to_f32(h);
+    else return __uint_as_float(h << 16);
+}
+
+// Binary32 exponent byte of the widened value whose 16-bit magnitude is m16.
+template <bool F16>
+__device__ __forceinline__ uint32_t exp_byte_of_mag(uint32_t m16) {
+    if constexpr (F16) return __float_as_uint(f16_bits_to_f32(m16)) >> 23;
+    else return m16 >> 7;
+}
+
+// E8M0 from the block's max exponent byte: floor at 0, then at 1.
+__device__ __forceinline__ uint32_t e8m0_of(uint32_t max_exp, int bias) {
+    int v = static_cast<int>(max_exp) - bias;
+    return static_cast<uint32_t>(v < 1 ? 1 : v);
+}
+
+// 2^(127 - E): the binary32 with exponent field 254 - E and zero fraction.
+__device__ __forceinline__ float prescale_mul(uint32_t e8m0) {
+    return __uint_as_float((254u - e8m0) << 23);
+}
+
+__device__ __forceinline__ uint32_t mag2(uint32_t w) { return w & 0x7FFF7FFFu; }
+__device__ __forceinline__ uint32_t hmax(uint32_t m) {
+    uint32_t lo = m & 0xFFFFu, hi = m >> 16;
+    return lo > hi ? lo : hi;
+}
+
+// Scale-row placement (plain / interleaved).
+__device__ __forceinline__ int64_t scale_slot(int64_t i, int mode) {
+    return mode == 1 ? (i & 3) + 32 * (i >> 2) : i;
+}
+
+// Byte offset of scale (srow, scol) in the scale buffer.  Mode 2 is the
+// tensor-core scale-factor layout: 512-byte tiles of 128 rows x 4 columns,
+// scale (r, c) at (r % 32) * 16 + ((r / 32) % 4) * 4 + c % 4 inside its tile.
+__device__ __forceinline__ int64_t scale_offset(const QuantArgs& q, int64_t srow, int64_t scol) {
+    if (q.scale_mode == 2) {
+        const int64_t tile = (srow >> 7) * q.sf_ntk + (scol >> 2);
+        return tile * 512 + (srow & 31) * 16 + ((srow >> 5) & 3) * 4 + (scol & 3);
+    }
+    return scale_slot(srow, q.scale_mode) * q.scale_cols + scol;
+}
+
+template <int FMT>
+__device__ __forceinline__ uint32_t cvt_pair(float hi, float lo) {
+    if constexpr (FMT == kE4M3) return cvt_e4m3x2(hi, lo);
+    else if constexpr (FMT == kE5M2) return cvt_e5m2x2(hi, lo);
+    else return cvt_e2m1x2(hi, lo);
+}
+
+// One element, special values handled explicitly (used where a block holds
+// Inf/NaN, and by the generic kernel).
+template <int FMT>
+__device__ __forceinline__ uint32_t encode1(float y) {
+    const uint32_t sign = __float_as_uint(y) >> 31;
+    if constexpr (FMT == kE2M1) {
+        if (isnan(y)) return sign << 3;
+        if (isinf(y)) return (sign << 3) | 7u;
+        return cvt_e2m1x2(0.0f, y) & 0xFu;
+    } else {
+        constexpr uint32_t kMax = (FMT == kE4M3) ? 0x7Eu : 0x7Bu;
+        if (isnan(y)) return (sign << 7) | 0x7Fu;
+        if (isinf(y)) return (sign << 7) | kMax;
+        return cvt_pair<FMT>(0.0f, y) & 0xFFu;
+    }
+}
+
+// 8 prescaled values of one row -> packed output.
+// FP8: two 32-bit words, byte j = element j.
+// e2m1: one 32-bit word; pair p = elements (2p, 2p+1) forms one byte (the
+// even element in the high nibble for parity 0), and the four pair-bytes are
+// placed by the lane-remap permutation `perm`.
+template <int FMT>
+__device__ __forceinline__ void pack8(const float (&y)[8], bool special, int parity, uint32_t perm,
+                                      uint32_t& w0, uint32_t& w1) {
+    if constexpr (FMT == kE2M1) {
+        uint32_t b[4];
+        if (!special) {
+#pragma unroll
+            for (int p = 0; p < 4; ++p)
+                b[p] = parity ? cvt_pair<FMT>(y[2 * p + 1], y[2 * p]) : cvt_pair<FMT>(y[2 * p], y[2 * p + 1]);
+        } else {
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+                uint32_t n0 = encode1<FMT>(y[2 * p]), n1 = encode1<FMT>(y[2 * p + 1]);
+                b[p] = parity ? ((n1 << 4) | n0) : ((n0 << 4) | n1);
+            }
+        }
+        uint32_t src = b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24);
+        w0 = __byte_perm(src, 0u, perm);
+        w1 = 0;
+    } else {
+        if (!special) {
+            w0 = cvt_pair<FMT>(y[1], y[0]) | (cvt_pair<FMT>(y[3], y[2]) << 16);
+            w1 = cvt_pair<FMT>(y[5], y[4]) | (cvt_pair<FMT>(y[7], y[6]) << 16);
+        } else {
+            uint32_t c[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) c[j] = encode1<FMT>(y[j]);
+            w0 = c[0] | (c[1] << 8) | (c[2] << 16) | (c[3] << 24);
+            w1 = c[4] | (c[5] << 8) | (c[6] << 16) | (c[7] << 24);
+        }
+    }
+}
+
+template <int FMT>
+__device__ __forceinline__ void store8(uint8_t* dst, uint32_t w0, uint32_t w1) {
+    if constexpr (FMT == kE2M1) *reinterpret_cast<uint32_t*>(dst) = w0;
+    else *reinterpret_cast<uint2*>(dst) = make_uint2(w0, w1);
+}
+
+// ------------------------------------------------------ 8x4 blocks, dim=-2
+
+// Thread unit: row group g (8 rows) x column chunk c (8 columns) = 2 blocks.
+// Consecutive threads take consecutive chunks of the same rows.
+template <bool F16, int FMT>
+__global__ void __launch_bounds__(kThreads) quant_g84(QuantArgs q) {
+    const int64_t nchunk = q.cols >> 3;
+    const int64_t total = (q.rows >> 3) * nchunk;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    const int64_t in_pitch = q.ld_in * 2;
+    for (int64_t u = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; u < total; u += stride) {
+        const int64_t g = u / nchunk;
+        const int64_t c = u - g * nchunk;
+        const uint8_t* src = q.in + (g * 8) * in_pitch + c * 16;
+        uint4 v[8];
+#pragma unroll
+        for (int r = 0; r < 8; ++r) v[r] = ld_stream_v4(src + r * in_pitch);
+
+        uint32_t ma = 0, mb = 0;
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+            ma = vmax_u16x2(ma, vmax_u16x2(mag2(v[r].x), mag2(v[r].y)));
+            mb = vmax_u16x2(mb, vmax_u16x2(mag2(v[r].z), mag2(v[r].w)));
+        }
+        const uint32_t xa = exp_byte_of_mag<F16>(hmax(ma));
+        const uint32_t xb = exp_byte_of_mag<F16>(hmax(mb));
+        const uint32_t ea = e8m0_of(xa, q.emax_bias), eb = e8m0_of(xb, q.emax_bias);
+        const float sa = prescale_mul(ea), sb = prescale_mul(eb);
+        const bool special = (xa == 255u) | (xb == 255u);
+
+        constexpr int kOutBytes = (FMT == kE2M1) ? 4 : 8;
+        uint8_t* dst = q.data + (g * 8) * q.ld_data + c * kOutBytes;
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+            float y[8];
+            y[0] = mul_rn(widen_lo<F16>(v[r].x), sa);
+            y[1] = mul_rn(widen_hi<F16>(v[r].x), sa);
+            y[2] = mul_rn(widen_lo<F16>(v[r].y), sa);
+            y[3] = mul_rn(widen_hi<F16>(v[r].y), sa);
+            y[4] = mul_rn(widen_lo<F16>(v[r].z), sb);
+            y[5] = mul_rn(widen_hi<F16>(v[r].z), sb);
+            y[6] = mul_rn(widen_lo<F16>(v[r].w), sb);
+            y[7] = mul_rn(widen_hi<F16>(v[r].w), sb);
+            uint32_t w0, w1;
+            pack8<FMT>(y, special, q.fp4_parity, q.fp4_perm, w0, w1);
+            store8<FMT>(dst + r * q.ld_data, w0, w1);
+        }
+        *reinterpret_cast<uint16_t*>(q.scale + scale_slot(g, q.scale_mode) * q.scale_cols + c * 2) =
+            static_cast<uint16_t>(ea | (eb << 8));
+    }
+}
+
+// ------------------------------------------------ 1x32 blocks along rows
+
+// Thread unit: 4 rows x 8 columns; the 4 lanes 4j..4j+3 hold one block per
+// row.  The loop is warp-uniform so every lane takes part in the shuffles.
+template <bool F16, int FMT>
+__global__ void __launch_bounds__(kThreads) quant_g1x32(QuantArgs q) {
+    constexpr int TR = 4;
+    const int lane = threadIdx.x & 31;
+    const int64_t nchunk = q.cols >> 3;
+    const int64_t ngroups = (q.rows + TR - 1) / TR;
+    const int64_t total = ngroups * nchunk;  // multiple of 4: nchunk % 4 == 0
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    const int64_t in_pitch = q.ld_in * 2;
+    for (int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x + (threadIdx.x & ~31);
+         base < total; base += stride) {
+        const int64_t u = base + lane;
+        const bool active = u < total;
+        const int64_t g = active ? u / nchunk : 0;
+        const int64_t c = active ? u - g * nchunk : 0;
+        const int64_t r0 = g * TR;
+        uint4 v[TR];
+#pragma unroll
+        for (int r = 0; r < TR; ++r) {
+            if (active && r0 + r < q.rows) v[r] = ld_stream_v4(q.in + (r0 + r) * in_pitch + c * 16);
+            else v[r] = make_uint4(0, 0, 0, 0);
+        }
+        uint32_t e[TR];
+        float s[TR];
+        bool special = false;
+#pragma unroll
+        for (int r = 0; r < TR; ++r) {
+            uint32_t m = vmax_u16x2(vmax_u16x2(mag2(v[r].x), mag2(v[r].y)),
+                                    vmax_u16x2(mag2(v[r].z), mag2(v[r].w)));
+            m = hmax(m);
+            m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
+            m = max(m, __shfl_xor_sync(0xffffffffu, m, 2));
+            const uint32_t x = exp_byte_of_mag<F16>(m);
+            special |= (x == 255u);
+            e[r] = e8m0_of(x, q.emax_bias);
+            s[r] = prescale_mul(e[r]);
+        }
+        if (active) {
+            constexpr int kOutBytes = (FMT == kE2M1) ? 4 : 8;
+#pragma unroll
+            for (int r = 0; r < TR; ++r) {
+                if (r0 + r >= q.rows) break;
+                float y[8];
+                y[0] = mul_rn(widen_lo<F16>(v[r].x), s[r]);
+                y[1] = mul_rn(widen_hi<F16>(v[r].x), s[r]);
+                y[2] = mul_rn(widen_lo<F16>(v[r].y), s[r]);
+                y[3] = mul_rn(widen_hi<F16>(v[r].y), s[r]);
+                y[4] = mul_rn(widen_lo<F16>(v[r].z), s[r]);
+                y[5] = mul_rn(widen_hi<F16>(v[r].z), s[r]);
+                y[6] = mul_rn(widen_lo<F16>(v[r].w), s[r]);
+                y[7] = mul_rn(widen_hi<F16>(v[r].w), s[r]);
+                uint32_t w0, w1;
+                pack8<FMT>(y, special, q.fp4_parity, q.fp4_perm, w0, w1);
+                store8<FMT>(q.data + (r0 + r) * q.ld_data + c * kOutBytes, w0, w1);
+            }
+            // lane t of the 4-lane group writes row t's scale byte
+            const int t = lane & 3;
+            const uint32_t et = t == 0 ? e[0] : t == 1 ? e[1] : t == 2 ? e[2] : e[3];
+            if (r0 + t < q.rows)
+                q.scale[scale_offset(q, r0 + t, c >> 2)] = static_cast<uint8_t>(et);
+        }
+    }
+}
+
+// ----------------------------------------------------------------- generic
+
+// Position (byte index, high nibble?) of linear nibble index n after the
+// page's lane_remap and nibble-parity rule.
+__device__ __forceinline__ int64_t remap_index(int64_t n, int stride) {
+    if (stride == 0) return n;
+    const int64_t w = 2 * stride;
+    const int64_t qq = n / w, r = n - qq * w;
+    int64_t res = w * (qq + 1) - r;
+    if ((n & 1) == 0) res -= 2;
+    return res;
+}
+
+// One thread per tile of br rows x tc columns (tc = max(bc, 8), the last
+// tile of a row may hold only 4 columns).  Every block of the tile is whole.
+template <bool F16, int FMT>
+__global__ void __launch_bounds__(kThreads) quant_generic(QuantArgs q) {
+    const int br = q.block_rows, bc = q.block_cols;
+    const int tc = bc > 8 ? bc : 8;
+    const int64_t ntc = (q.cols + tc - 1) / tc;
+    const int64_t total = (q.rows / br) * ntc;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t u = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; u < total; u += stride) {
+        const int64_t g = u / ntc, t = u - (u / ntc) * ntc;
+        const int64_t r0 = g * br, c0 = t * tc;
+        const int64_t rem = q.cols - c0;
+        const int ncols = static_cast<int>(rem < tc ? rem : tc);
+        const int nblk = ncols / bc;  // blocks across this tile (1..8)
+        uint32_t e[8];
+        bool special = false;
+        for (int b = 0; b < 8; ++b) {
+            if (b >= nblk) break;
+            uint32_t m = 0;
+            for (int dr = 0; dr < br; ++dr)
+                for (int dc = 0; dc < bc; ++dc) {
+                    uint32_t h = ld_u16(q.in + ((r0 + dr) * q.ld_in + c0 + b * bc + dc) * 2) & 0x7FFFu;
+                    m = h > m ? h : m;
+                }
+            const uint32_t x = exp_byte_of_mag<F16>(m);
+            special |= (x == 255u);
+            e[b] = e8m0_of(x, q.emax_bias);
+            q.scale[scale_offset(q, g, c0 / bc + b)] = static_cast<uint8_t>(e[b]);
+        }
+        for (int dr = 0; dr < br; ++dr) {
+            const int64_t r = r0 + dr;
+            for (int cc = 0; cc < ncols; cc += 2) {
+                const uint32_t h0 = ld_u16(q.in + (r * q.ld_in + c0 + cc) * 2);
+                const uint32_t h1 = ld_u16(q.in + (r * q.ld_in + c0 + cc + 1) * 2);
+                const float y0 = mul_rn(widen1<F16>(h0), prescale_mul(e[cc / bc]));
+                const float y1 = mul_rn(widen1<F16>(h1), prescale_mul(e[(cc + 1) / bc]));
+                if constexpr (FMT == kE2M1) {
+                    uint32_t n0, n1;
+                    if (special) { n0 = encode1<FMT>(y0); n1 = encode1<FMT>(y1); }
+                    else { uint32_t p = cvt_pair<FMT>(y0, y1); n0 = p >> 4; n1 = p & 0xFu; }
+                    const uint32_t byte = q.fp4_parity ? ((n1 << 4) | n0) : ((n0 << 4) | n1);
+                    const int64_t idx = remap_index(r * q.cols + c0 + cc, q.fp4_stride) >> 1;
+                    q.data[idx] = static_cast<uint8_t>(byte);
+                } else {
+                    uint32_t pair;
+                    if (special) pair = encode1<FMT>(y0) | (encode1<FMT>(y1) << 8);
+                    else pair = cvt_pair<FMT>(y1, y0);
+                    *reinterpret_cast<uint16_t*>(q.data + r * q.ld_data + c0 + cc) = static_cast<uint16_t>(pair);
+                }
+            }
+        }
+    }
+}
+
+template <bool F16, int FMT>
+cudaError_t launch_typed(const QuantArgs& q, cudaStream_t stream) {
+    const int sms = device_sm_count();
+    auto grid_for = [&](int64_t units) {
+        int64_t blocks = (units + kThreads - 1) / kThreads;
+        const int64_t cap = static_cast<int64_t>(sms) * 8;
+        if (blocks > cap) blocks = cap;
+        return static_cast<unsigned>(blocks < 1 ? 1 : blocks);
+    };
+    const bool wide = (q.cols % 8) == 0 && q.vec_ok;
+    if (wide && q.block_rows == 8 && q.block_cols == 4) {
+        const int64_t units = (q.rows / 8) * (q.cols / 8);
+        quant_g84<F16, FMT><<<grid_for(units), kThreads, 0, stream>>>(q);
+    } else if (wide && q.block_rows == 1 && q.block_cols == 32) {
+        const int64_t units = ((q.rows + 3) / 4) * (q.cols / 8);
+        // round the grid so each warp's 32 units stay inside one launch slot
+        quant_g1x32<F16, FMT><<<grid_for(units), kThreads, 0, stream>>>(q);
+    } else {
+        const int tc = q.block_cols > 8 ? q.block_cols : 8;
+        const int64_t units = (q.rows / q.block_rows) * ((q.cols + tc - 1) / tc);
+        quant_generic<F16, FMT><<<grid_for(units), kThreads, 0, stream>>>(q);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_quantize(const QuantArgs& q, bool in_f16, int fmt, cudaStream_t stream) {
+    if (q.rows == 0 || q.cols == 0) return cudaSuccess;
+    if (in_f16) {
+        switch (fmt) {
+        case kE4M3: return launch_typed<true, kE4M3>(q, stream);
+        case kE5M2: return launch_typed<true, kE5M2>(q, stream);
+        default: return launch_typed<true, kE2M1>(q, stream);
+        }
+    }
+    switch (fmt) {
+    case kE4M3: return launch_typed<false, kE4M3>(q, stream);
+    case kE5M2: return launch_typed<false, kE5M2>(q, stream);
+    default: return launch_typed<false, kE2M1>(q, stream);
+    }
+}
+
+}  // namespace mx

@@ -1,0 +1,163 @@
+"""The C-ABI boundary without a GPU: the library loads, exports every
+function include/mx.h declares, and rejects bad arguments with the documented
+status codes before touching the device."""
+import ctypes
+
+import pytest
+
+from helpers import header_functions
+
+
+@pytest.fixture(scope="module")
+def mx():
+    import mx_fp8_microscaling_gb300 as mx
+    return mx
+
+
+@pytest.fixture(scope="module")
+def lib(mx):
+    return mx.raw_library()
+
+
+FAKE = ctypes.c_void_p(0x10000)          # never dereferenced: every call below fails validation first
+FAKE_MISALIGNED = ctypes.c_void_p(0x10004)
+FAKE_ODD = ctypes.c_void_p(0x10001)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = header_functions()
+    assert "mx_quantize" in names and "mx_scaled_matmul" in names
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_version_and_status_strings(mx):
+    assert mx.mx_version() >= 100
+    for code, name in mx.STATUS_NAMES.items():
+        assert mx.mx_status_string(code).startswith(name)
+
+
+def test_default_cfg(mx):
+    cfg = mx.QuantCfg()
+    assert mx.raw_library().mx_quant_cfg_default(ctypes.byref(cfg)) == 0
+    assert (cfg.geometry, cfg.scale_layout, cfg.block_size, cfg.dim, cfg.scale_method,
+            cfg.fp4_lane_stride, cfg.fp4_nibble_parity, cfg.emax_alt) == (0, 0, 32, -2, 0, 2, 0, 0)
+
+
+@pytest.mark.parametrize("rows,cols,kw,expect", [
+    (64, 64, dict(geometry="8x4", dim=-2), (64 * 64, 8, 16)),
+    (64, 64, dict(geometry="8x4", dim=-1), (64 * 64, 16, 8)),
+    (64, 64, dict(geometry="1x32", dim=-1), (64 * 64, 64, 2)),
+    (64, 64, dict(geometry="1x32", dim=-2), (64 * 64, 2, 64)),
+    (8192, 8192, dict(geometry="8x4", dim=-2, scale_layout="interleave"), (8192 * 8192, 8192, 2048)),
+    (40, 64, dict(geometry="8x4", dim=-2, scale_layout="interleave"), (40 * 64, 64, 16)),
+    (200, 96, dict(geometry="1x32", dim=-1, scale_layout="sf"), (200 * 96, 256, 4)),
+])
+def test_quantize_sizes(mx, rows, cols, kw, expect):
+    cfg = mx.make_cfg(**kw)
+    assert mx.mx_quantize_sizes(rows, cols, "bf16", "e4m3fn", cfg) == expect
+
+
+def test_quantize_sizes_fp4(mx):
+    cfg = mx.make_cfg(geometry="8x4", dim=-2, scale_layout="interleave")
+    assert mx.mx_quantize_sizes(16384, 16384, "bf16", "e2m1", cfg) == (16384 * 16384 // 2, 16384, 4096)
+
+
+def _quantize_status(lib, mx, in_dtype=1, out_dtype=4, rows=64, cols=64, ld=64, cfg=None,
+                     src=FAKE, data=FAKE, scale=FAKE):
+    cfg = cfg if cfg is not None else mx.make_cfg()
+    return lib.mx_quantize(src, in_dtype, rows, cols, ld, out_dtype, ctypes.byref(cfg), data, scale, None)
+
+
+@pytest.mark.parametrize("kwargs,status", [
+    (dict(in_dtype=3), 2),                       # f32 input: only bf16/f16
+    (dict(out_dtype=7), 2),                      # e8m0 data
+    (dict(out_dtype=3), 2),
+    (dict(rows=-8), 1),
+    (dict(ld=32), 1),                            # pitch < width
+    (dict(cols=66, ld=72), 5),                   # x4 container
+    (dict(rows=12), 5),                          # 8x4 needs rows % 8
+    (dict(src=None), 1),
+    (dict(scale=None), 1),
+    (dict(src=FAKE_ODD), 6),                     # bf16 input needs 2-byte alignment
+    (dict(data=FAKE_ODD), 6),
+])
+def test_quantize_argument_errors(lib, mx, kwargs, status):
+    assert _quantize_status(lib, mx, **kwargs) == status
+
+
+@pytest.mark.parametrize("cfg_kw,status", [
+    (dict(block_size=16), 3),
+    (dict(block_size=64), 3),
+    (dict(dim=-3), 4),
+    (dict(dim=2), 4),
+    (dict(scale_method=1), 11),
+    (dict(geometry=2), 1),
+    (dict(scale_layout=3), 1),
+    (dict(scale_layout="sf"), 1),                # SF layout needs 1x32 along dim=-1
+    (dict(fp4_lane_stride=3), 1),
+    (dict(fp4_nibble_parity=2), 1),
+    (dict(emax_alt=2), 1),
+])
+def test_quantize_cfg_errors(lib, mx, cfg_kw, status):
+    cfg = mx.make_cfg(**{k: v for k, v in cfg_kw.items() if k != "emax_alt"})
+    if "emax_alt" in cfg_kw:
+        cfg.emax_alt = cfg_kw["emax_alt"]
+    assert _quantize_status(lib, mx, cfg=cfg) == status
+
+
+def test_fp4_stride_needs_window_divisibility(lib, mx):
+    cfg = mx.make_cfg(geometry="8x4", dim=-2, fp4_lane_stride=4)
+    assert _quantize_status(lib, mx, out_dtype=6, rows=8, cols=36, ld=40, cfg=cfg) == 5
+
+
+def test_empty_quantize_is_a_no_op(lib, mx):
+    assert _quantize_status(lib, mx, rows=0, src=None, data=None, scale=None) == 0
+
+
+def _matmul_status(lib, elem=4, M=128, N=128, K=128, out=3, ldc=128, a=FAKE, bt=FAKE, sa=FAKE, sb=FAKE,
+                   c=FAKE, sf=1, ws=None, ws_bytes=0):
+    return lib.mx_scaled_matmul(a, bt, sa, sb, sf, elem, M, N, K, out, c, ldc, ws, ws_bytes, None)
+
+
+@pytest.mark.parametrize("kwargs,status", [
+    (dict(elem=6), 2),          # e2m1 operands: not a ScaledMatmul target
+    (dict(elem=1), 2),
+    (dict(out=4), 2),           # output only f32 / bf16
+    (dict(K=48), 5),
+    (dict(K=0), 5),
+    (dict(M=-1), 1),
+    (dict(ldc=64), 1),
+    (dict(a=None), 1),
+    (dict(a=FAKE_MISALIGNED), 6),  # TMA needs 16-byte aligned operands
+    (dict(c=FAKE_ODD), 6),         # f32 output needs 4-byte alignment
+    (dict(sf=0), 7),            # plain scales need workspace
+    (dict(sf=0, ws=FAKE, ws_bytes=16), 7),
+])
+def test_matmul_argument_errors(lib, kwargs, status):
+    assert _matmul_status(lib, **kwargs) == status
+
+
+def test_matmul_workspace_sizes(mx):
+    # two SF buffers, each ceil(mn/128) * ceil(k/128) * 512 bytes
+    assert mx.mx_scaled_matmul_workspace(8192, 8192, 8192) == 2 * 64 * 64 * 512
+    assert mx.mx_scaled_matmul_workspace(8192, 8192, 8192, True) == 0
+    assert mx.mx_sf_layout_bytes(200, 96) == 2 * 1 * 512
+    assert mx.mx_fused_quantize_matmul_workspace(256, 512, 256) == 256 * 256 + 2 * 2 * 512
+
+
+def test_fused_argument_errors(lib):
+    st = lib.mx_fused_quantize_matmul(FAKE, 3, 128, FAKE, FAKE, 4, 128, 128, 128, 1, FAKE, 128, FAKE, 1 << 20, None)
+    assert st == 2  # x must be bf16/f16
+    st = lib.mx_fused_quantize_matmul(FAKE, 1, 128, FAKE, FAKE, 4, 128, 128, 128, 1, FAKE, 128, FAKE, 16, None)
+    assert st == 7  # workspace too small
+
+
+def test_folded_view_rules(mx):
+    import torch
+    x = torch.zeros(2, 3, 8, 32, dtype=torch.bfloat16)
+    assert mx._view2d(x, -1) == (48, 32, 32)
+    y = torch.zeros(16, 64, dtype=torch.bfloat16)[:, :32]
+    assert mx._view2d(y, -1) == (16, 32, 64)
+    with pytest.raises(ValueError):
+        mx._view2d(torch.zeros(8, 32, dtype=torch.bfloat16).t(), -1)
