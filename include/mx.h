@@ -216,6 +216,34 @@ mx_status mx_scaled_matmul(const void* a, const void* bt, const uint8_t* a_scale
                            int64_t M, int64_t N, int64_t K, mx_dtype out_dtype, void* c,
                            int64_t ldc, void* workspace, size_t workspace_bytes, mx_stream stream);
 
+/* Size of the fixed scratch array behind mx_scaled_matmul_noalloc (4 MiB). */
+#define MX_NOALLOC_SCRATCH_BYTES (4 * 1024 * 1024)
+
+/*
+ * mx_scaled_matmul with plain scales, for callers that cannot allocate device
+ * memory (no counterpart on the pages).  Some callers have no way to hand the
+ * library a workspace: a plugin driven by a host runtime that owns all device
+ * memory and gives the plugin no allocator, or a latency-critical path that
+ * must not call cudaMalloc, which can synchronise the device.  This call keeps
+ * the scratch for the two repacked scale tensors in a fixed device array
+ * inside the library instead, and calls no allocating routine.
+ *   Arguments as mx_scaled_matmul with scales_are_sf_layout = 0 and no
+ *   workspace.
+ *   Limit: the repacked scales, 16-byte rounded each, must fit in
+ *   MX_NOALLOC_SCRATCH_BYTES (4 MiB), i.e.
+ *   ceil(M/128)*ceil(K/128)*512 + ceil(N/128)*ceil(K/128)*512 <= 4 MiB
+ *   (M = N = K = 8192 fits); larger problems get MX_ERR_WORKSPACE.
+ *   The array takes 4 MiB on every device that loads the library, until
+ *   process exit.  The first call on a device looks up the array's device
+ *   address (make that first call before any stream capture on the device).
+ *   Every call shares the array: calls whose kernels may overlap on the GPU
+ *   (unordered streams) race on it; calls ordered on one stream are safe.
+ */
+mx_status mx_scaled_matmul_noalloc(const void* a, const void* bt, const uint8_t* a_scale,
+                                   const uint8_t* b_scale, mx_dtype elem_dtype, int64_t M,
+                                   int64_t N, int64_t K, mx_dtype out_dtype, void* c, int64_t ldc,
+                                   mx_stream stream);
+
 /*
  * Workspace bytes of mx_fused_quantize_matmul: the quantized activation
  * (M*K bytes) and its SF-layout scales, each 16-byte aligned.

@@ -65,6 +65,7 @@ def _load():
         "mx_repack_scales": [P, I64, I64, I64, P, P],
         "mx_scaled_matmul_workspace": [I64, I64, I64, I, PS],
         "mx_scaled_matmul": [P, P, P, P, I, I, I64, I64, I64, I, P, I64, P, SZ, P],
+        "mx_scaled_matmul_noalloc": [P, P, P, P, I, I64, I64, I64, I, P, I64, P],
         "mx_fused_quantize_matmul_workspace": [I64, I64, I64, PS],
         "mx_fused_quantize_matmul": [P, I, I64, P, P, I, I64, I64, I64, I, P, I64, P, SZ, P],
         "mx_get_device_status": [ctypes.POINTER(I)],
@@ -218,6 +219,24 @@ def mx_scaled_matmul(a: torch.Tensor, bt: torch.Tensor, a_scale: torch.Tensor, b
                                  _dev_ptr(out), out.stride(0), _dev_ptr(workspace),
                                  workspace.numel() if workspace is not None else 0, _stream(stream)),
            "mx_scaled_matmul")
+    return out
+
+
+def mx_scaled_matmul_noalloc(a: torch.Tensor, bt: torch.Tensor, a_scale: torch.Tensor, b_scale: torch.Tensor,
+                             elem_dtype: str = "e4m3fn", out_dtype: str = "f32", *,
+                             out: torch.Tensor | None = None, K: int | None = None, stream=None) -> torch.Tensor:
+    """ScaledMatmul with plain scales whose scratch lives in the library's
+    fixed device array (for callers that cannot allocate a workspace; see
+    include/mx.h).  The output tensor is still the caller's."""
+    M, Kb = a.shape
+    N = bt.shape[0]
+    K = Kb if K is None else K
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32 if out_dtype == "f32" else torch.bfloat16, device=a.device)
+    _check(_lib.mx_scaled_matmul_noalloc(_dev_ptr(a), _dev_ptr(bt), _dev_ptr(a_scale), _dev_ptr(b_scale),
+                                         DTYPES[elem_dtype], M, N, K, DTYPES[out_dtype], _dev_ptr(out),
+                                         out.stride(0), _stream(stream)),
+           "mx_scaled_matmul_noalloc")
     return out
 
 
