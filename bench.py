@@ -133,41 +133,102 @@ class ClockSampler:
 # ---------------------------------------------------------------- workloads
 
 class Timer:
-    """Accumulates CUDA-event durations per label on the current stream."""
+    """CUDA-event durations per label on the current stream.  Event pairs are
+    created up front so recording a span costs two cudaEventRecord calls."""
 
-    def __init__(self, torch):
+    def __init__(self, torch, capacity=4096):
         self.torch = torch
-        self.pending = []
+        self.events = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                       for _ in range(capacity)]
+        self.used = []
         self.totals = {}
         self.counts = {}
 
-    def span(self, label):
-        torch = self.torch
-        timer = self
-
-        class _Span:
-            def __enter__(self_inner):
-                self_inner.a = torch.cuda.Event(enable_timing=True)
-                self_inner.b = torch.cuda.Event(enable_timing=True)
-                self_inner.a.record()
-
-            def __exit__(self_inner, *exc):
-                self_inner.b.record()
-                timer.pending.append((label, self_inner.a, self_inner.b))
-        return _Span()
+    def run(self, label, fn):
+        a, b = self.events[len(self.used)]
+        a.record()
+        fn()
+        b.record()
+        self.used.append((label, a, b))
 
     def collect(self):
-        for label, a, b in self.pending:
+        for label, a, b in self.used:
             ms = a.elapsed_time(b)
             self.totals[label] = self.totals.get(label, 0.0) + ms
             self.counts[label] = self.counts.get(label, 0) + 1
-        self.pending = []
+        self.used = []
 
     def avg_ms(self, label):
         return self.totals[label] / self.counts[label]
 
     def reset(self):
-        self.pending, self.totals, self.counts = [], {}, {}
+        self.used, self.totals, self.counts = [], {}, {}
+
+
+class Api:
+    """Direct C-ABI calls with arguments marshalled once (the binding's
+    per-call conveniences cost more host time than a 35 us kernel)."""
+
+    def __init__(self, torch, mx):
+        import ctypes
+        self.torch, self.mx, self.lib, self.ct = torch, mx, mx.raw_library(), ctypes
+
+    def stream(self):
+        return self.ct.c_void_p(self.torch.cuda.current_stream().cuda_stream)
+
+    def quantize(self, x, fmt, geometry, dim, layout, data, scale):
+        mx, ct = self.mx, self.ct
+        rows, cols, ld = mx._view2d(x, dim)
+        cfg = mx.make_cfg(geometry, dim, layout)
+        args = (ct.c_void_p(x.data_ptr()), mx.DTYPES[mx._in_dtype(x)], rows, cols, ld, mx.DTYPES[fmt],
+                ct.byref(cfg), ct.c_void_p(data.data_ptr()), ct.c_void_p(scale.data_ptr()), self.stream())
+        fn = self.lib.mx_quantize
+
+        def call():
+            st = fn(*args)
+            if st:
+                raise mx.MxError(st, "mx_quantize")
+        call.cfg = cfg  # keep the struct alive
+        return call
+
+    def repack(self, plain, k, sf):
+        mx, ct = self.mx, self.ct
+        args = (ct.c_void_p(plain.data_ptr()), plain.shape[0], k, plain.stride(0), ct.c_void_p(sf.data_ptr()),
+                self.stream())
+        fn = self.lib.mx_repack_scales
+
+        def call():
+            st = fn(*args)
+            if st:
+                raise mx.MxError(st, "mx_repack_scales")
+        return call
+
+    def matmul_sf(self, a, bt, sfa, sfb, fmt, out_dtype, c, K):
+        mx, ct = self.mx, self.ct
+        args = (ct.c_void_p(a.data_ptr()), ct.c_void_p(bt.data_ptr()), ct.c_void_p(sfa.data_ptr()),
+                ct.c_void_p(sfb.data_ptr()), 1, mx.DTYPES[fmt], a.shape[0], bt.shape[0], K, mx.DTYPES[out_dtype],
+                ct.c_void_p(c.data_ptr()), c.stride(0), None, 0, self.stream())
+        fn = self.lib.mx_scaled_matmul
+
+        def call():
+            st = fn(*args)
+            if st:
+                raise mx.MxError(st, "mx_scaled_matmul")
+        return call
+
+    def fused(self, x, wt, wsf, fmt, out_dtype, c, work):
+        mx, ct = self.mx, self.ct
+        M, K = x.shape
+        args = (ct.c_void_p(x.data_ptr()), mx.DTYPES[mx._in_dtype(x)], x.stride(0), ct.c_void_p(wt.data_ptr()),
+                ct.c_void_p(wsf.data_ptr()), mx.DTYPES[fmt], M, wt.shape[0], K, mx.DTYPES[out_dtype],
+                ct.c_void_p(c.data_ptr()), c.stride(0), ct.c_void_p(work.data_ptr()), work.numel(), self.stream())
+        fn = self.lib.mx_fused_quantize_matmul
+
+        def call():
+            st = fn(*args)
+            if st:
+                raise mx.MxError(st, "mx_fused_quantize_matmul")
+        return call
 
 
 def dev_bits(torch, bits, in_dtype):
@@ -176,85 +237,78 @@ def dev_bits(torch, bits, in_dtype):
 
 
 class Sweep:
-    def __init__(self, torch, mx):
+    def __init__(self, torch, mx, api):
         self.mx, self.torch = mx, torch
         self.host, self.x, self.out = {}, {}, {}
         for in_dtype, fmt in SWEEP_VARIANTS:
             bits = syn.sweep_input(*SWEEP, in_dtype, fmt, seed=0)
             self.host[(in_dtype, fmt)] = bits
             self.x[(in_dtype, fmt)] = dev_bits(torch, bits, in_dtype)
+        self.ops = []
+        # layouts outermost: consecutive launches read different 128 MiB inputs
         for layout in ("plain", "interleave"):
             for in_dtype, fmt in SWEEP_VARIANTS:
                 cfg = mx.make_cfg("8x4", -2, layout)
                 _, sr, sc = mx.mx_quantize_sizes(*SWEEP, in_dtype, fmt, cfg)
-                self.out[(layout, in_dtype, fmt)] = (
-                    torch.empty(SWEEP[0] * SWEEP[1], dtype=torch.uint8, device="cuda"),
-                    torch.empty(sr * sc, dtype=torch.uint8, device="cuda"))
+                d = torch.empty(SWEEP[0] * SWEEP[1], dtype=torch.uint8, device="cuda")
+                s = torch.empty(sr * sc, dtype=torch.uint8, device="cuda")
+                self.out[(layout, in_dtype, fmt)] = (d, s)
+                self.ops.append(("sweep", api.quantize(self.x[(in_dtype, fmt)], fmt, "8x4", -2, layout, d, s)))
         self.launches = 8
 
     def step(self, timer):
-        # layouts outermost: consecutive launches read different 128 MiB inputs
-        for layout in ("plain", "interleave"):
-            for in_dtype, fmt in SWEEP_VARIANTS:
-                d, s = self.out[(layout, in_dtype, fmt)]
-                with timer.span("sweep"):
-                    self.mx.mx_quantize(self.x[(in_dtype, fmt)], fmt, geometry="8x4", dim=-2,
-                                        scale_layout=layout, out_data=d, out_scale=s)
+        for label, fn in self.ops:
+            timer.run(label, fn)
 
 
 class Gemm:
     CASES = [("e4m3fn", "bf16"), ("e5m2", "f32")]
 
-    def __init__(self, torch, mx):
-        self.mx, self.torch = mx, torch
+    def __init__(self, torch, mx, api):
         a_bits, b_bits = syn.gemm_operands(GEMM_N, GEMM_N, GEMM_N, seed=0)
-        self.a = dev_bits(torch, a_bits, "bf16")
-        self.b = dev_bits(torch, b_bits, "bf16")
+        a = dev_bits(torch, a_bits, "bf16")
+        b = dev_bits(torch, b_bits, "bf16")
         n = GEMM_N
-        self.qa = torch.empty((n, n), dtype=torch.uint8, device="cuda")
-        self.qb = torch.empty((n, n), dtype=torch.uint8, device="cuda")
-        self.sa = torch.empty((n, n // 32), dtype=torch.uint8, device="cuda")
-        self.sb = torch.empty((n, n // 32), dtype=torch.uint8, device="cuda")
+        qa = torch.empty((n, n), dtype=torch.uint8, device="cuda")
+        qb = torch.empty((n, n), dtype=torch.uint8, device="cuda")
+        sa = torch.empty((n, n // 32), dtype=torch.uint8, device="cuda")
+        sb = torch.empty((n, n // 32), dtype=torch.uint8, device="cuda")
         sfb = mx.mx_sf_layout_bytes(n, n)
-        self.sfa = torch.empty(sfb, dtype=torch.uint8, device="cuda")
-        self.sfb = torch.empty(sfb, dtype=torch.uint8, device="cuda")
+        sfa_t = torch.empty(sfb, dtype=torch.uint8, device="cuda")
+        sfb_t = torch.empty(sfb, dtype=torch.uint8, device="cuda")
+        self.keep = (a, b, qa, qb, sa, sb, sfa_t, sfb_t)
         self.c = {"bf16": torch.empty((n, n), dtype=torch.bfloat16, device="cuda"),
                   "f32": torch.empty((n, n), dtype=torch.float32, device="cuda")}
+        self.ops = []
+        for fmt, out in self.CASES:
+            self.ops.append(("gemm_quantize", api.quantize(a, fmt, "1x32", -1, "plain", qa, sa)))
+            self.ops.append(("gemm_quantize", api.quantize(b, fmt, "1x32", -1, "plain", qb, sb)))
+            self.ops.append(("gemm_repack", api.repack(sa, n, sfa_t)))
+            self.ops.append(("gemm_repack", api.repack(sb, n, sfb_t)))
+            self.ops.append((f"gemm_{fmt}_{out}", api.matmul_sf(qa, qb, sfa_t, sfb_t, fmt, out, self.c[out], n)))
         self.launches = 2 * (2 + 2 + 1)
 
     def step(self, timer):
-        mx = self.mx
-        for fmt, out in self.CASES:
-            with timer.span("gemm_quantize"):
-                mx.mx_quantize(self.a, fmt, geometry="1x32", dim=-1, out_data=self.qa, out_scale=self.sa)
-                mx.mx_quantize(self.b, fmt, geometry="1x32", dim=-1, out_data=self.qb, out_scale=self.sb)
-            with timer.span("gemm_repack"):
-                mx.mx_repack_scales(self.sa, GEMM_N, out=self.sfa)
-                mx.mx_repack_scales(self.sb, GEMM_N, out=self.sfb)
-            with timer.span(f"gemm_{fmt}_{out}"):
-                mx.mx_scaled_matmul(self.qa, self.qb, self.sfa, self.sfb, fmt, out, scales_are_sf_layout=True,
-                                    out=self.c[out], K=GEMM_N)
+        for label, fn in self.ops:
+            timer.run(label, fn)
 
 
 class Fp4:
-    def __init__(self, torch, mx):
-        self.mx = mx
+    def __init__(self, torch, mx, api):
         self.x = dev_bits(torch, syn.fp4_input(*FP4_SHAPE, seed=0), "bf16")
         cfg = mx.make_cfg("8x4", -2, "interleave")
         db, sr, sc = mx.mx_quantize_sizes(*FP4_SHAPE, "bf16", "e2m1", cfg)
         self.d = torch.empty(db, dtype=torch.uint8, device="cuda")
         self.s = torch.empty(sr * sc, dtype=torch.uint8, device="cuda")
+        self.op = api.quantize(self.x, "e2m1", "8x4", -2, "interleave", self.d, self.s)
         self.launches = 1
 
     def step(self, timer):
-        with timer.span("fp4"):
-            self.mx.mx_quantize(self.x, "e2m1", geometry="8x4", dim=-2, scale_layout="interleave",
-                                out_data=self.d, out_scale=self.s)
+        timer.run("fp4", self.op)
 
 
 class Fused:
-    def __init__(self, torch, mx):
-        self.mx = mx
+    def __init__(self, torch, mx, api):
         M, N, K = FUSED
         x_bits, w_bits = syn.fused_operands(M, N, K, seed=0)
         self.x = dev_bits(torch, x_bits, "bf16")
@@ -266,12 +320,11 @@ class Fused:
         del wt
         self.c = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
         self.work = torch.empty(mx.mx_fused_quantize_matmul_workspace(M, N, K), dtype=torch.uint8, device="cuda")
+        self.op = api.fused(self.x, self.wq, self.ws, "e4m3fn", "bf16", self.c, self.work)
         self.launches = 2
 
     def step(self, timer):
-        with timer.span("fused"):
-            self.mx.mx_fused_quantize_matmul(self.x, self.wq, self.ws, "e4m3fn", "bf16", out=self.c,
-                                             workspace=self.work)
+        timer.run("fused", self.op)
 
 
 # ------------------------------------------------------------- CPU oracle
@@ -401,12 +454,14 @@ def main():
     parts = {}
     want = ["sweep", "gemm", "fp4", "fused"] if args.workload == "all" else [args.workload]
     builders = {"sweep": Sweep, "gemm": Gemm, "fp4": Fp4, "fused": Fused}
+    api = Api(torch, mx)
     for name in want:
-        parts[name] = builders[name](torch, mx)
+        parts[name] = builders[name](torch, mx, api)
     torch.cuda.synchronize()
     launches_per_step = sum(p.launches for p in parts.values())
 
-    timer = Timer(torch)
+    timer = Timer(torch, capacity=max(args.steps, args.warmup) * sum(
+        len(getattr(p, "ops", [None])) for p in parts.values()) + 64)
     for _ in range(args.warmup):
         for p in parts.values():
             p.step(timer)
