@@ -289,6 +289,14 @@ int mx_version(void);
  */
 mx_status mx_debug_gemm_fault_injection(int skip_producer, uint64_t timeout_ns);
 
+/*
+ * Testing hook (no counterpart on the pages): which ScaledMatmul kernel later
+ * calls use.  0 = automatic (the 2-SM pair kernel when M > 128, else the
+ * 1-SM kernel), 1 = always the 1-SM kernel, 2 = always the pair kernel.
+ * Both give results within the same tolerance.  Not thread-safe; host only.
+ */
+mx_status mx_debug_set_gemm_variant(int variant);
+
 #ifdef __cplusplus
 }
 #endif

@@ -72,6 +72,7 @@ def _load():
         "mx_status_string": [I],
         "mx_version": [],
         "mx_debug_gemm_fault_injection": [I, ctypes.c_uint64],
+        "mx_debug_set_gemm_variant": [I],
     }
     for name, args in sigs.items():
         fn = getattr(lib, name)
@@ -281,6 +282,11 @@ def mx_version() -> int:
 
 def mx_debug_gemm_fault_injection(skip_producer: bool, timeout_ns: int = 0):
     _check(_lib.mx_debug_gemm_fault_injection(int(skip_producer), timeout_ns), "mx_debug_gemm_fault_injection")
+
+
+def mx_debug_set_gemm_variant(variant: int):
+    """0 automatic, 1 force the 1-SM ScaledMatmul kernel, 2 force the 2-SM pair kernel."""
+    _check(_lib.mx_debug_set_gemm_variant(int(variant)), "mx_debug_set_gemm_variant")
 
 
 def raw_library() -> ctypes.CDLL:

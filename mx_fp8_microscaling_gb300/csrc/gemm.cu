@@ -6,23 +6,35 @@
 // the scale is applied as 2^(E8M0 - 127), the inverse of the quantizer's
 // prescale, page "MX Microscaling", quantizeDataApplyingMxScales NOTE.)
 //
-// Design (one CTA per SM, persistent over 128 x 256 output tiles):
-//   warp 0      TMA producer: per 128-wide K block, one 2-D TMA load of the
-//               A tile (128 x 128 B) and of the B tile (256 x 128 B), both
-//               128-byte swizzled, plus three 512-byte bulk copies of the
-//               scale-factor tiles, into a 4-stage shared-memory ring.
+// Two persistent, warp-specialised kernels share one structure (one CTA per
+// SM, 320 threads):
+//   warp 0      TMA producer: per 128-wide K block, 2-D TMA loads of the
+//               operand tiles (128-byte swizzle) and of the scale-factor
+//               tiles into a ring of shared-memory stages.
 //   warp 1      MMA issuer (one thread): tcgen05.cp moves the stage's scale
 //               tiles into tensor memory, then four
-//               tcgen05.mma.kind::mxf8f6f4.block_scale (M=128, N=256, K=32)
-//               accumulate into a 128 x 256 f32 tile in tensor memory;
+//               tcgen05.mma.kind::mxf8f6f4.block_scale (K = 32 each)
+//               accumulate into an f32 tile in tensor memory;
 //               tcgen05.commit frees the stage / hands the tile over.
 //   warps 2-9   epilogue: tcgen05.ld the accumulator (each warp its TMEM lane
-//               quarter and one 128-column half), release tensor memory to the
-//               MMA warp, then convert (f32 or bf16, round to nearest even) and
-//               store rows straight to global memory while the next tile's
-//               main loop runs.
+//               quarter and one 128-column half), release tensor memory, then
+//               convert (f32, or bf16 round-to-nearest-even) and store rows to
+//               global memory while the next tile's main loop runs.
+//
+//   mx_gemm_kernel      1 SM per 128 x 256 tile (M = 128 MMA), 4 stages of
+//                       A 16 KB + B 32 KB + scales 1.5 KB.  Used for M <= 128.
+//   mx_gemm_2sm_kernel  a cluster of 2 CTAs per 256 x 256 tile with the pair
+//                       MMA (cta_group::2, M = 256): each CTA loads its own
+//                       128 rows of A and 128 rows of B, so each SM takes in
+//                       32 KB of operands per K block instead of 48 KB.
+//                       6 stages.  Rank 0 issues the MMAs; both CTAs' loads
+//                       complete on rank 0's barriers.
+//
 // Tensor memory (512 columns): accumulator in columns 0..255, scale factors
-// of pipeline stage s at 256 + 16 s (A: 4 columns, B: 8 columns).
+// of stage s at 256 + 16 s (A: 4 columns, B: 8 columns).  The scale-factor
+// tile for 128 rows is 512 bytes (row r at byte (r%32)*16 + (r/32)*4 + kblock),
+// the layout one tcgen05.cp.32x128b.warpx4 moves into a 4-column group.
+//
 // Every mbarrier wait is bounded (2 s of wall clock by default); a wait that
 // gives up records MX_ERR_TIMEOUT in the device status word and all roles
 // leave their loops, wait for their own asynchronous work, free tensor memory
@@ -47,26 +59,11 @@ namespace {
 
 using namespace dev;
 
-constexpr int BM = 128, BN = 256, BK = 128;
-constexpr int STAGES = 4;
+constexpr int BK = 128;
 constexpr int NUM_EPI_WARPS = 8;
 constexpr int NUM_THREADS = 64 + NUM_EPI_WARPS * 32;
-constexpr uint32_t A_STAGE = BM * BK;   // 16 KB
-constexpr uint32_t B_STAGE = BN * BK;   // 32 KB
-constexpr uint32_t SFA_STAGE = 512;
-constexpr uint32_t SFB_STAGE = 1024;
-constexpr uint32_t OFF_A = 0;
-constexpr uint32_t OFF_B = OFF_A + STAGES * A_STAGE;
-constexpr uint32_t OFF_SFA = OFF_B + STAGES * B_STAGE;
-constexpr uint32_t OFF_SFB = OFF_SFA + STAGES * SFA_STAGE;
-constexpr uint32_t OFF_BAR = OFF_SFB + STAGES * SFB_STAGE;
-constexpr int NUM_BARS = 2 * STAGES + 3;  // full[S], empty[S], tmem_full, tmem_empty, mma_done
-constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
-constexpr uint32_t SMEM_BYTES = OFF_MISC + 16;
-constexpr uint32_t SMEM_ALLOC = SMEM_BYTES + 1024;  // slack to align the base to 1024
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TMEM_SF = 256;
-constexpr uint32_t STAGE_TX = A_STAGE + B_STAGE + SFA_STAGE + SFB_STAGE;
 
 struct KParams {
     const uint8_t* sfa;
@@ -84,6 +81,8 @@ struct KParams {
     int skip_producer;   // fault injection: never issue loads (waits must time out)
 };
 
+// Tile order: groups of `group_m` M-tiles, column-major inside a group, so
+// the tiles running at once share A and B panels in L2.
 __device__ __forceinline__ void tile_coords(int t, const KParams& p, int& mt, int& nt) {
     const int group = p.group_m * p.num_n_tiles;
     const int g = t / group;
@@ -100,9 +99,76 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return r;
 }
 
+// Store one accumulator row segment: row m, columns [n0, n0 + 128).
+__device__ __forceinline__ void store_row128(const KParams& p, int64_t m, int64_t n0, const uint32_t (&v)[4][32]) {
+    if (m >= p.M || n0 >= p.N) return;
+    if (p.out_bf16) {
+        uint16_t* crow = reinterpret_cast<uint16_t*>(p.c) + m * p.ldc + n0;
+        if (p.vec_store && n0 + 128 <= p.N) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    uint4 w;
+                    w.x = pack_bf16x2(__uint_as_float(v[j][8 * q + 0]), __uint_as_float(v[j][8 * q + 1]));
+                    w.y = pack_bf16x2(__uint_as_float(v[j][8 * q + 2]), __uint_as_float(v[j][8 * q + 3]));
+                    w.z = pack_bf16x2(__uint_as_float(v[j][8 * q + 4]), __uint_as_float(v[j][8 * q + 5]));
+                    w.w = pack_bf16x2(__uint_as_float(v[j][8 * q + 6]), __uint_as_float(v[j][8 * q + 7]));
+                    *reinterpret_cast<uint4*>(crow + 32 * j + 8 * q) = w;
+                }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    if (n0 + 32 * j + i < p.N)
+                        crow[32 * j + i] =
+                            static_cast<uint16_t>(pack_bf16x2(__uint_as_float(v[j][i]), 0.0f) & 0xFFFFu);
+        }
+    } else {
+        float* crow = reinterpret_cast<float*>(p.c) + m * p.ldc + n0;
+        if (p.vec_store && n0 + 128 <= p.N) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    *reinterpret_cast<uint4*>(crow + 32 * j + 4 * q) =
+                        make_uint4(v[j][4 * q], v[j][4 * q + 1], v[j][4 * q + 2], v[j][4 * q + 3]);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    if (n0 + 32 * j + i < p.N) crow[32 * j + i] = __uint_as_float(v[j][i]);
+        }
+    }
+}
+
+// ====================================================== 1-SM, 128 x 256 tiles
+
+namespace sm1 {
+constexpr int BM = 128, BN = 256;
+constexpr int STAGES = 4;
+constexpr uint32_t A_STAGE = BM * BK;   // 16 KB
+constexpr uint32_t B_STAGE = BN * BK;   // 32 KB
+constexpr uint32_t SFA_STAGE = 512;
+constexpr uint32_t SFB_STAGE = 1024;
+constexpr uint32_t OFF_A = 0;
+constexpr uint32_t OFF_B = OFF_A + STAGES * A_STAGE;
+constexpr uint32_t OFF_SFA = OFF_B + STAGES * B_STAGE;
+constexpr uint32_t OFF_SFB = OFF_SFA + STAGES * SFA_STAGE;
+constexpr uint32_t OFF_BAR = OFF_SFB + STAGES * SFB_STAGE;
+constexpr int NUM_BARS = 2 * STAGES + 3;  // full[S], empty[S], tmem_full, tmem_empty, mma_done
+constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
+constexpr uint32_t SMEM_BYTES = OFF_MISC + 16;
+constexpr uint32_t SMEM_ALLOC = SMEM_BYTES + 1024;  // slack to align the base to 1024
+constexpr uint32_t STAGE_TX = A_STAGE + B_STAGE + SFA_STAGE + SFB_STAGE;
+}  // namespace sm1
+
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     mx_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                    const KParams p) {
+    using namespace sm1;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sb = smem_u32(smem);
@@ -249,50 +315,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(tmem_empty);
             acc_phase ^= 1u;
-
-            const int64_t m = static_cast<int64_t>(mt) * BM + quarter * 32 + lane;
-            const int64_t n0 = static_cast<int64_t>(nt) * BN + half * 128;
-            if (m >= p.M || n0 >= p.N) continue;
-            if (p.out_bf16) {
-                uint16_t* crow = reinterpret_cast<uint16_t*>(p.c) + m * p.ldc + n0;
-                if (p.vec_store && n0 + 128 <= p.N) {
-#pragma unroll
-                    for (int j = 0; j < 4; ++j)
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            uint4 w;
-                            w.x = pack_bf16x2(__uint_as_float(v[j][8 * q + 0]), __uint_as_float(v[j][8 * q + 1]));
-                            w.y = pack_bf16x2(__uint_as_float(v[j][8 * q + 2]), __uint_as_float(v[j][8 * q + 3]));
-                            w.z = pack_bf16x2(__uint_as_float(v[j][8 * q + 4]), __uint_as_float(v[j][8 * q + 5]));
-                            w.w = pack_bf16x2(__uint_as_float(v[j][8 * q + 6]), __uint_as_float(v[j][8 * q + 7]));
-                            *reinterpret_cast<uint4*>(crow + 32 * j + 8 * q) = w;
-                        }
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 4; ++j)
-#pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            if (n0 + 32 * j + i < p.N)
-                                crow[32 * j + i] = static_cast<uint16_t>(
-                                    pack_bf16x2(__uint_as_float(v[j][i]), 0.0f) & 0xFFFFu);
-                }
-            } else {
-                float* crow = reinterpret_cast<float*>(p.c) + m * p.ldc + n0;
-                if (p.vec_store && n0 + 128 <= p.N) {
-#pragma unroll
-                    for (int j = 0; j < 4; ++j)
-#pragma unroll
-                        for (int q = 0; q < 8; ++q)
-                            *reinterpret_cast<uint4*>(crow + 32 * j + 4 * q) =
-                                make_uint4(v[j][4 * q], v[j][4 * q + 1], v[j][4 * q + 2], v[j][4 * q + 3]);
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 4; ++j)
-#pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            if (n0 + 32 * j + i < p.N) crow[32 * j + i] = __uint_as_float(v[j][i]);
-                }
-            }
+            store_row128(p, static_cast<int64_t>(mt) * BM + quarter * 32 + lane,
+                         static_cast<int64_t>(nt) * BN + half * 128, v);
         }
     }
 
@@ -300,6 +324,199 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     __syncthreads();
     tc_fence_after();
     if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
+}
+
+// ================================================ 2-SM pair, 256 x 256 tiles
+
+namespace sm2 {
+constexpr int BM = 256, BN = 256;        // pair tile; each CTA holds 128 rows of A and of B
+constexpr int STAGES = 6;
+constexpr uint32_t A_STAGE = 128 * BK;   // 16 KB
+constexpr uint32_t B_STAGE = 128 * BK;   // 16 KB
+constexpr uint32_t SFA_STAGE = 512;      // this CTA's 128 rows of A
+constexpr uint32_t SFB_STAGE = 1024;     // all 256 rows of B (both CTAs need them)
+constexpr uint32_t OFF_A = 0;
+constexpr uint32_t OFF_B = OFF_A + STAGES * A_STAGE;
+constexpr uint32_t OFF_SFA = OFF_B + STAGES * B_STAGE;
+constexpr uint32_t OFF_SFB = OFF_SFA + STAGES * SFA_STAGE;
+constexpr uint32_t OFF_BAR = OFF_SFB + STAGES * SFB_STAGE;
+constexpr int NUM_BARS = 2 * STAGES + 3;
+constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
+constexpr uint32_t SMEM_BYTES = OFF_MISC + 16;
+constexpr uint32_t SMEM_ALLOC = SMEM_BYTES + 1024;
+constexpr uint32_t CTA_TX = A_STAGE + B_STAGE + SFA_STAGE + SFB_STAGE;
+constexpr uint32_t PAIR_TX = 2 * CTA_TX;
+}  // namespace sm2
+
+// Scale-factor buffers are read by TMA as [2 * tiles, 256] bytes: a 512-byte
+// tile t is rows 2t and 2t+1 (box 256 x 2); tiles past the end read as zeros.
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    mx_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                       const __grid_constant__ CUtensorMap tmap_sfa, const __grid_constant__ CUtensorMap tmap_sfb,
+                       const KParams p) {
+    using namespace sm2;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sb = smem_u32(smem);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const int cluster = blockIdx.x >> 1, num_clusters = gridDim.x >> 1;
+
+    auto full_bar = [&](int s) { return sb + OFF_BAR + 8u * s; };
+    auto empty_bar = [&](int s) { return sb + OFF_BAR + 8u * (STAGES + s); };
+    const uint32_t tmem_full = sb + OFF_BAR + 8u * (2 * STAGES);
+    const uint32_t tmem_empty = tmem_full + 8;
+    const uint32_t mma_done = tmem_full + 16;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full_bar(s), 1);     // rank 0's: its arrive + both CTAs' bytes
+            mbar_init(empty_bar(s), 1);    // one multicast commit per use
+        }
+        mbar_init(tmem_full, 1);
+        mbar_init(tmem_empty, 2 * NUM_EPI_WARPS);  // rank 0's: both CTAs' epilogue warps
+        mbar_init(mma_done, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        prefetch_tmap(&tmap_a);
+        prefetch_tmap(&tmap_b);
+        prefetch_tmap(&tmap_sfa);
+        prefetch_tmap(&tmap_sfb);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(smem_u32(tmem_slot), TMEM_COLS);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();  // the peer's barriers are initialised before any remote use
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const int num_tiles = p.num_m_tiles * p.num_n_tiles;  // pair tiles
+
+    if (warp == 0) {
+        if (lane == 0 && !p.skip_producer) {
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int t = cluster; t < num_tiles && ok; t += num_clusters) {
+                int mt, nt;
+                tile_coords(t, p, mt, nt);
+                const int a_row = mt * BM + static_cast<int>(rank) * 128;
+                const int b_row = nt * BN + static_cast<int>(rank) * 128;
+                const int sfa_tile = 2 * mt + static_cast<int>(rank);
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, p.timeout_ns, &g_mx_status)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = mapa_shared(full_bar(stage), 0);
+                    if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), PAIR_TX);
+                    tma_load_2d_pair(sb + OFF_A + stage * A_STAGE, &tmap_a, fb, kb * BK, a_row);
+                    tma_load_2d_pair(sb + OFF_B + stage * B_STAGE, &tmap_b, fb, kb * BK, b_row);
+                    tma_load_2d_pair(sb + OFF_SFA + stage * SFA_STAGE, &tmap_sfa, fb, 0,
+                                     2 * (sfa_tile * p.num_kb + kb));
+                    tma_load_2d_pair(sb + OFF_SFB + stage * SFB_STAGE, &tmap_sfb, fb, 0,
+                                     2 * ((2 * nt) * p.num_kb + kb));
+                    tma_load_2d_pair(sb + OFF_SFB + stage * SFB_STAGE + 512u, &tmap_sfb, fb, 0,
+                                     2 * ((2 * nt + 1) * p.num_kb + kb));
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (rank == 0) {
+                // rank 0's full barriers count both CTAs' bytes: once the last
+                // STAGES fills have completed, no copy of the pair is in flight
+                for (int i = 0; i < STAGES; ++i) {
+                    if (--stage < 0) {
+                        stage = STAGES - 1;
+                        phase ^= 1u;
+                    }
+                    volatile int no_abort = 0;
+                    (void)mbar_wait_bounded(full_bar(stage), phase, &no_abort, 100000000ull, &g_mx_status);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && rank == 0) {
+            int stage = 0;
+            uint32_t phase = 0, acc_phase = 0;
+            bool ok = true;
+            for (int t = cluster; t < num_tiles && ok; t += num_clusters) {
+                if (!mbar_wait_bounded(tmem_empty, acc_phase ^ 1u, abort_flag, p.timeout_ns, &g_mx_status)) break;
+                tc_fence_after();
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    if (!mbar_wait_bounded(full_bar(stage), phase, abort_flag, p.timeout_ns, &g_mx_status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sfa_t = tmem_base + TMEM_SF + 16u * stage;
+                    const uint32_t sfb_t = sfa_t + 4u;
+                    const uint32_t s_sfa = sb + OFF_SFA + stage * SFA_STAGE;
+                    const uint32_t s_sfb = sb + OFF_SFB + stage * SFB_STAGE;
+                    tc_cp_pair_32x128b_warpx4(sfa_t, sdesc_sf_tile(s_sfa));
+                    tc_cp_pair_32x128b_warpx4(sfb_t, sdesc_sf_tile(s_sfb));
+                    tc_cp_pair_32x128b_warpx4(sfb_t + 4u, sdesc_sf_tile(s_sfb + 512u));
+                    const uint32_t sa = sb + OFF_A + stage * A_STAGE;
+                    const uint32_t sbb = sb + OFF_B + stage * B_STAGE;
+#pragma unroll
+                    for (int kk = 0; kk < BK / 32; ++kk) {
+                        const uint32_t idesc = p.idesc | (static_cast<uint32_t>(kk) << 4) |
+                                               (static_cast<uint32_t>(kk) << 29);
+                        tc_mma_mxf8_pair(tmem_base, sdesc_kmajor_sw128(sa + kk * 32),
+                                         sdesc_kmajor_sw128(sbb + kk * 32), idesc, sfa_t, sfb_t, (kb | kk) != 0);
+                    }
+                    tc_commit_pair_mc(empty_bar(stage), 3);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                tc_commit_pair_mc(tmem_full, 3);
+                acc_phase ^= 1u;
+            }
+            tc_commit_pair_mc(mma_done, 3);
+            volatile int no_abort = 0;
+            (void)mbar_wait_bounded(mma_done, 0, &no_abort, 100000000ull, &g_mx_status);
+        }
+    } else {
+        const int quarter = warp & 3;
+        const int half = (warp - 2) >> 2;
+        const uint32_t tmem_empty_rank0 = mapa_shared(tmem_empty, 0);
+        uint32_t acc_phase = 0;
+        for (int t = cluster; t < num_tiles; t += num_clusters) {
+            int mt, nt;
+            tile_coords(t, p, mt, nt);
+            bool ok = true;
+            if (lane == 0) ok = mbar_wait_bounded(tmem_full, acc_phase, abort_flag, p.timeout_ns, &g_mx_status);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            tc_fence_after();
+            uint32_t v[4][32];
+            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + half * 128;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) tmem_ld_32x32b_x32(taddr + 32u * j, v[j]);
+            tmem_wait_ld();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(tmem_empty_rank0);
+            acc_phase ^= 1u;
+            store_row128(p, static_cast<int64_t>(mt) * BM + rank * 128 + quarter * 32 + lane,
+                         static_cast<int64_t>(nt) * BN + half * 128, v);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();  // neither CTA frees its memories while the pair may still use them
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc_pair(tmem_base, TMEM_COLS);
 }
 
 // ------------------------------------------------------------------- host
@@ -332,28 +549,25 @@ bool make_operand_map(CUtensorMap* map, const void* base, int64_t rows, int64_t 
     return r == CUDA_SUCCESS;
 }
 
-uint64_t g_timeout_ns = 2000000000ull;
-int g_fault_skip_producer = 0;
-
-}  // namespace
-
-void set_gemm_fault_injection(int skip_producer, uint64_t timeout_ns) {
-    g_fault_skip_producer = skip_producer;
-    g_timeout_ns = timeout_ns ? timeout_ns : 2000000000ull;
+// A scale-factor buffer of `tiles` 512-byte tiles as [2 * tiles, 256] bytes, box 256 x 2.
+bool make_sf_map(CUtensorMap* map, const void* base, int64_t tiles) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {256, static_cast<cuuint64_t>(2 * tiles)};
+    cuuint64_t strides[1] = {256};
+    cuuint32_t box[2] = {256, 2};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
 }
 
-cudaError_t launch_scaled_matmul(const GemmArgs& g, cudaStream_t stream) {
-    static std::once_flag attr_once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(attr_once, [] {
-        attr_err = cudaFuncSetAttribute(mx_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
-    });
-    if (attr_err != cudaSuccess) return attr_err;
+uint64_t g_timeout_ns = 2000000000ull;
+int g_fault_skip_producer = 0;
+int g_variant = 0;  // 0 automatic, 1 force the 1-SM kernel, 2 force the 2-SM kernel
 
-    CUtensorMap ma, mb;
-    if (!make_operand_map(&ma, g.a, g.M, g.K, BM) || !make_operand_map(&mb, g.bt, g.N, g.K, BN))
-        return cudaErrorInvalidValue;
-
+KParams base_params(const GemmArgs& g, int bm, int bn) {
     KParams p{};
     p.sfa = g.sfa;
     p.sfb = g.sfb;
@@ -364,20 +578,104 @@ cudaError_t launch_scaled_matmul(const GemmArgs& g, cudaStream_t stream) {
     p.K = static_cast<int>(g.K);
     p.out_bf16 = g.out_bf16;
     p.vec_store = g.vec_store;
-    p.num_m_tiles = static_cast<int>((g.M + BM - 1) / BM);
-    p.num_n_tiles = static_cast<int>((g.N + BN - 1) / BN);
+    p.num_m_tiles = static_cast<int>((g.M + bm - 1) / bm);
+    p.num_n_tiles = static_cast<int>((g.N + bn - 1) / bn);
     p.num_kb = static_cast<int>((g.K + BK - 1) / BK);
     p.num_sf_n_tiles = static_cast<int>((g.N + 127) / 128);
     p.group_m = 16;
-    p.idesc = make_idesc_mxf8(g.elem_fmt, g.elem_fmt, BM, BN);
+    p.idesc = make_idesc_mxf8(g.elem_fmt, g.elem_fmt, bm, bn);
     p.timeout_ns = g_timeout_ns;
     p.skip_producer = g_fault_skip_producer;
+    return p;
+}
 
+cudaError_t launch_1sm(const GemmArgs& g, cudaStream_t stream) {
+    static std::once_flag attr_once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(attr_once, [] {
+        attr_err = cudaFuncSetAttribute(mx_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, sm1::SMEM_ALLOC);
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+    CUtensorMap ma, mb;
+    if (!make_operand_map(&ma, g.a, g.M, g.K, sm1::BM) || !make_operand_map(&mb, g.bt, g.N, g.K, sm1::BN))
+        return cudaErrorInvalidValue;
+    KParams p = base_params(g, sm1::BM, sm1::BN);
     const int tiles = p.num_m_tiles * p.num_n_tiles;
     const int sms = device_sm_count();
     const int grid = tiles < sms ? tiles : sms;
-    mx_gemm_kernel<<<grid, NUM_THREADS, SMEM_ALLOC, stream>>>(ma, mb, p);
+    mx_gemm_kernel<<<grid, NUM_THREADS, sm1::SMEM_ALLOC, stream>>>(ma, mb, p);
     return cudaGetLastError();
+}
+
+void pair_launch_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, int clusters, cudaStream_t stream) {
+    *cfg = cudaLaunchConfig_t{};
+    cfg->gridDim = dim3(2 * clusters, 1, 1);
+    cfg->blockDim = dim3(NUM_THREADS, 1, 1);
+    cfg->dynamicSmemBytes = sm2::SMEM_ALLOC;
+    cfg->stream = stream;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg->attrs = attr;
+    cfg->numAttrs = 1;
+}
+
+// Co-resident 2-CTA clusters of the pair kernel on the current device (cached).
+int max_pair_clusters() {
+    static std::mutex mu;
+    static int cached[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+    std::lock_guard<std::mutex> lock(mu);
+    if (cached[dev] == 0) {
+        cudaLaunchConfig_t cfg;
+        cudaLaunchAttribute attr[1];
+        pair_launch_config(&cfg, attr, device_sm_count() / 2, nullptr);
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, mx_gemm_2sm_kernel, &cfg) != cudaSuccess || n <= 0)
+            n = device_sm_count() / 2;
+        cached[dev] = n > 0 ? n : 1;
+    }
+    return cached[dev];
+}
+
+cudaError_t launch_2sm(const GemmArgs& g, cudaStream_t stream) {
+    static std::once_flag attr_once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(attr_once, [] {
+        attr_err =
+            cudaFuncSetAttribute(mx_gemm_2sm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, sm2::SMEM_ALLOC);
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+    CUtensorMap ma, mb, msa, msb;
+    const int64_t sfa_tiles = ((g.M + 127) / 128) * ((g.K + 127) / 128);
+    const int64_t sfb_tiles = ((g.N + 127) / 128) * ((g.K + 127) / 128);
+    if (!make_operand_map(&ma, g.a, g.M, g.K, 128) || !make_operand_map(&mb, g.bt, g.N, g.K, 128) ||
+        !make_sf_map(&msa, g.sfa, sfa_tiles) || !make_sf_map(&msb, g.sfb, sfb_tiles))
+        return cudaErrorInvalidValue;
+    KParams p = base_params(g, sm2::BM, sm2::BN);
+    const int tiles = p.num_m_tiles * p.num_n_tiles;
+    const int cap = max_pair_clusters();
+    const int clusters = tiles < cap ? tiles : cap;
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr[1];
+    pair_launch_config(&cfg, attr, clusters, stream);
+    return cudaLaunchKernelEx(&cfg, mx_gemm_2sm_kernel, ma, mb, msa, msb, p);
+}
+
+}  // namespace
+
+void set_gemm_fault_injection(int skip_producer, uint64_t timeout_ns) {
+    g_fault_skip_producer = skip_producer;
+    g_timeout_ns = timeout_ns ? timeout_ns : 2000000000ull;
+}
+
+void set_gemm_variant(int variant) { g_variant = variant; }
+
+cudaError_t launch_scaled_matmul(const GemmArgs& g, cudaStream_t stream) {
+    const bool pair = g_variant == 2 || (g_variant == 0 && g.M > 128);
+    return pair ? launch_2sm(g, stream) : launch_1sm(g, stream);
 }
 
 cudaError_t read_and_clear_device_status(int* status) {

@@ -19,6 +19,7 @@
 namespace mx {
 
 void set_gemm_fault_injection(int skip_producer, uint64_t timeout_ns);
+void set_gemm_variant(int variant);
 
 namespace {
 
@@ -377,6 +378,12 @@ int mx_version(void) { return 100; }
 
 mx_status mx_debug_gemm_fault_injection(int skip_producer, uint64_t timeout_ns) {
     set_gemm_fault_injection(skip_producer, timeout_ns);
+    return MX_OK;
+}
+
+mx_status mx_debug_set_gemm_variant(int variant) {
+    if (variant < 0 || variant > 2) return MX_ERR_INVALID_ARG;
+    set_gemm_variant(variant);
     return MX_OK;
 }
 

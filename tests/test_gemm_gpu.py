@@ -23,6 +23,14 @@ def mx():
     return mx
 
 
+@pytest.fixture(params=[1, 2], ids=["1sm", "2sm"])
+def variant(request, mx):
+    """Run a test on the 1-SM kernel and on the 2-SM pair kernel."""
+    mx.mx_debug_set_gemm_variant(request.param)
+    yield request.param
+    mx.mx_debug_set_gemm_variant(0)
+
+
 def _random_operands(M, N, K, fmt, seed, scale_lo=112, scale_hi=142):
     rng = np.random.default_rng(seed)
     bad = {"e4m3fn": lambda c: (c & 0x7F) == 0x7F, "e5m2": lambda c: (c & 0x7F) >= 0x7C}[fmt]
@@ -48,8 +56,9 @@ def _gpu_matmul(mx, a, bt, sa, sb, fmt, out_dtype, sf_layout=False):
 @pytest.mark.parametrize("fmt", ["e4m3fn", "e5m2"])
 @pytest.mark.parametrize("out_dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("M,N,K", [(128, 256, 128), (256, 512, 512), (384, 768, 1024),
-                                   (200, 300, 96), (1, 1, 32), (130, 260, 160), (512, 256, 4096)])
-def test_matmul_matches_oracle(mx, fmt, out_dtype, M, N, K):
+                                   (200, 300, 96), (1, 1, 32), (130, 260, 160), (512, 256, 4096),
+                                   (640, 1280, 256), (100, 700, 64)])
+def test_matmul_matches_oracle(mx, variant, fmt, out_dtype, M, N, K):
     a, bt, sa, sb = _random_operands(M, N, K, fmt, seed=M * 7 + N + K)
     c = _gpu_matmul(mx, a, bt, sa, sb, fmt, out_dtype)
     c_ref, s_ref = orc.scaled_matmul(a, bt, sa, sb, fmt)
@@ -57,7 +66,7 @@ def test_matmul_matches_oracle(mx, fmt, out_dtype, M, N, K):
 
 
 @pytest.mark.parametrize("fmt", ["e4m3fn", "e5m2"])
-def test_matmul_sf_layout_scales(mx, fmt):
+def test_matmul_sf_layout_scales(mx, variant, fmt):
     M, N, K = 256, 512, 384
     a, bt, sa, sb = _random_operands(M, N, K, fmt, seed=3)
     c = _gpu_matmul(mx, a, bt, sa, sb, fmt, "f32", sf_layout=True)
@@ -65,7 +74,7 @@ def test_matmul_sf_layout_scales(mx, fmt):
     check_gemm(c, c_ref, s_ref, "f32", TOL)
 
 
-def test_matmul_distinct_scales_per_block(mx):
+def test_matmul_distinct_scales_per_block(mx, variant):
     # every (row, K-block) scale different and every product positive, so a
     # scale applied to the wrong row or K block shows up as a large error
     M, N, K = 256, 256, 512
@@ -79,7 +88,7 @@ def test_matmul_distinct_scales_per_block(mx):
     check_gemm(c, c_ref, s_ref, "f32", TOL)
 
 
-def test_matmul_strided_output(mx):
+def test_matmul_strided_output(mx, variant):
     import torch
     M, N, K = 256, 256, 256
     a, bt, sa, sb = _random_operands(M, N, K, "e4m3fn", seed=8)
@@ -174,7 +183,7 @@ def test_fused_full_size_sampled(mx):
     check_gemm(c_cols, c_ref, s_ref, "bf16", TOL)
 
 
-def test_bounded_wait_times_out_without_fault(mx):
+def test_bounded_wait_times_out_without_fault(mx, variant):
     """With loads suppressed, every wait of the GEMM runs out after 50 ms; the
     kernel records MX_ERR_TIMEOUT, frees its tensor memory and returns, and the
     context stays usable."""
