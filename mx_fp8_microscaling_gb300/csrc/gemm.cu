@@ -28,7 +28,9 @@
 //                       128 rows of A and 128 rows of B, so each SM takes in
 //                       32 KB of operands per K block instead of 48 KB.
 //                       6 stages.  Rank 0 issues the MMAs; both CTAs' loads
-//                       complete on rank 0's barriers.
+//                       complete on rank 0's barriers.  An eleventh warp
+//                       issues the scale-factor copies (tcgen05.cp), which
+//                       would otherwise hold up the MMA thread.
 //
 // Tensor memory (512 columns): accumulator in columns 0..255, scale factors
 // of stage s at 256 + 16 s (A: 4 columns, B: 8 columns).  The scale-factor
@@ -340,17 +342,19 @@ constexpr uint32_t OFF_B = OFF_A + STAGES * A_STAGE;
 constexpr uint32_t OFF_SFA = OFF_B + STAGES * B_STAGE;
 constexpr uint32_t OFF_SFB = OFF_SFA + STAGES * SFA_STAGE;
 constexpr uint32_t OFF_BAR = OFF_SFB + STAGES * SFB_STAGE;
-constexpr int NUM_BARS = 2 * STAGES + 3;
+constexpr int NUM_BARS = 3 * STAGES + 4;  // full, empty, sf_full [S]; tmem_full, tmem_empty, mma_done, sf_done
 constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
 constexpr uint32_t SMEM_BYTES = OFF_MISC + 16;
 constexpr uint32_t SMEM_ALLOC = SMEM_BYTES + 1024;
 constexpr uint32_t CTA_TX = A_STAGE + B_STAGE + SFA_STAGE + SFB_STAGE;
 constexpr uint32_t PAIR_TX = 2 * CTA_TX;
+constexpr int SF_WARP = 10;              // warp that copies scale factors to tensor memory
+constexpr int THREADS = NUM_THREADS + 32;
 }  // namespace sm2
 
 // Scale-factor buffers are read by TMA as [2 * tiles, 256] bytes: a 512-byte
 // tile t is rows 2t and 2t+1 (box 256 x 2); tiles past the end read as zeros.
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+__global__ void __launch_bounds__(sm2::THREADS, 1)
     mx_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                        const __grid_constant__ CUtensorMap tmap_sfa, const __grid_constant__ CUtensorMap tmap_sfb,
                        const KParams p) {
@@ -364,9 +368,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     auto full_bar = [&](int s) { return sb + OFF_BAR + 8u * s; };
     auto empty_bar = [&](int s) { return sb + OFF_BAR + 8u * (STAGES + s); };
-    const uint32_t tmem_full = sb + OFF_BAR + 8u * (2 * STAGES);
+    auto sf_full_bar = [&](int s) { return sb + OFF_BAR + 8u * (2 * STAGES + s); };
+    const uint32_t tmem_full = sb + OFF_BAR + 8u * (3 * STAGES);
     const uint32_t tmem_empty = tmem_full + 8;
     const uint32_t mma_done = tmem_full + 16;
+    const uint32_t sf_done = tmem_full + 24;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
 
@@ -374,10 +380,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full_bar(s), 1);     // rank 0's: its arrive + both CTAs' bytes
             mbar_init(empty_bar(s), 1);    // one multicast commit per use
+            mbar_init(sf_full_bar(s), 1);  // rank 0's: the scale copies of the stage are done
         }
         mbar_init(tmem_full, 1);
         mbar_init(tmem_empty, 2 * NUM_EPI_WARPS);  // rank 0's: both CTAs' epilogue warps
         mbar_init(mma_done, 1);
+        mbar_init(sf_done, 1);
         *abort_flag = 0;
         fence_mbar_init();
         prefetch_tmap(&tmap_a);
@@ -450,18 +458,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if (!mbar_wait_bounded(tmem_empty, acc_phase ^ 1u, abort_flag, p.timeout_ns, &g_mx_status)) break;
                 tc_fence_after();
                 for (int kb = 0; kb < p.num_kb; ++kb) {
-                    if (!mbar_wait_bounded(full_bar(stage), phase, abort_flag, p.timeout_ns, &g_mx_status)) {
+                    // the scale-copy warp has seen the stage's operands land
+                    // and its copies into tensor memory have completed
+                    if (!mbar_wait_bounded(sf_full_bar(stage), phase, abort_flag, p.timeout_ns, &g_mx_status)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     const uint32_t sfa_t = tmem_base + TMEM_SF + 16u * stage;
                     const uint32_t sfb_t = sfa_t + 4u;
-                    const uint32_t s_sfa = sb + OFF_SFA + stage * SFA_STAGE;
-                    const uint32_t s_sfb = sb + OFF_SFB + stage * SFB_STAGE;
-                    tc_cp_pair_32x128b_warpx4(sfa_t, sdesc_sf_tile(s_sfa));
-                    tc_cp_pair_32x128b_warpx4(sfb_t, sdesc_sf_tile(s_sfb));
-                    tc_cp_pair_32x128b_warpx4(sfb_t + 4u, sdesc_sf_tile(s_sfb + 512u));
                     const uint32_t sa = sb + OFF_A + stage * A_STAGE;
                     const uint32_t sbb = sb + OFF_B + stage * B_STAGE;
 #pragma unroll
@@ -484,6 +489,38 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tc_commit_pair_mc(mma_done, 3);
             volatile int no_abort = 0;
             (void)mbar_wait_bounded(mma_done, 0, &no_abort, 100000000ull, &g_mx_status);
+        }
+    } else if (warp == SF_WARP) {
+        // Scale-factor copies, one K block at a time, off the MMA thread: a
+        // tcgen05.cp costs the issuing thread as much as the four MMAs of a
+        // K block, so the MMA thread only waits for this warp's commit.
+        if (lane == 0 && rank == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int t = cluster; t < num_tiles && ok; t += num_clusters) {
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    if (!mbar_wait_bounded(full_bar(stage), phase, abort_flag, p.timeout_ns, &g_mx_status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sfa_t = tmem_base + TMEM_SF + 16u * stage;
+                    const uint32_t s_sfa = sb + OFF_SFA + stage * SFA_STAGE;
+                    const uint32_t s_sfb = sb + OFF_SFB + stage * SFB_STAGE;
+                    tc_cp_pair_32x128b_warpx4(sfa_t, sdesc_sf_tile(s_sfa));
+                    tc_cp_pair_32x128b_warpx4(sfa_t + 4u, sdesc_sf_tile(s_sfb));
+                    tc_cp_pair_32x128b_warpx4(sfa_t + 8u, sdesc_sf_tile(s_sfb + 512u));
+                    tc_commit_pair_mc(sf_full_bar(stage), 1);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            tc_commit_pair_mc(sf_done, 1);
+            volatile int no_abort = 0;
+            (void)mbar_wait_bounded(sf_done, 0, &no_abort, 100000000ull, &g_mx_status);
         }
     } else {
         const int quarter = warp & 3;
@@ -610,7 +647,7 @@ cudaError_t launch_1sm(const GemmArgs& g, cudaStream_t stream) {
 void pair_launch_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, int clusters, cudaStream_t stream) {
     *cfg = cudaLaunchConfig_t{};
     cfg->gridDim = dim3(2 * clusters, 1, 1);
-    cfg->blockDim = dim3(NUM_THREADS, 1, 1);
+    cfg->blockDim = dim3(sm2::THREADS, 1, 1);
     cfg->dynamicSmemBytes = sm2::SMEM_ALLOC;
     cfg->stream = stream;
     attr[0].id = cudaLaunchAttributeClusterDimension;
