@@ -7,17 +7,22 @@
 // prescale, page "MX Microscaling", quantizeDataApplyingMxScales NOTE.)
 //
 // Two persistent, warp-specialised kernels share one structure (one CTA per
-// SM, 320 threads):
+// SM, 352 threads):
 //   warp 0      TMA producer: per 128-wide K block, 2-D TMA loads of the
 //               operand tiles (128-byte swizzle) and of the scale-factor
 //               tiles into a ring of shared-memory stages.
-//   warp 1      MMA issuer (one thread): tcgen05.cp moves the stage's scale
-//               tiles into tensor memory, then four
-//               tcgen05.mma.kind::mxf8f6f4.block_scale (K = 32 each)
-//               accumulate into an f32 tile in tensor memory;
+//   warp 10     scale copies (one thread): once a stage's operands land,
+//               tcgen05.cp moves its scale tiles into tensor memory and a
+//               tcgen05.commit tells the MMA thread.  A tcgen05.cp costs its
+//               issuing thread about as much as the four MMAs of a K block,
+//               so it is kept off the MMA thread.
+//   warp 1      MMA issuer (one thread): four
+//               tcgen05.mma.kind::mxf8f6f4.block_scale (K = 32 each) per K
+//               block accumulate into an f32 tile in tensor memory;
 //               tcgen05.commit frees the stage / hands the tile over.
 //   warps 2-9   epilogue: tcgen05.ld the accumulator (each warp its TMEM lane
-//               quarter and one 128-column half), release tensor memory, then
+//               quarter and one 128-column half, one x128 load), release
+//               tensor memory, then
 //               convert (f32, or bf16 round-to-nearest-even) and store rows to
 //               global memory while the next tile's main loop runs.
 //
@@ -28,9 +33,7 @@
 //                       128 rows of A and 128 rows of B, so each SM takes in
 //                       32 KB of operands per K block instead of 48 KB.
 //                       6 stages.  Rank 0 issues the MMAs; both CTAs' loads
-//                       complete on rank 0's barriers.  An eleventh warp
-//                       issues the scale-factor copies (tcgen05.cp), which
-//                       would otherwise hold up the MMA thread.
+//                       complete on rank 0's barriers.
 //
 // Tensor memory (512 columns): accumulator in columns 0..255, scale factors
 // of stage s at 256 + 16 s (A: 4 columns, B: 8 columns).  The scale-factor
@@ -160,14 +163,16 @@ constexpr uint32_t OFF_B = OFF_A + STAGES * A_STAGE;
 constexpr uint32_t OFF_SFA = OFF_B + STAGES * B_STAGE;
 constexpr uint32_t OFF_SFB = OFF_SFA + STAGES * SFA_STAGE;
 constexpr uint32_t OFF_BAR = OFF_SFB + STAGES * SFB_STAGE;
-constexpr int NUM_BARS = 2 * STAGES + 3;  // full[S], empty[S], tmem_full, tmem_empty, mma_done
+constexpr int NUM_BARS = 3 * STAGES + 4;  // full, empty, sf_full [S]; tmem_full, tmem_empty, mma_done, sf_done
 constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
 constexpr uint32_t SMEM_BYTES = OFF_MISC + 16;
 constexpr uint32_t SMEM_ALLOC = SMEM_BYTES + 1024;  // slack to align the base to 1024
 constexpr uint32_t STAGE_TX = A_STAGE + B_STAGE + SFA_STAGE + SFB_STAGE;
+constexpr int SF_WARP = 10;              // warp that copies scale factors to tensor memory
+constexpr int THREADS = NUM_THREADS + 32;
 }  // namespace sm1
 
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+__global__ void __launch_bounds__(sm1::THREADS, 1)
     mx_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                    const KParams p) {
     using namespace sm1;
@@ -178,9 +183,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     auto full_bar = [&](int s) { return sb + OFF_BAR + 8u * s; };
     auto empty_bar = [&](int s) { return sb + OFF_BAR + 8u * (STAGES + s); };
-    const uint32_t tmem_full = sb + OFF_BAR + 8u * (2 * STAGES);
+    auto sf_full_bar = [&](int s) { return sb + OFF_BAR + 8u * (2 * STAGES + s); };
+    const uint32_t tmem_full = sb + OFF_BAR + 8u * (3 * STAGES);
     const uint32_t tmem_empty = tmem_full + 8;
     const uint32_t mma_done = tmem_full + 16;
+    const uint32_t sf_done = tmem_full + 24;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
 
@@ -188,10 +195,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full_bar(s), 1);
             mbar_init(empty_bar(s), 1);
+            mbar_init(sf_full_bar(s), 1);
         }
         mbar_init(tmem_full, 1);
         mbar_init(tmem_empty, NUM_EPI_WARPS);
         mbar_init(mma_done, 1);
+        mbar_init(sf_done, 1);
         *abort_flag = 0;
         fence_mbar_init();
         prefetch_tmap(&tmap_a);
@@ -259,18 +268,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if (!mbar_wait_bounded(tmem_empty, acc_phase ^ 1u, abort_flag, p.timeout_ns, &g_mx_status)) break;
                 tc_fence_after();
                 for (int kb = 0; kb < p.num_kb; ++kb) {
-                    if (!mbar_wait_bounded(full_bar(stage), phase, abort_flag, p.timeout_ns, &g_mx_status)) {
+                    if (!mbar_wait_bounded(sf_full_bar(stage), phase, abort_flag, p.timeout_ns, &g_mx_status)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     const uint32_t sfa_t = tmem_base + TMEM_SF + 16u * stage;
                     const uint32_t sfb_t = sfa_t + 4u;
-                    const uint32_t s_sfa = sb + OFF_SFA + stage * SFA_STAGE;
-                    const uint32_t s_sfb = sb + OFF_SFB + stage * SFB_STAGE;
-                    tc_cp_32x128b_warpx4(sfa_t, sdesc_sf_tile(s_sfa));
-                    tc_cp_32x128b_warpx4(sfb_t, sdesc_sf_tile(s_sfb));
-                    tc_cp_32x128b_warpx4(sfb_t + 4u, sdesc_sf_tile(s_sfb + 512u));
                     const uint32_t sa = sb + OFF_A + stage * A_STAGE;
                     const uint32_t sbb = sb + OFF_B + stage * B_STAGE;
 #pragma unroll
@@ -295,6 +299,36 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             volatile int no_abort = 0;
             (void)mbar_wait_bounded(mma_done, 0, &no_abort, 100000000ull, &g_mx_status);
         }
+    } else if (warp == SF_WARP) {
+        // scale-factor copies for each stage, off the MMA thread
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    if (!mbar_wait_bounded(full_bar(stage), phase, abort_flag, p.timeout_ns, &g_mx_status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sfa_t = tmem_base + TMEM_SF + 16u * stage;
+                    const uint32_t s_sfa = sb + OFF_SFA + stage * SFA_STAGE;
+                    const uint32_t s_sfb = sb + OFF_SFB + stage * SFB_STAGE;
+                    tc_cp_32x128b_warpx4(sfa_t, sdesc_sf_tile(s_sfa));
+                    tc_cp_32x128b_warpx4(sfa_t + 4u, sdesc_sf_tile(s_sfb));
+                    tc_cp_32x128b_warpx4(sfa_t + 8u, sdesc_sf_tile(s_sfb + 512u));
+                    tc_commit(sf_full_bar(stage));
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            tc_commit(sf_done);
+            volatile int no_abort = 0;
+            (void)mbar_wait_bounded(sf_done, 0, &no_abort, 100000000ull, &g_mx_status);
+        }
     } else {
         const int quarter = warp & 3;          // TMEM lanes this warp may access
         const int half = (warp - 2) >> 2;      // accumulator columns [128*half, +128)
@@ -310,8 +344,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tc_fence_after();
             uint32_t v[4][32];
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + half * 128;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) tmem_ld_32x32b_x32(taddr + 32u * j, v[j]);
+            tmem_ld_32x32b_x128(taddr, v);
             tmem_wait_ld();
             tc_fence_before();
             __syncwarp();
@@ -537,8 +570,7 @@ __global__ void __launch_bounds__(sm2::THREADS, 1)
             tc_fence_after();
             uint32_t v[4][32];
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + half * 128;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) tmem_ld_32x32b_x32(taddr + 32u * j, v[j]);
+            tmem_ld_32x32b_x128(taddr, v);
             tmem_wait_ld();
             tc_fence_before();
             __syncwarp();
@@ -640,7 +672,7 @@ cudaError_t launch_1sm(const GemmArgs& g, cudaStream_t stream) {
     const int tiles = p.num_m_tiles * p.num_n_tiles;
     const int sms = device_sm_count();
     const int grid = tiles < sms ? tiles : sms;
-    mx_gemm_kernel<<<grid, NUM_THREADS, sm1::SMEM_ALLOC, stream>>>(ma, mb, p);
+    mx_gemm_kernel<<<grid, sm1::THREADS, sm1::SMEM_ALLOC, stream>>>(ma, mb, p);
     return cudaGetLastError();
 }
 
