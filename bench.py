@@ -529,10 +529,10 @@ def main():
             "cases": g, "pipeline_tflops_incl_quantize_repack": round(GEMM_FLOP / (pipe_ms * 1e-3) / 1e12, 1),
             "quantize_operands_ms": round(timer.totals["gemm_quantize"] / timer.counts["gemm_quantize"], 4),
             "repack_ms": round(timer.totals["gemm_repack"] / timer.counts["gemm_repack"], 4),
-            "roofline": {"bound": "tensor", "kernel": "mx_gemm_kernel", "achieved": round(avg, 1),
+            "roofline": {"bound": "tensor", "kernel": "mx_gemm_2sm_kernel", "achieved": round(avg, 1),
                          "peak": round(peak_fp8, 1), "unit": "TFLOP/s", "frac": round(avg / peak_fp8, 4),
                          "peak_source": f"{peaks['src']} bf16 burst x {FP8_OVER_BF16} (nominal MXFP8/bf16)",
-                         "traffic": profiled_traffic("mx_gemm_kernel", source_hash("gemm.cu"))}}
+                         "traffic": profiled_traffic("mx_gemm_2sm_kernel", source_hash("gemm.cu"))}}
     if "fp4" in parts:
         ms = timer.avg_ms("fp4")
         gbs = FP4_BYTES / (ms * 1e-3) / 1e9
