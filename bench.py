@@ -10,6 +10,7 @@ A step is one pass of the whole hot path over its synthetic inputs:
          ([8192, 8192] bf16, 1x32 blocks along K), repack of both scale
          tensors to the tensor-core layout, ScaledMatmul 8192^3;
   fp4    QuantizeMX [16384, 16384] bf16 -> e2m1, 8x4, packed, interleaved;
+  dequant  MX dequantize of [8192, 8192] e4m3fn codes with 8x4 scales to bf16;
   fused  activation quantize + ScaledMatmul, X [16384, 8192] bf16 times a
          pre-quantized e4m3fn weight W [8192, 28672] -> bf16.
 The headline `value` is QuantizeMX GB/s over the sweep (algorithmic bytes:
@@ -257,8 +258,12 @@ class Sweep:
         self.launches = 8
 
     def step(self, timer):
-        for label, fn in self.ops:
-            timer.run(label, fn)
+        # one event pair around the 8 back-to-back launches: per-launch event
+        # records would add their own gaps to 33 us kernels
+        def all_launches():
+            for _, fn in self.ops:
+                fn()
+        timer.run("sweep", all_launches)
 
 
 class Gemm:
@@ -305,6 +310,33 @@ class Fp4:
 
     def step(self, timer):
         timer.run("fp4", self.op)
+
+
+class Dequant:
+    """[8192, 8192] e4m3fn codes + plain 8x4 scales -> bf16 (1 + 1/32 B read, 2 B written per element)."""
+
+    def __init__(self, torch, mx, api):
+        import ctypes
+        bits = syn.sweep_input(*SWEEP, "bf16", "e4m3fn", seed=0)
+        x = dev_bits(torch, bits, "bf16")
+        self.d, self.s = mx.mx_quantize(x, "e4m3fn", geometry="8x4", dim=-2)
+        del x
+        self.out = torch.empty(SWEEP, dtype=torch.bfloat16, device="cuda")
+        self.cfg = mx.make_cfg("8x4", -2, "plain")
+        lib = mx.raw_library()
+        args = (ctypes.c_void_p(self.d.data_ptr()), ctypes.c_void_p(self.s.data_ptr()), mx.DTYPES["e4m3fn"],
+                SWEEP[0], SWEEP[1], ctypes.byref(self.cfg), mx.DTYPES["bf16"], ctypes.c_void_p(self.out.data_ptr()),
+                SWEEP[1], api.stream())
+
+        def call():
+            st = lib.mx_dequantize(*args)
+            if st:
+                raise mx.MxError(st, "mx_dequantize")
+        self.op = call
+        self.launches = 1
+
+    def step(self, timer):
+        timer.run("dequant", self.op)
 
 
 class Fused:
@@ -383,31 +415,32 @@ def barrier(ws):
         dist.barrier()
 
 
-def max_over_ranks(ws, value):
+def _all_reduce(ws, value, op_name):
+    """Reduce a host scalar over ranks (timing bookkeeping only; the data
+    path has no collective)."""
     if ws == 1:
         return value
     import torch
     import torch.distributed as dist
-    t = torch.tensor([value], dtype=torch.float64, device="cuda")
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    device = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=getattr(dist.ReduceOp, op_name))
     return float(t.item())
+
+
+def max_over_ranks(ws, value):
+    return _all_reduce(ws, value, "MAX")
 
 
 def sum_over_ranks(ws, value):
-    if ws == 1:
-        return value
-    import torch
-    import torch.distributed as dist
-    t = torch.tensor([value], dtype=torch.float64, device="cuda")
-    dist.all_reduce(t, op=dist.ReduceOp.SUM)
-    return float(t.item())
+    return _all_reduce(ws, value, "SUM")
 
 
 def run_reference(args):
-    ws, rank, _ = int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")), 0
+    rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    rows = 1024
+    rows = args.reference_rows
     vals = []
     for _ in range(args.warmup):
         oracle_sweep_sample(rows=rows)
@@ -436,8 +469,10 @@ def main():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="mx", choices=["mx", "reference"])
-    ap.add_argument("--workload", default="all", choices=["all", "sweep", "gemm", "fp4", "fused"])
+    ap.add_argument("--workload", default="all", choices=["all", "sweep", "gemm", "fp4", "fused", "dequant"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--reference-rows", type=int, default=1024,
+                    help="rows of each [rows, 8192] sweep slice the reference arm quantizes per step")
     args = ap.parse_args()
     if args.warmup < 3:
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
@@ -452,8 +487,8 @@ def main():
 
     peaks = load_peaks()
     parts = {}
-    want = ["sweep", "gemm", "fp4", "fused"] if args.workload == "all" else [args.workload]
-    builders = {"sweep": Sweep, "gemm": Gemm, "fp4": Fp4, "fused": Fused}
+    want = ["sweep", "gemm", "fp4", "dequant", "fused"] if args.workload == "all" else [args.workload]
+    builders = {"sweep": Sweep, "gemm": Gemm, "fp4": Fp4, "dequant": Dequant, "fused": Fused}
     api = Api(torch, mx)
     for name in want:
         parts[name] = builders[name](torch, mx, api)
@@ -498,9 +533,10 @@ def main():
 
     if "sweep" in parts:
         sweep_ms = max_over_ranks(ws, timer.totals["sweep"])
-        n_launch = timer.counts["sweep"]
+        n_launch = timer.counts["sweep"] * 8
         value = sum_over_ranks(ws, SWEEP_BYTES * n_launch) / (sweep_ms * 1e-3) / 1e9
-        achieved = SWEEP_BYTES / (timer.avg_ms("sweep") * 1e-3) / 1e9
+        # average launch duration = each step's 8-launch span / 8 (gaps included)
+        achieved = SWEEP_BYTES / (timer.avg_ms("sweep") / 8 * 1e-3) / 1e9
         line.update({"value": round(value, 2), "unit": "GB/s",
                      "config": {"workload": "QuantizeMX sweep [8192,8192] {bf16,f16}x{e4m3fn,e5m2}x"
                                             "{plain,interleave}, 8x4 blocks, dim=-2",
@@ -541,6 +577,14 @@ def main():
                                 "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm"],
                                              "unit": "GB/s", "frac": round(gbs / peaks["hbm"], 4),
                                              "peak_source": peaks["src"]}}
+    if "dequant" in parts:
+        ms = timer.avg_ms("dequant")
+        gbs = SWEEP_BYTES / (ms * 1e-3) / 1e9
+        line["dequantize"] = {"value": round(gbs, 1), "unit": "GB/s", "ms": round(ms, 4),
+                              "config": "[8192,8192] e4m3fn + 8x4 plain scales -> bf16",
+                              "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm"],
+                                           "unit": "GB/s", "frac": round(gbs / peaks["hbm"], 4),
+                                           "peak_source": peaks["src"]}}
     if "fused" in parts:
         ms = timer.avg_ms("fused")
         tf = FUSED_FLOP / (ms * 1e-3) / 1e12

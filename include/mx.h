@@ -161,6 +161,27 @@ mx_status mx_quantize(const void* in, mx_dtype in_dtype, int64_t rows, int64_t c
                       mx_stream stream);
 
 /*
+ * MX dequantize (page "MX Microscaling", quantizeDataApplyingMxScales NOTE:
+ * the matmul side applies ldexpf(x, E8M0 - 127); "FP4 x4-Pack": the read-back
+ * uses the same lane permutation): out[r,c] = decode(code) * 2^(E - 127).
+ *   data       device codes as mx_quantize writes them (dense; 4-byte aligned)
+ *   scale      device scale buffer in cfg's layout (plain / interleaved / SF)
+ *   in_dtype   MX_E4M3FN | MX_E5M2 | MX_E2M1
+ *   rows, cols, cfg   as for mx_quantize (geometry, dim, layout, FP4 stride
+ *              and parity must match the ones that produced the data)
+ *   out_dtype  MX_F32 (exact: every value is representable, E = 0xFF gives
+ *              NaN, overflow gives Inf) | MX_BF16 (round to nearest even)
+ *   out, ld_out  device [rows, ld_out], element aligned; caller owns every buffer
+ * Errors (nothing launched): MX_ERR_SHAPE / MX_ERR_INVALID_ARG as for
+ * mx_quantize, also ld_out < cols or a null pointer; MX_ERR_ALIGNMENT (data
+ * not 4-byte aligned, out not element aligned); MX_ERR_UNSUPPORTED_DTYPE;
+ * MX_ERR_DEVICE off sm_103.  Asynchronous on `stream`; allocates nothing.
+ */
+mx_status mx_dequantize(const void* data, const void* scale, mx_dtype in_dtype, int64_t rows, int64_t cols,
+                        const mx_quant_cfg* cfg, mx_dtype out_dtype, void* out, int64_t ld_out,
+                        mx_stream stream);
+
+/*
  * Bytes of the tensor-core scale-factor ("SF") layout for an operand of `mn`
  * rows and K = `k` elements per row (k % 32 == 0): the E8M0 matrix
  * [mn, k/32] padded to 128-row x 4-column tiles of 512 bytes,

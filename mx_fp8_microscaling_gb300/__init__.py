@@ -61,6 +61,7 @@ def _load():
         "mx_quant_cfg_default": [ctypes.POINTER(QuantCfg)],
         "mx_quantize_sizes": [I, I, I64, I64, ctypes.POINTER(QuantCfg), PS, PI64, PI64, PS],
         "mx_quantize": [P, I, I64, I64, I64, I, ctypes.POINTER(QuantCfg), P, P, P],
+        "mx_dequantize": [P, P, I, I64, I64, ctypes.POINTER(QuantCfg), I, P, I64, P],
         "mx_sf_layout_bytes": [I64, I64, PS],
         "mx_repack_scales": [P, I64, I64, I64, P, P],
         "mx_scaled_matmul_workspace": [I64, I64, I64, I, PS],
@@ -177,6 +178,20 @@ def mx_quantize(x: torch.Tensor, out_dtype: str = "e4m3fn", *, geometry="8x4", d
                             ctypes.byref(cfg), _dev_ptr(out_data), _dev_ptr(out_scale), _stream(stream)),
            "mx_quantize")
     return out_data, out_scale
+
+
+def mx_dequantize(data: torch.Tensor, scale: torch.Tensor, rows: int, cols: int, in_dtype: str = "e4m3fn",
+                  out_dtype: str = "f32", *, geometry="8x4", dim=-2, scale_layout="plain", fp4_lane_stride=2,
+                  fp4_nibble_parity=0, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """decode(code) * 2^(E - 127) for an MX tensor as mx_quantize wrote it."""
+    cfg = make_cfg(geometry, dim, scale_layout, fp4_lane_stride, fp4_nibble_parity)
+    if out is None:
+        out = torch.empty((rows, cols), dtype=torch.float32 if out_dtype == "f32" else torch.bfloat16,
+                          device=data.device)
+    _check(_lib.mx_dequantize(_dev_ptr(data), _dev_ptr(scale), DTYPES[in_dtype], rows, cols, ctypes.byref(cfg),
+                              DTYPES[out_dtype], _dev_ptr(out), out.stride(0), _stream(stream)),
+           "mx_dequantize")
+    return out
 
 
 def mx_sf_layout_bytes(mn: int, k: int) -> int:

@@ -229,6 +229,42 @@ mx_status mx_quantize(const void* in, mx_dtype in_dtype, int64_t rows, int64_t c
     return from_cuda(launch_quantize(q, plan.in_f16, plan.fmt, s));
 }
 
+mx_status mx_dequantize(const void* data, const void* scale, mx_dtype in_dtype, int64_t rows, int64_t cols,
+                        const mx_quant_cfg* cfg, mx_dtype out_dtype, void* out, int64_t ld_out, mx_stream stream) {
+    QuantPlan plan;
+    // the codes' format and the block layout are checked as QuantizeMX checks them
+    mx_status st = plan_quantize(MX_BF16, in_dtype, rows, cols, cfg, &plan);
+    if (st != MX_OK) return st;
+    if (out_dtype != MX_F32 && out_dtype != MX_BF16) return MX_ERR_UNSUPPORTED_DTYPE;
+    if (ld_out < cols) return MX_ERR_INVALID_ARG;
+    if (rows == 0 || cols == 0) return MX_OK;
+    if (!data || !scale || !out) return MX_ERR_INVALID_ARG;
+    const uintptr_t esize = out_dtype == MX_F32 ? 4 : 2;
+    if ((reinterpret_cast<uintptr_t>(data) & 3u) || (reinterpret_cast<uintptr_t>(out) & (esize - 1)))
+        return MX_ERR_ALIGNMENT;
+    if (!device_is_sm103()) return MX_ERR_DEVICE;
+    DequantArgs q{};
+    q.data = static_cast<const uint8_t*>(data);
+    q.scale = static_cast<const uint8_t*>(scale);
+    q.rows = rows;
+    q.cols = cols;
+    q.block_rows = plan.br;
+    q.block_cols = plan.bc;
+    q.scale_mode = plan.scale_mode;
+    q.scale_cols = plan.scale_cols;
+    q.sf_ntk = plan.scale_cols / 4;
+    // inverse of the packing selector: source byte p sits at destination byte d(p)
+    const uint32_t fwd = fp4_pair_perm(plan.stride);
+    uint32_t inv = 0;
+    for (int d = 0; d < 4; ++d) inv |= static_cast<uint32_t>(d) << (4 * ((fwd >> (4 * d)) & 0xFu));
+    q.fp4_inv_perm = inv;
+    q.fp4_parity = plan.parity;
+    q.out = out;
+    q.ld_out = ld_out;
+    q.vec_ok = aligned16(out) && (ld_out * static_cast<int64_t>(esize)) % 16 == 0;
+    return from_cuda(launch_dequantize(q, plan.fmt, out_dtype == MX_BF16, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 mx_status mx_sf_layout_bytes(int64_t mn, int64_t k, size_t* bytes) {
     if (!bytes || mn < 0 || k < 0) return MX_ERR_INVALID_ARG;
     if (k % 32 != 0) return MX_ERR_SHAPE;

@@ -35,6 +35,24 @@ struct QuantArgs {
 
 cudaError_t launch_quantize(const QuantArgs& q, bool in_f16, int fmt, cudaStream_t stream);
 
+// One MX dequantize launch (see mx_dequantize).
+struct DequantArgs {
+    const uint8_t* data;    // dense codes: rows*cols bytes (FP8) or rows*cols/2 (e2m1)
+    const uint8_t* scale;   // scale buffer in the layout of `scale_mode`
+    int64_t rows, cols;
+    int32_t block_rows, block_cols;  // (8,4), (4,8), (1,32) or (32,1)
+    int32_t scale_mode;     // 0 plain, 1 interleave, 2 tensor-core SF
+    int64_t scale_cols;     // scale tensor columns (SF: rounded up to 4)
+    int64_t sf_ntk;
+    uint32_t fp4_inv_perm;  // __byte_perm selector undoing the lane permutation of an 8-element chunk
+    int32_t fp4_parity;
+    void* out;              // f32 or bf16
+    int64_t ld_out;         // elements
+    int32_t vec_ok;         // 16-byte aligned output rows
+};
+
+cudaError_t launch_dequantize(const DequantArgs& q, int fmt, bool out_bf16, cudaStream_t stream);
+
 // Scale-factor repack: plain [mn, k/32] -> SF tiles (see mx_repack_scales).
 cudaError_t launch_repack_scales(const uint8_t* plain, int64_t mn, int64_t k, int64_t ld_plain,
                                  uint8_t* sf, cudaStream_t stream);

@@ -356,9 +356,13 @@ __global__ void __launch_bounds__(kThreads) quant_generic(QuantArgs q) {
 template <bool F16, int FMT>
 cudaError_t launch_typed(const QuantArgs& q, cudaStream_t stream) {
     const int sms = device_sm_count();
+    // 16 blocks of 256 threads per SM (3-4 resident, the rest queued):
+    // measured 5 % faster than 8 on the 8192 x 8192 sweep, as fast as 512-
+    // thread blocks, and at the level of a no-arithmetic copy of the same
+    // access pattern.
     auto grid_for = [&](int64_t units) {
         int64_t blocks = (units + kThreads - 1) / kThreads;
-        const int64_t cap = static_cast<int64_t>(sms) * 8;
+        const int64_t cap = static_cast<int64_t>(sms) * 16;
         if (blocks > cap) blocks = cap;
         return static_cast<unsigned>(blocks < 1 ? 1 : blocks);
     };
