@@ -582,9 +582,11 @@ def main():
         gbs = SWEEP_BYTES / (ms * 1e-3) / 1e9
         line["dequantize"] = {"value": round(gbs, 1), "unit": "GB/s", "ms": round(ms, 4),
                               "config": "[8192,8192] e4m3fn + 8x4 plain scales -> bf16",
-                              "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm"],
-                                           "unit": "GB/s", "frac": round(gbs / peaks["hbm"], 4),
-                                           "peak_source": peaks["src"]}}
+                              "roofline": {"bound": "hbm", "kernel": "dequant_kernel", "achieved": round(gbs, 1),
+                                           "peak": peaks["hbm"], "unit": "GB/s",
+                                           "frac": round(gbs / peaks["hbm"], 4), "peak_source": peaks["src"],
+                                           "traffic": profiled_traffic("dequant_kernel",
+                                                                       source_hash("dequantize.cu"))}}
     if "fused" in parts:
         ms = timer.avg_ms("fused")
         tf = FUSED_FLOP / (ms * 1e-3) / 1e12
