@@ -327,3 +327,95 @@ def scaled_matmul(a, bt, sa, sb, fmt_a: str, fmt_b: str | None = None, rows=None
     da = dequantize_rows(a, sa, fmt_a, rows)
     db = dequantize_rows(bt, sb, fmt_b, cols)
     return da @ db.T, np.abs(da) @ np.abs(db).T
+
+
+# ---------------------------------------------------- general block-scaled dot
+
+class DotDimsError(ValueError):
+    """A dot-dimension-number check of the ScaledMatmul contract failed."""
+
+
+def check_dot_dims(lhs_shape, rhs_shape, lhs_batch, rhs_batch, lhs_contract, rhs_contract):
+    """The ScaledMatmul contract's checks (page "MX-FP8 Microscaling
+    Legalization", section 4.2 and the ScaledMatmul verifier list): ranks >= 2;
+    as many batch dimensions on each side, in bounds, of equal extents;
+    contracting dimensions in bounds, of equal size and not overlapping the
+    batch dimensions.  Reading: exactly one contracting dimension per side
+    (MX blocks run along one axis), its extent a multiple of 32.  Negative
+    indices count from the end."""
+    lr, rr = len(lhs_shape), len(rhs_shape)
+    if lr < 2 or rr < 2:
+        raise DotDimsError("operands must have rank >= 2")
+    if len(lhs_batch) != len(rhs_batch):
+        raise DotDimsError("batch dimension counts differ")
+    if len(lhs_contract) != 1 or len(rhs_contract) != 1:
+        raise DotDimsError("exactly one contracting dimension per operand")
+
+    def norm(d, r):
+        d = int(d)
+        if not -r <= d < r:
+            raise DotDimsError(f"dimension {d} out of bounds for tensor of rank {r}")
+        return d % r
+
+    lb = [norm(d, lr) for d in lhs_batch]
+    rb = [norm(d, rr) for d in rhs_batch]
+    lc, rc = norm(lhs_contract[0], lr), norm(rhs_contract[0], rr)
+    if len(set(lb)) != len(lb) or len(set(rb)) != len(rb):
+        raise DotDimsError("repeated batch dimension")
+    if lc in lb or rc in rb:
+        raise DotDimsError("contracting dimension overlaps a batch dimension")
+    for a, b in zip(lb, rb):
+        if lhs_shape[a] != rhs_shape[b]:
+            raise DotDimsError("batch extents differ")
+    if lhs_shape[lc] != rhs_shape[rc]:
+        raise DotDimsError("contracting extents differ")
+    if lhs_shape[lc] % 32 != 0:
+        raise DotDimsError("contracting extent not a multiple of the 32-element block")
+    return lb, rb, lc, rc
+
+
+def block_values(codes, scale, fmt: str, axis: int) -> np.ndarray:
+    """decode(code) * 2^(E8M0 - 127) in binary64 for an N-d FP8 operand whose
+    scale tensor is the operand's shape with `axis` divided by 32 (one E8M0 per
+    32 consecutive elements along `axis`)."""
+    codes = np.asarray(codes, np.uint8)
+    scale = np.asarray(scale, np.uint8)
+    e8m0 = np.array([decode_e8m0(e) for e in range(256)], np.float64)
+    return decode_array(fmt, codes) * np.repeat(e8m0[scale], 32, axis=axis)
+
+
+def block_scaled_dot(lhs, rhs, lhs_scale, rhs_scale, fmt: str, *, lhs_batch=(), rhs_batch=(),
+                     lhs_contract=(-1,), rhs_contract=(-1,), fmt_rhs: str | None = None):
+    """block_scaled_dot(lhs, rhs, lhs_scale, rhs_scale) with dot dimension
+    numbers (page "MX-FP8 Microscaling Legalization", sections 3.2 and 4.2):
+
+      out[b..., i..., j...] = sum_k  lhs_val[.., k, ..] * rhs_val[.., k, ..]
+
+    over the contracting axis k, with the batch axes b paired in the listed
+    order, i the remaining lhs axes and j the remaining rhs axes in their own
+    order (the dot-general result order: batch, lhs free, rhs free).  Values
+    are decode(code) * 2^(E8M0 - 127) (block_values).  The contraction is
+    numpy's binary64 einsum (a library routine; every product is exact in
+    binary64).  Returns (C, S), S the same sum over |products|.
+    """
+    lhs = np.asarray(lhs, np.uint8)
+    rhs = np.asarray(rhs, np.uint8)
+    lb, rb, lc, rc = check_dot_dims(lhs.shape, rhs.shape, lhs_batch, rhs_batch, lhs_contract, rhs_contract)
+    vl = block_values(lhs, lhs_scale, fmt, lc)
+    vr = block_values(rhs, rhs_scale, fmt if fmt_rhs is None else fmt_rhs, rc)
+    letters = iter("abcdefghijklmnopqrstuvwxyz")
+    ls, rs = [None] * lhs.ndim, [None] * rhs.ndim
+    batch = []
+    for a, b in zip(lb, rb):
+        ls[a] = rs[b] = next(letters)
+        batch.append(ls[a])
+    ls[lc] = rs[rc] = next(letters)
+    lfree = [i for i in range(lhs.ndim) if ls[i] is None]
+    rfree = [i for i in range(rhs.ndim) if rs[i] is None]
+    for i in lfree:
+        ls[i] = next(letters)
+    for i in rfree:
+        rs[i] = next(letters)
+    out = "".join(batch) + "".join(ls[i] for i in lfree) + "".join(rs[i] for i in rfree)
+    sub = f"{''.join(ls)},{''.join(rs)}->{out}"
+    return np.einsum(sub, vl, vr), np.einsum(sub, np.abs(vl), np.abs(vr))
