@@ -44,7 +44,7 @@ typedef enum mx_status {
     MX_ERR_INVALID_ARG = 1,       /* NULL pointer, negative size, unknown enum value, pitch < width */
     MX_ERR_UNSUPPORTED_DTYPE = 2, /* dtype combination outside the dispatch matrix */
     MX_ERR_BLOCK_SIZE = 3,        /* block_size other than 32 (0 selects 32) */
-    MX_ERR_DIM = 4,               /* dim other than -1 / -2 (or 1 / 0 for a 2-D tensor) */
+    MX_ERR_DIM = 4,               /* dim other than -1 / -2 (or 1 / 0 for a 2-D tensor); bad dot dimension numbers */
     MX_ERR_SHAPE = 5,             /* extents not divisible by the block / the x4 container */
     MX_ERR_ALIGNMENT = 6,         /* pointer or pitch not 16-byte aligned */
     MX_ERR_WORKSPACE = 7,         /* workspace missing or too small */
@@ -287,6 +287,71 @@ mx_status mx_fused_quantize_matmul(const void* x, mx_dtype x_dtype, int64_t ld_x
                                    const uint8_t* w_scale_sf, mx_dtype elem_dtype, int64_t M,
                                    int64_t N, int64_t K, mx_dtype out_dtype, void* c, int64_t ldc,
                                    void* workspace, size_t workspace_bytes, mx_stream stream);
+
+/* ------------------------------------------------ general block-scaled dot */
+
+#define MX_MAX_RANK 8
+
+/*
+ * Dot dimension numbers of the ScaledMatmul contract (page "MX-FP8
+ * Microscaling Legalization", section 4.2: lhs_batch_dimensions,
+ * rhs_batch_dimensions, lhs_contracting_dimensions,
+ * rhs_contracting_dimensions).  Indices are axes of the operand (negative
+ * ones count from the end).  Exactly one contracting dimension per operand:
+ * MX blocks run along one axis.
+ */
+typedef struct mx_dot_dims {
+    int lhs_n_batch, rhs_n_batch;
+    int64_t lhs_batch[MX_MAX_RANK], rhs_batch[MX_MAX_RANK];
+    int lhs_n_contract, rhs_n_contract;
+    int64_t lhs_contract[MX_MAX_RANK], rhs_contract[MX_MAX_RANK];
+} mx_dot_dims;
+
+/*
+ * Result shape of mx_block_scaled_dot: the batch extents (in the listed
+ * order), then the lhs free extents, then the rhs free extents, each in
+ * operand axis order.  out_dims holds at least MX_MAX_RANK entries.
+ * Errors as for mx_block_scaled_dot's dimension checks.
+ */
+mx_status mx_block_scaled_dot_shape(const int64_t* lhs_dims, int lhs_rank, const int64_t* rhs_dims, int rhs_rank,
+                                    const mx_dot_dims* dims, int64_t* out_dims, int* out_rank);
+
+/* Workspace bytes mx_block_scaled_dot needs for these shapes. */
+mx_status mx_block_scaled_dot_workspace(const int64_t* lhs_dims, int lhs_rank, const int64_t* rhs_dims,
+                                        int rhs_rank, const mx_dot_dims* dims, size_t* bytes);
+
+/*
+ * block_scaled_dot(lhs, rhs, lhs_scale, rhs_scale) with dot dimension
+ * numbers (page "MX-FP8 Microscaling Legalization", sections 3.2 and 4.2):
+ *   out[b.., i.., j..] = sum_k lhs(b.., i.., k) 2^(sl - 127) * rhs(b.., j.., k) 2^(sr - 127)
+ * with the scale of each element the E8M0 of its 32-element block along the
+ * contracting axis.
+ *   lhs, rhs    device FP8 codes, dense row-major with extents lhs_dims /
+ *               rhs_dims (rank 2..MX_MAX_RANK)
+ *   lhs_scale, rhs_scale  device E8M0, dense, the operand's extents with the
+ *               contracting one divided by 32 (what mx_quantize writes for
+ *               1x32 blocks along that axis, plain layout)
+ *   dims        dot dimension numbers
+ *   elem_dtype  MX_E4M3FN | MX_E5M2 (both operands)
+ *   out_dtype   MX_F32 | MX_BF16 (round to nearest even); `out` is dense in
+ *               the order of mx_block_scaled_dot_shape, caller-owned
+ *   workspace   device, 16-byte aligned, mx_block_scaled_dot_workspace bytes
+ *               (canonical copies of operands that are not already
+ *               [batch.., free.., K] in memory, and the scales in the
+ *               tensor-core layout)
+ * Operands already in [batch.., free.., K] order are read in place and must
+ * be 16-byte aligned.  Accumulation is f32 on the tensor cores.
+ * Errors (nothing launched): MX_ERR_SHAPE (rank < 2 or > MX_MAX_RANK, batch
+ * or contracting extents differ, K not a multiple of 32 or < 32, extents
+ * over 2^30), MX_ERR_DIM (batch counts differ, an index out of bounds or
+ * repeated, contracting overlapping batch, not exactly one contracting
+ * dimension), MX_ERR_UNSUPPORTED_DTYPE, MX_ERR_INVALID_ARG, MX_ERR_ALIGNMENT,
+ * MX_ERR_WORKSPACE, MX_ERR_DEVICE.  Asynchronous on `stream`.
+ */
+mx_status mx_block_scaled_dot(const void* lhs, const int64_t* lhs_dims, int lhs_rank, const void* lhs_scale,
+                              const void* rhs, const int64_t* rhs_dims, int rhs_rank, const void* rhs_scale,
+                              const mx_dot_dims* dims, mx_dtype elem_dtype, mx_dtype out_dtype, void* out,
+                              void* workspace, size_t workspace_bytes, mx_stream stream);
 
 /*
  * Read and clear the current device's status word (synchronises the device).

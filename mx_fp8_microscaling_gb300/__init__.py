@@ -42,6 +42,16 @@ class MxError(RuntimeError):
         self.status = status
 
 
+MAX_RANK = 8
+
+
+class DotDims(ctypes.Structure):
+    _fields_ = [("lhs_n_batch", ctypes.c_int32), ("rhs_n_batch", ctypes.c_int32),
+                ("lhs_batch", ctypes.c_int64 * MAX_RANK), ("rhs_batch", ctypes.c_int64 * MAX_RANK),
+                ("lhs_n_contract", ctypes.c_int32), ("rhs_n_contract", ctypes.c_int32),
+                ("lhs_contract", ctypes.c_int64 * MAX_RANK), ("rhs_contract", ctypes.c_int64 * MAX_RANK)]
+
+
 class QuantCfg(ctypes.Structure):
     _fields_ = [("geometry", ctypes.c_int32), ("scale_layout", ctypes.c_int32),
                 ("block_size", ctypes.c_int32), ("dim", ctypes.c_int32),
@@ -69,6 +79,9 @@ def _load():
         "mx_scaled_matmul_noalloc": [P, P, P, P, I, I64, I64, I64, I, P, I64, P],
         "mx_fused_quantize_matmul_workspace": [I64, I64, I64, PS],
         "mx_fused_quantize_matmul": [P, I, I64, P, P, I, I64, I64, I64, I, P, I64, P, SZ, P],
+        "mx_block_scaled_dot_shape": [PI64, I, PI64, I, ctypes.POINTER(DotDims), PI64, ctypes.POINTER(I)],
+        "mx_block_scaled_dot_workspace": [PI64, I, PI64, I, ctypes.POINTER(DotDims), PS],
+        "mx_block_scaled_dot": [P, PI64, I, P, P, PI64, I, P, ctypes.POINTER(DotDims), I, I, P, P, SZ, P],
         "mx_get_device_status": [ctypes.POINTER(I)],
         "mx_status_string": [I],
         "mx_version": [],
@@ -253,6 +266,65 @@ def mx_scaled_matmul_noalloc(a: torch.Tensor, bt: torch.Tensor, a_scale: torch.T
                                          DTYPES[elem_dtype], M, N, K, DTYPES[out_dtype], _dev_ptr(out),
                                          out.stride(0), _stream(stream)),
            "mx_scaled_matmul_noalloc")
+    return out
+
+
+def make_dot_dims(lhs_batch=(), rhs_batch=(), lhs_contract=(-1,), rhs_contract=(-1,)) -> DotDims:
+    d = DotDims()
+    d.lhs_n_batch, d.rhs_n_batch = len(lhs_batch), len(rhs_batch)
+    d.lhs_n_contract, d.rhs_n_contract = len(lhs_contract), len(rhs_contract)
+    for dst, src in ((d.lhs_batch, lhs_batch), (d.rhs_batch, rhs_batch), (d.lhs_contract, lhs_contract),
+                     (d.rhs_contract, rhs_contract)):
+        if len(src) > MAX_RANK:
+            raise ValueError("more dimensions than MX_MAX_RANK")
+        for i, v in enumerate(src):
+            dst[i] = int(v)
+    return d
+
+
+def _dims_array(shape):
+    return (ctypes.c_int64 * max(1, len(shape)))(*[int(v) for v in shape])
+
+
+def mx_block_scaled_dot_shape(lhs_shape, rhs_shape, dims: DotDims) -> tuple:
+    out = (ctypes.c_int64 * MAX_RANK)()
+    rank = ctypes.c_int()
+    _check(_lib.mx_block_scaled_dot_shape(_dims_array(lhs_shape), len(lhs_shape), _dims_array(rhs_shape),
+                                          len(rhs_shape), ctypes.byref(dims), out, ctypes.byref(rank)),
+           "mx_block_scaled_dot_shape")
+    return tuple(out[i] for i in range(rank.value))
+
+
+def mx_block_scaled_dot_workspace(lhs_shape, rhs_shape, dims: DotDims) -> int:
+    n = ctypes.c_size_t()
+    _check(_lib.mx_block_scaled_dot_workspace(_dims_array(lhs_shape), len(lhs_shape), _dims_array(rhs_shape),
+                                              len(rhs_shape), ctypes.byref(dims), ctypes.byref(n)),
+           "mx_block_scaled_dot_workspace")
+    return n.value
+
+
+def mx_block_scaled_dot(lhs: torch.Tensor, rhs: torch.Tensor, lhs_scale: torch.Tensor, rhs_scale: torch.Tensor,
+                        elem_dtype: str = "e4m3fn", out_dtype: str = "f32", *, lhs_batch=(), rhs_batch=(),
+                        lhs_contract=(-1,), rhs_contract=(-1,), out: torch.Tensor | None = None,
+                        workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """block_scaled_dot with dot dimension numbers; operands are dense uint8
+    code tensors, scales their shape with the contracting extent / 32."""
+    for t in (lhs, rhs, lhs_scale, rhs_scale):
+        if not t.is_contiguous():
+            raise ValueError("mx_block_scaled_dot takes dense (contiguous) tensors")
+    dims = make_dot_dims(lhs_batch, rhs_batch, lhs_contract, rhs_contract)
+    shape = mx_block_scaled_dot_shape(lhs.shape, rhs.shape, dims)
+    if out is None:
+        out = torch.empty(shape, dtype=torch.float32 if out_dtype == "f32" else torch.bfloat16, device=lhs.device)
+    ws_bytes = mx_block_scaled_dot_workspace(lhs.shape, rhs.shape, dims)
+    if workspace is None and ws_bytes:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=lhs.device)
+    _check(_lib.mx_block_scaled_dot(_dev_ptr(lhs), _dims_array(lhs.shape), lhs.dim(), _dev_ptr(lhs_scale),
+                                    _dev_ptr(rhs), _dims_array(rhs.shape), rhs.dim(), _dev_ptr(rhs_scale),
+                                    ctypes.byref(dims), DTYPES[elem_dtype], DTYPES[out_dtype], _dev_ptr(out),
+                                    _dev_ptr(workspace), workspace.numel() if workspace is not None else 0,
+                                    _stream(stream)),
+           "mx_block_scaled_dot")
     return out
 
 

@@ -80,15 +80,23 @@ struct KParams {
     int vec_store;       // 16-byte row stores allowed (aligned c and pitch)
     int num_m_tiles, num_n_tiles, num_kb;
     int num_sf_n_tiles;  // 128-row scale tiles of B
+    int batch;           // independent problems; tiles run batch-major
+    int64_t c_batch_stride;   // elements between consecutive C matrices
+    int64_t sfa_batch_tiles;  // 512-byte scale tiles per problem (A / B)
+    int64_t sfb_batch_tiles;
     int group_m;
     uint32_t idesc;
     uint64_t timeout_ns;
     int skip_producer;   // fault injection: never issue loads (waits must time out)
 };
 
-// Tile order: groups of `group_m` M-tiles, column-major inside a group, so
-// the tiles running at once share A and B panels in L2.
-__device__ __forceinline__ void tile_coords(int t, const KParams& p, int& mt, int& nt) {
+// Tile order: problem by problem; inside one, groups of `group_m` M-tiles,
+// column-major inside a group, so the tiles running at once share A and B
+// panels in L2.
+__device__ __forceinline__ void tile_coords(int t, const KParams& p, int& b, int& mt, int& nt) {
+    const int per_problem = p.num_m_tiles * p.num_n_tiles;
+    b = t / per_problem;
+    t -= b * per_problem;
     const int group = p.group_m * p.num_n_tiles;
     const int g = t / group;
     const int first_m = g * p.group_m;
@@ -104,11 +112,13 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return r;
 }
 
-// Store one accumulator row segment: row m, columns [n0, n0 + 128).
-__device__ __forceinline__ void store_row128(const KParams& p, int64_t m, int64_t n0, const uint32_t (&v)[4][32]) {
+// Store one accumulator row segment of problem b: row m, columns [n0, n0 + 128).
+__device__ __forceinline__ void store_row128(const KParams& p, int b, int64_t m, int64_t n0,
+                                             const uint32_t (&v)[4][32]) {
     if (m >= p.M || n0 >= p.N) return;
+    const int64_t row = static_cast<int64_t>(b) * p.c_batch_stride + m * p.ldc + n0;
     if (p.out_bf16) {
-        uint16_t* crow = reinterpret_cast<uint16_t*>(p.c) + m * p.ldc + n0;
+        uint16_t* crow = reinterpret_cast<uint16_t*>(p.c) + row;
         if (p.vec_store && n0 + 128 <= p.N) {
 #pragma unroll
             for (int j = 0; j < 4; ++j)
@@ -131,7 +141,7 @@ __device__ __forceinline__ void store_row128(const KParams& p, int64_t m, int64_
                             static_cast<uint16_t>(pack_bf16x2(__uint_as_float(v[j][i]), 0.0f) & 0xFFFFu);
         }
     } else {
-        float* crow = reinterpret_cast<float*>(p.c) + m * p.ldc + n0;
+        float* crow = reinterpret_cast<float*>(p.c) + row;
         if (p.vec_store && n0 + 128 <= p.N) {
 #pragma unroll
             for (int j = 0; j < 4; ++j)
@@ -214,7 +224,7 @@ __global__ void __launch_bounds__(sm1::THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    const int num_tiles = p.num_m_tiles * p.num_n_tiles;
+    const int num_tiles = p.batch * p.num_m_tiles * p.num_n_tiles;
 
     if (warp == 0) {
         if (lane == 0 && !p.skip_producer) {
@@ -222,10 +232,12 @@ __global__ void __launch_bounds__(sm1::THREADS, 1)
             uint32_t phase = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-                int mt, nt;
-                tile_coords(t, p, mt, nt);
+                int b, mt, nt;
+                tile_coords(t, p, b, mt, nt);
                 const int nsf0 = 2 * nt;
                 const int nsf1 = (2 * nt + 1 < p.num_sf_n_tiles) ? 2 * nt + 1 : 2 * nt;
+                const uint8_t* sfa = p.sfa + static_cast<size_t>(b) * p.sfa_batch_tiles * 512u;
+                const uint8_t* sfb = p.sfb + static_cast<size_t>(b) * p.sfb_batch_tiles * 512u;
                 for (int kb = 0; kb < p.num_kb; ++kb) {
                     if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, p.timeout_ns, &g_mx_status)) {
                         ok = false;
@@ -233,14 +245,14 @@ __global__ void __launch_bounds__(sm1::THREADS, 1)
                     }
                     const uint32_t fb = full_bar(stage);
                     mbar_arrive_expect_tx(fb, STAGE_TX);
-                    tma_load_2d(sb + OFF_A + stage * A_STAGE, &tmap_a, fb, kb * BK, mt * BM);
-                    tma_load_2d(sb + OFF_B + stage * B_STAGE, &tmap_b, fb, kb * BK, nt * BN);
+                    tma_load_3d(sb + OFF_A + stage * A_STAGE, &tmap_a, fb, kb * BK, mt * BM, b);
+                    tma_load_3d(sb + OFF_B + stage * B_STAGE, &tmap_b, fb, kb * BK, nt * BN, b);
                     bulk_load(sb + OFF_SFA + stage * SFA_STAGE,
-                              p.sfa + (static_cast<size_t>(mt) * p.num_kb + kb) * 512u, 512u, fb);
+                              sfa + (static_cast<size_t>(mt) * p.num_kb + kb) * 512u, 512u, fb);
                     bulk_load(sb + OFF_SFB + stage * SFB_STAGE,
-                              p.sfb + (static_cast<size_t>(nsf0) * p.num_kb + kb) * 512u, 512u, fb);
+                              sfb + (static_cast<size_t>(nsf0) * p.num_kb + kb) * 512u, 512u, fb);
                     bulk_load(sb + OFF_SFB + stage * SFB_STAGE + 512u,
-                              p.sfb + (static_cast<size_t>(nsf1) * p.num_kb + kb) * 512u, 512u, fb);
+                              sfb + (static_cast<size_t>(nsf1) * p.num_kb + kb) * 512u, 512u, fb);
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
@@ -334,8 +346,8 @@ __global__ void __launch_bounds__(sm1::THREADS, 1)
         const int half = (warp - 2) >> 2;      // accumulator columns [128*half, +128)
         uint32_t acc_phase = 0;
         for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
-            int mt, nt;
-            tile_coords(t, p, mt, nt);
+            int b, mt, nt;
+            tile_coords(t, p, b, mt, nt);
             // one lane waits; the warp follows its verdict so it never diverges
             bool ok = true;
             if (lane == 0) ok = mbar_wait_bounded(tmem_full, acc_phase, abort_flag, p.timeout_ns, &g_mx_status);
@@ -350,7 +362,7 @@ __global__ void __launch_bounds__(sm1::THREADS, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(tmem_empty);
             acc_phase ^= 1u;
-            store_row128(p, static_cast<int64_t>(mt) * BM + quarter * 32 + lane,
+            store_row128(p, b, static_cast<int64_t>(mt) * BM + quarter * 32 + lane,
                          static_cast<int64_t>(nt) * BN + half * 128, v);
         }
     }
@@ -435,7 +447,7 @@ __global__ void __launch_bounds__(sm2::THREADS, 1)
     cluster_sync_all();  // the peer's barriers are initialised before any remote use
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    const int num_tiles = p.num_m_tiles * p.num_n_tiles;  // pair tiles
+    const int num_tiles = p.batch * p.num_m_tiles * p.num_n_tiles;  // pair tiles
 
     if (warp == 0) {
         if (lane == 0 && !p.skip_producer) {
@@ -443,11 +455,16 @@ __global__ void __launch_bounds__(sm2::THREADS, 1)
             uint32_t phase = 0;
             bool ok = true;
             for (int t = cluster; t < num_tiles && ok; t += num_clusters) {
-                int mt, nt;
-                tile_coords(t, p, mt, nt);
+                int b, mt, nt;
+                tile_coords(t, p, b, mt, nt);
                 const int a_row = mt * BM + static_cast<int>(rank) * 128;
                 const int b_row = nt * BN + static_cast<int>(rank) * 128;
-                const int sfa_tile = 2 * mt + static_cast<int>(rank);
+                // scale tiles past this problem's last one belong to rows past
+                // M / N (the next problem's tiles, or zeros past the buffer):
+                // their products land in rows the epilogue never stores
+                const int64_t sfa_tile = b * p.sfa_batch_tiles + (2 * mt + static_cast<int>(rank)) * p.num_kb;
+                const int64_t sfb_tile0 = b * p.sfb_batch_tiles + (2 * nt) * p.num_kb;
+                const int64_t sfb_tile1 = sfb_tile0 + p.num_kb;
                 for (int kb = 0; kb < p.num_kb; ++kb) {
                     if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, p.timeout_ns, &g_mx_status)) {
                         ok = false;
@@ -455,14 +472,14 @@ __global__ void __launch_bounds__(sm2::THREADS, 1)
                     }
                     const uint32_t fb = mapa_shared(full_bar(stage), 0);
                     if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), PAIR_TX);
-                    tma_load_2d_pair(sb + OFF_A + stage * A_STAGE, &tmap_a, fb, kb * BK, a_row);
-                    tma_load_2d_pair(sb + OFF_B + stage * B_STAGE, &tmap_b, fb, kb * BK, b_row);
+                    tma_load_3d_pair(sb + OFF_A + stage * A_STAGE, &tmap_a, fb, kb * BK, a_row, b);
+                    tma_load_3d_pair(sb + OFF_B + stage * B_STAGE, &tmap_b, fb, kb * BK, b_row, b);
                     tma_load_2d_pair(sb + OFF_SFA + stage * SFA_STAGE, &tmap_sfa, fb, 0,
-                                     2 * (sfa_tile * p.num_kb + kb));
+                                     static_cast<int>(2 * (sfa_tile + kb)));
                     tma_load_2d_pair(sb + OFF_SFB + stage * SFB_STAGE, &tmap_sfb, fb, 0,
-                                     2 * ((2 * nt) * p.num_kb + kb));
+                                     static_cast<int>(2 * (sfb_tile0 + kb)));
                     tma_load_2d_pair(sb + OFF_SFB + stage * SFB_STAGE + 512u, &tmap_sfb, fb, 0,
-                                     2 * ((2 * nt + 1) * p.num_kb + kb));
+                                     static_cast<int>(2 * (sfb_tile1 + kb)));
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
@@ -561,8 +578,8 @@ __global__ void __launch_bounds__(sm2::THREADS, 1)
         const uint32_t tmem_empty_rank0 = mapa_shared(tmem_empty, 0);
         uint32_t acc_phase = 0;
         for (int t = cluster; t < num_tiles; t += num_clusters) {
-            int mt, nt;
-            tile_coords(t, p, mt, nt);
+            int b, mt, nt;
+            tile_coords(t, p, b, mt, nt);
             bool ok = true;
             if (lane == 0) ok = mbar_wait_bounded(tmem_full, acc_phase, abort_flag, p.timeout_ns, &g_mx_status);
             ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -576,7 +593,7 @@ __global__ void __launch_bounds__(sm2::THREADS, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(tmem_empty_rank0);
             acc_phase ^= 1u;
-            store_row128(p, static_cast<int64_t>(mt) * BM + rank * 128 + quarter * 32 + lane,
+            store_row128(p, b, static_cast<int64_t>(mt) * BM + rank * 128 + quarter * 32 + lane,
                          static_cast<int64_t>(nt) * BN + half * 128, v);
         }
     }
@@ -604,15 +621,18 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
-// K-major FP8 operand [rows, k] as a 2-D tensor map with a (128 B x box_rows) box, 128B swizzle.
-bool make_operand_map(CUtensorMap* map, const void* base, int64_t rows, int64_t k, uint32_t box_rows) {
+// K-major FP8 operands [batch, rows, k] (problem stride `batch_stride` bytes)
+// as a 3-D tensor map with a (128 B x box_rows x 1) box, 128B swizzle.  Rows
+// past `rows` read as zeros inside each problem.
+bool make_operand_map(CUtensorMap* map, const void* base, int64_t rows, int64_t k, uint32_t box_rows,
+                      int64_t batch, int64_t batch_stride) {
     auto enc = tensor_map_encoder();
     if (!enc) return false;
-    cuuint64_t dims[2] = {static_cast<cuuint64_t>(k), static_cast<cuuint64_t>(rows)};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(k)};
-    cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), box_rows};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(k), static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(batch)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(k), static_cast<cuuint64_t>(batch_stride)};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(BK), box_rows, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
@@ -651,6 +671,10 @@ KParams base_params(const GemmArgs& g, int bm, int bn) {
     p.num_n_tiles = static_cast<int>((g.N + bn - 1) / bn);
     p.num_kb = static_cast<int>((g.K + BK - 1) / BK);
     p.num_sf_n_tiles = static_cast<int>((g.N + 127) / 128);
+    p.batch = static_cast<int>(g.batch);
+    p.c_batch_stride = g.c_batch_stride;
+    p.sfa_batch_tiles = ((g.M + 127) / 128) * static_cast<int64_t>(p.num_kb);
+    p.sfb_batch_tiles = ((g.N + 127) / 128) * static_cast<int64_t>(p.num_kb);
     p.group_m = 16;
     p.idesc = make_idesc_mxf8(g.elem_fmt, g.elem_fmt, bm, bn);
     p.timeout_ns = g_timeout_ns;
@@ -666,10 +690,11 @@ cudaError_t launch_1sm(const GemmArgs& g, cudaStream_t stream) {
     });
     if (attr_err != cudaSuccess) return attr_err;
     CUtensorMap ma, mb;
-    if (!make_operand_map(&ma, g.a, g.M, g.K, sm1::BM) || !make_operand_map(&mb, g.bt, g.N, g.K, sm1::BN))
+    if (!make_operand_map(&ma, g.a, g.M, g.K, sm1::BM, g.batch, g.a_batch_stride) ||
+        !make_operand_map(&mb, g.bt, g.N, g.K, sm1::BN, g.batch, g.b_batch_stride))
         return cudaErrorInvalidValue;
     KParams p = base_params(g, sm1::BM, sm1::BN);
-    const int tiles = p.num_m_tiles * p.num_n_tiles;
+    const int tiles = p.batch * p.num_m_tiles * p.num_n_tiles;
     const int sms = device_sm_count();
     const int grid = tiles < sms ? tiles : sms;
     mx_gemm_kernel<<<grid, sm1::THREADS, sm1::SMEM_ALLOC, stream>>>(ma, mb, p);
@@ -718,13 +743,14 @@ cudaError_t launch_2sm(const GemmArgs& g, cudaStream_t stream) {
     });
     if (attr_err != cudaSuccess) return attr_err;
     CUtensorMap ma, mb, msa, msb;
-    const int64_t sfa_tiles = ((g.M + 127) / 128) * ((g.K + 127) / 128);
-    const int64_t sfb_tiles = ((g.N + 127) / 128) * ((g.K + 127) / 128);
-    if (!make_operand_map(&ma, g.a, g.M, g.K, 128) || !make_operand_map(&mb, g.bt, g.N, g.K, 128) ||
+    const int64_t sfa_tiles = g.batch * ((g.M + 127) / 128) * ((g.K + 127) / 128);
+    const int64_t sfb_tiles = g.batch * ((g.N + 127) / 128) * ((g.K + 127) / 128);
+    if (!make_operand_map(&ma, g.a, g.M, g.K, 128, g.batch, g.a_batch_stride) ||
+        !make_operand_map(&mb, g.bt, g.N, g.K, 128, g.batch, g.b_batch_stride) ||
         !make_sf_map(&msa, g.sfa, sfa_tiles) || !make_sf_map(&msb, g.sfb, sfb_tiles))
         return cudaErrorInvalidValue;
     KParams p = base_params(g, sm2::BM, sm2::BN);
-    const int tiles = p.num_m_tiles * p.num_n_tiles;
+    const int tiles = p.batch * p.num_m_tiles * p.num_n_tiles;
     const int cap = max_pair_clusters();
     const int clusters = tiles < cap ? tiles : cap;
     cudaLaunchConfig_t cfg;

@@ -149,6 +149,127 @@ uint32_t fp4_pair_perm(int stride) {
 mx_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MX_OK : MX_ERR_CUDA; }
 
 size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// General block-scaled dot: each operand is brought to [batch, rows, K]
+// (batch axes in the listed order, free axes in their own order, the
+// contracting axis innermost); perm[c] is the operand axis at canonical
+// position c.
+struct DotPlan {
+    int64_t batch = 1, M = 0, N = 0, K = 0;
+    int lrank = 0, rrank = 0;
+    int lperm[MX_MAX_RANK] = {}, rperm[MX_MAX_RANK] = {};
+    int lc = 0, rc = 0;
+    bool lcanon = true, rcanon = true;
+    size_t off_lq = 0, off_ls = 0, off_rq = 0, off_rs = 0, off_sfa = 0, off_sfb = 0, total = 0;
+};
+
+mx_status plan_dot(const int64_t* ldims, int lrank, const int64_t* rdims, int rrank, const mx_dot_dims* dn,
+                   DotPlan* P) {
+    if (!ldims || !rdims || !dn || !P) return MX_ERR_INVALID_ARG;
+    // the contract's checks: rank >= 2, equal batch counts, indices in
+    // bounds, batch extents equal, contracting sizes equal and disjoint from
+    // the batch dimensions; one contracting dimension per operand
+    if (lrank < 2 || rrank < 2 || lrank > MX_MAX_RANK || rrank > MX_MAX_RANK) return MX_ERR_SHAPE;
+    for (int i = 0; i < lrank; ++i)
+        if (ldims[i] < 0) return MX_ERR_INVALID_ARG;
+    for (int i = 0; i < rrank; ++i)
+        if (rdims[i] < 0) return MX_ERR_INVALID_ARG;
+    if (dn->lhs_n_batch != dn->rhs_n_batch || dn->lhs_n_batch < 0 || dn->lhs_n_batch > MX_MAX_RANK) return MX_ERR_DIM;
+    if (dn->lhs_n_contract != 1 || dn->rhs_n_contract != 1) return MX_ERR_DIM;
+    auto norm = [](int64_t d, int r, int* out) {
+        if (d < -r || d >= r) return false;
+        *out = static_cast<int>(d < 0 ? d + r : d);
+        return true;
+    };
+    const int nb = dn->lhs_n_batch;
+    int lb[MX_MAX_RANK], rb[MX_MAX_RANK];
+    bool lused[MX_MAX_RANK] = {}, rused[MX_MAX_RANK] = {};
+    for (int i = 0; i < nb; ++i) {
+        if (!norm(dn->lhs_batch[i], lrank, &lb[i]) || !norm(dn->rhs_batch[i], rrank, &rb[i])) return MX_ERR_DIM;
+        if (lused[lb[i]] || rused[rb[i]]) return MX_ERR_DIM;
+        lused[lb[i]] = rused[rb[i]] = true;
+    }
+    int lc, rc;
+    if (!norm(dn->lhs_contract[0], lrank, &lc) || !norm(dn->rhs_contract[0], rrank, &rc)) return MX_ERR_DIM;
+    if (lused[lc] || rused[rc]) return MX_ERR_DIM;
+    lused[lc] = rused[rc] = true;
+    int64_t batch = 1;
+    for (int i = 0; i < nb; ++i) {
+        if (ldims[lb[i]] != rdims[rb[i]]) return MX_ERR_SHAPE;
+        batch *= ldims[lb[i]];
+    }
+    const int64_t K = ldims[lc];
+    if (K != rdims[rc] || K < 32 || K % 32 != 0) return MX_ERR_SHAPE;
+    DotPlan p;
+    p.lrank = lrank;
+    p.rrank = rrank;
+    p.lc = lc;
+    p.rc = rc;
+    int n = 0;
+    for (int i = 0; i < nb; ++i) p.lperm[n++] = lb[i];
+    int64_t M = 1;
+    for (int i = 0; i < lrank; ++i)
+        if (!lused[i]) p.lperm[n++] = i, M *= ldims[i];
+    p.lperm[n] = lc;
+    n = 0;
+    for (int i = 0; i < nb; ++i) p.rperm[n++] = rb[i];
+    int64_t N = 1;
+    for (int i = 0; i < rrank; ++i)
+        if (!rused[i]) p.rperm[n++] = i, N *= rdims[i];
+    p.rperm[n] = rc;
+    for (int i = 0; i < lrank; ++i) p.lcanon = p.lcanon && p.lperm[i] == i;
+    for (int i = 0; i < rrank; ++i) p.rcanon = p.rcanon && p.rperm[i] == i;
+    if (M > (int64_t(1) << 30) || N > (int64_t(1) << 30) || K > (int64_t(1) << 30)) return MX_ERR_SHAPE;
+    // tiles of all problems are counted in 32-bit integers by the kernels
+    if (batch * ((M + 127) / 128) * ((N + 127) / 128) > (int64_t(1) << 30)) return MX_ERR_SHAPE;
+    p.batch = batch;
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    size_t off = 0;
+    if (!p.lcanon) {
+        p.off_lq = off;
+        off += align256(static_cast<size_t>(batch * M * K));
+        p.off_ls = off;
+        off += align256(static_cast<size_t>(batch * M * (K / 32)));
+    }
+    if (!p.rcanon) {
+        p.off_rq = off;
+        off += align256(static_cast<size_t>(batch * N * K));
+        p.off_rs = off;
+        off += align256(static_cast<size_t>(batch * N * (K / 32)));
+    }
+    p.off_sfa = off;
+    off += align256(static_cast<size_t>(batch) * sf_layout_bytes(M, K));
+    p.off_sfb = off;
+    off += align256(static_cast<size_t>(batch) * sf_layout_bytes(N, K));
+    p.total = off;
+    *P = p;
+    return MX_OK;
+}
+
+// Copy an operand (codes, or scales with the contracting axis divided by 32)
+// into canonical order.
+cudaError_t permute_operand(const void* src, const int64_t* dims, int rank, const int* perm, int contract,
+                            int64_t contract_div, uint8_t* dst, cudaStream_t s) {
+    int64_t ext[MX_MAX_RANK], stride[MX_MAX_RANK];
+    for (int i = 0; i < rank; ++i) ext[i] = i == contract ? dims[i] / contract_div : dims[i];
+    int64_t st = 1;
+    for (int i = rank - 1; i >= 0; --i) {
+        stride[i] = st;
+        st *= ext[i];
+    }
+    PermuteArgs a{};
+    a.src = static_cast<const uint8_t*>(src);
+    a.dst = dst;
+    a.rank = rank;
+    for (int c = 0; c < rank; ++c) {
+        a.dst_dims[c] = ext[perm[c]];
+        a.src_stride[c] = stride[perm[c]];
+    }
+    return launch_permute_bytes(a, s);
+}
 
 }  // namespace
 
@@ -348,6 +469,10 @@ mx_status mx_scaled_matmul(const void* a, const void* bt, const uint8_t* a_scale
     g.elem_fmt = elem_dtype == MX_E4M3FN ? kE4M3 : kE5M2;
     g.out_bf16 = out_dtype == MX_BF16;
     g.vec_store = aligned16(c) && (ldc * (out_dtype == MX_F32 ? 4 : 2)) % 16 == 0;
+    g.batch = 1;
+    g.a_batch_stride = M * K;
+    g.b_batch_stride = N * K;
+    g.c_batch_stride = M * ldc;
     return from_cuda(launch_scaled_matmul(g, s));
 }
 
@@ -384,6 +509,92 @@ mx_status mx_fused_quantize_matmul(const void* x, mx_dtype x_dtype, int64_t ld_x
     st = mx_quantize(x, x_dtype, M, K, ld_x, elem_dtype, &cfg, xq, xs, stream);
     if (st != MX_OK) return st;
     return mx_scaled_matmul(xq, wt, xs, w_scale_sf, 1, elem_dtype, M, N, K, out_dtype, c, ldc, nullptr, 0, stream);
+}
+
+mx_status mx_block_scaled_dot_shape(const int64_t* lhs_dims, int lhs_rank, const int64_t* rhs_dims, int rhs_rank,
+                                    const mx_dot_dims* dims, int64_t* out_dims, int* out_rank) {
+    DotPlan P;
+    mx_status st = plan_dot(lhs_dims, lhs_rank, rhs_dims, rhs_rank, dims, &P);
+    if (st != MX_OK) return st;
+    if (!out_dims || !out_rank) return MX_ERR_INVALID_ARG;
+    int n = 0;
+    for (int c = 0; c < lhs_rank - 1; ++c) out_dims[n++] = lhs_dims[P.lperm[c]];
+    for (int c = dims->rhs_n_batch; c < rhs_rank - 1; ++c) out_dims[n++] = rhs_dims[P.rperm[c]];
+    *out_rank = n;
+    return MX_OK;
+}
+
+mx_status mx_block_scaled_dot_workspace(const int64_t* lhs_dims, int lhs_rank, const int64_t* rhs_dims,
+                                        int rhs_rank, const mx_dot_dims* dims, size_t* bytes) {
+    DotPlan P;
+    mx_status st = plan_dot(lhs_dims, lhs_rank, rhs_dims, rhs_rank, dims, &P);
+    if (st != MX_OK) return st;
+    if (!bytes) return MX_ERR_INVALID_ARG;
+    *bytes = P.total;
+    return MX_OK;
+}
+
+mx_status mx_block_scaled_dot(const void* lhs, const int64_t* lhs_dims, int lhs_rank, const void* lhs_scale,
+                              const void* rhs, const int64_t* rhs_dims, int rhs_rank, const void* rhs_scale,
+                              const mx_dot_dims* dims, mx_dtype elem_dtype, mx_dtype out_dtype, void* out,
+                              void* workspace, size_t workspace_bytes, mx_stream stream) {
+    DotPlan P;
+    mx_status st = plan_dot(lhs_dims, lhs_rank, rhs_dims, rhs_rank, dims, &P);
+    if (st != MX_OK) return st;
+    if (elem_dtype != MX_E4M3FN && elem_dtype != MX_E5M2) return MX_ERR_UNSUPPORTED_DTYPE;
+    if (out_dtype != MX_F32 && out_dtype != MX_BF16) return MX_ERR_UNSUPPORTED_DTYPE;
+    if (P.batch == 0 || P.M == 0 || P.N == 0) return MX_OK;
+    if (!lhs || !rhs || !lhs_scale || !rhs_scale || !out) return MX_ERR_INVALID_ARG;
+    const uintptr_t esize = out_dtype == MX_F32 ? 4 : 2;
+    if ((P.lcanon && !aligned16(lhs)) || (P.rcanon && !aligned16(rhs)) ||
+        (reinterpret_cast<uintptr_t>(out) & (esize - 1)))
+        return MX_ERR_ALIGNMENT;
+    if (!workspace || workspace_bytes < P.total) return MX_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return MX_ERR_ALIGNMENT;
+    if (!device_is_sm103()) return MX_ERR_DEVICE;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    const uint8_t* a = static_cast<const uint8_t*>(lhs);
+    const uint8_t* sa = static_cast<const uint8_t*>(lhs_scale);
+    const uint8_t* bt = static_cast<const uint8_t*>(rhs);
+    const uint8_t* sb = static_cast<const uint8_t*>(rhs_scale);
+    cudaError_t e = cudaSuccess;
+    if (!P.lcanon) {
+        e = permute_operand(lhs, lhs_dims, lhs_rank, P.lperm, P.lc, 1, ws + P.off_lq, s);
+        if (e == cudaSuccess) e = permute_operand(lhs_scale, lhs_dims, lhs_rank, P.lperm, P.lc, 32, ws + P.off_ls, s);
+        a = ws + P.off_lq;
+        sa = ws + P.off_ls;
+    }
+    if (e == cudaSuccess && !P.rcanon) {
+        e = permute_operand(rhs, rhs_dims, rhs_rank, P.rperm, P.rc, 1, ws + P.off_rq, s);
+        if (e == cudaSuccess) e = permute_operand(rhs_scale, rhs_dims, rhs_rank, P.rperm, P.rc, 32, ws + P.off_rs, s);
+        bt = ws + P.off_rq;
+        sb = ws + P.off_rs;
+    }
+    const int64_t kb = P.K / 32;
+    if (e == cudaSuccess)
+        e = launch_repack_scales_batched(sa, P.M, P.K, kb, P.M * kb, P.batch, ws + P.off_sfa, s);
+    if (e == cudaSuccess)
+        e = launch_repack_scales_batched(sb, P.N, P.K, kb, P.N * kb, P.batch, ws + P.off_sfb, s);
+    if (e != cudaSuccess) return MX_ERR_CUDA;
+    GemmArgs g{};
+    g.a = a;
+    g.bt = bt;
+    g.sfa = ws + P.off_sfa;
+    g.sfb = ws + P.off_sfb;
+    g.M = P.M;
+    g.N = P.N;
+    g.K = P.K;
+    g.c = out;
+    g.ldc = P.N;
+    g.elem_fmt = elem_dtype == MX_E4M3FN ? kE4M3 : kE5M2;
+    g.out_bf16 = out_dtype == MX_BF16;
+    g.vec_store = aligned16(out) && (P.N * static_cast<int64_t>(esize)) % 16 == 0;
+    g.batch = P.batch;
+    g.a_batch_stride = P.M * P.K;
+    g.b_batch_stride = P.N * P.K;
+    g.c_batch_stride = P.M * P.N;
+    return from_cuda(launch_scaled_matmul(g, s));
 }
 
 mx_status mx_get_device_status(int* status) {

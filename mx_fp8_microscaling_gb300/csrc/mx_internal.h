@@ -56,6 +56,23 @@ cudaError_t launch_dequantize(const DequantArgs& q, int fmt, bool out_bf16, cuda
 // Scale-factor repack: plain [mn, k/32] -> SF tiles (see mx_repack_scales).
 cudaError_t launch_repack_scales(const uint8_t* plain, int64_t mn, int64_t k, int64_t ld_plain,
                                  uint8_t* sf, cudaStream_t stream);
+// `batch` problems: plain scales every plain_batch_stride bytes, SF layouts
+// back to back (sf_layout_bytes(mn, k) each).
+cudaError_t launch_repack_scales_batched(const uint8_t* plain, int64_t mn, int64_t k, int64_t ld_plain,
+                                         int64_t plain_batch_stride, int64_t batch, uint8_t* sf,
+                                         cudaStream_t stream);
+
+// Byte-tensor permutation: dst (dense, `rank` axes of extents dst_dims,
+// outermost first) takes dst[i_0, .., i_{r-1}] = src[sum_a i_a * src_stride[a]].
+constexpr int kMaxPermuteRank = 8;
+struct PermuteArgs {
+    const uint8_t* src;
+    uint8_t* dst;
+    int rank;
+    int64_t dst_dims[kMaxPermuteRank];
+    int64_t src_stride[kMaxPermuteRank];  // elements
+};
+cudaError_t launch_permute_bytes(const PermuteArgs& a, cudaStream_t stream);
 size_t sf_layout_bytes(int64_t mn, int64_t k);
 
 // Block-scaled GEMM on SF-layout scales.
@@ -70,6 +87,11 @@ struct GemmArgs {
     int32_t elem_fmt;        // kE4M3 | kE5M2
     int32_t out_bf16;        // 1: bf16 output, 0: f32
     int32_t vec_store;       // 1: c and ldc allow 16-byte row stores
+    // `batch` independent problems: A, Bt and C advance by their batch strides
+    // (bytes, bytes, elements); sfa / sfb hold the problems' SF layouts back
+    // to back (sf_layout_bytes(M, K) / (N, K) each).
+    int64_t batch;
+    int64_t a_batch_stride, b_batch_stride, c_batch_stride;
 };
 cudaError_t launch_scaled_matmul(const GemmArgs& g, cudaStream_t stream);
 

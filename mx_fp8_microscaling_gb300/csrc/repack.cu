@@ -10,7 +10,8 @@
 // Padding rows/columns are written as 0.
 //
 // One thread writes one 32-bit word (the four K-block scales of one row), so
-// stores are fully coalesced; the reads gather four rows 32 apart.
+// stores are fully coalesced; the reads gather four rows 32 apart.  A batch of
+// problems is one launch: their SF layouts are written back to back.
 
 #include <cstdint>
 
@@ -20,10 +21,15 @@ namespace mx {
 namespace {
 
 __global__ void __launch_bounds__(256) repack_sf_kernel(const uint8_t* __restrict__ plain, int64_t mn,
-                                                       int64_t kb, int64_t ld, int64_t ntk,
-                                                       int64_t nwords, uint32_t* __restrict__ sf) {
+                                                       int64_t kb, int64_t ld, int64_t ntk, int64_t nwords,
+                                                       int64_t plain_batch_stride, int64_t batch,
+                                                       uint32_t* __restrict__ sf) {
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    for (int64_t w = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; w < nwords; w += stride) {
+    const int64_t total = nwords * batch;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total; i += stride) {
+        const int64_t b = batch == 1 ? 0 : i / nwords;
+        const int64_t w = i - b * nwords;
+        const uint8_t* src = plain + b * plain_batch_stride;
         const int64_t tile = w >> 7;          // 128 words per 512-byte tile
         const int within = static_cast<int>(w & 127);
         const int64_t tm = tile / ntk, tk = tile - (tile / ntk) * ntk;
@@ -33,9 +39,9 @@ __global__ void __launch_bounds__(256) repack_sf_kernel(const uint8_t* __restric
         if (r < mn) {
 #pragma unroll
             for (int j = 0; j < 4; ++j)
-                if (c0 + j < kb) word |= static_cast<uint32_t>(plain[r * ld + c0 + j]) << (8 * j);
+                if (c0 + j < kb) word |= static_cast<uint32_t>(src[r * ld + c0 + j]) << (8 * j);
         }
-        sf[w] = word;
+        sf[i] = word;
     }
 }
 
@@ -46,18 +52,24 @@ size_t sf_layout_bytes(int64_t mn, int64_t k) {
     return static_cast<size_t>((mn + 127) / 128) * static_cast<size_t>((kb + 3) / 4) * 512u;
 }
 
-cudaError_t launch_repack_scales(const uint8_t* plain, int64_t mn, int64_t k, int64_t ld_plain,
-                                 uint8_t* sf, cudaStream_t stream) {
+cudaError_t launch_repack_scales_batched(const uint8_t* plain, int64_t mn, int64_t k, int64_t ld_plain,
+                                         int64_t plain_batch_stride, int64_t batch, uint8_t* sf,
+                                         cudaStream_t stream) {
     const int64_t kb = k / 32;
     const int64_t ntk = (kb + 3) / 4;
     const int64_t nwords = static_cast<int64_t>(sf_layout_bytes(mn, k) / 4);
-    if (nwords == 0) return cudaSuccess;
-    int64_t blocks = (nwords + 255) / 256;
+    if (nwords == 0 || batch == 0) return cudaSuccess;
+    int64_t blocks = (nwords * batch + 255) / 256;
     const int64_t cap = static_cast<int64_t>(device_sm_count()) * 8;
     if (blocks > cap) blocks = cap;
     repack_sf_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-        plain, mn, kb, ld_plain, ntk, nwords, reinterpret_cast<uint32_t*>(sf));
+        plain, mn, kb, ld_plain, ntk, nwords, plain_batch_stride, batch, reinterpret_cast<uint32_t*>(sf));
     return cudaGetLastError();
+}
+
+cudaError_t launch_repack_scales(const uint8_t* plain, int64_t mn, int64_t k, int64_t ld_plain,
+                                 uint8_t* sf, cudaStream_t stream) {
+    return launch_repack_scales_batched(plain, mn, k, ld_plain, 0, 1, sf, stream);
 }
 
 }  // namespace mx

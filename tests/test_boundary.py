@@ -161,3 +161,71 @@ def test_folded_view_rules(mx):
     assert mx._view2d(y, -1) == (16, 32, 64)
     with pytest.raises(ValueError):
         mx._view2d(torch.zeros(8, 32, dtype=torch.bfloat16).t(), -1)
+
+
+# ---- general block-scaled dot: the contract's dimension checks
+
+@pytest.mark.parametrize("lshape,rshape,lb,rb,lc,rc,status", [
+    ((4,), (4, 32), (), (), (0,), (1,), 5),                   # rank < 2
+    ((2, 32), (2, 32), (0,), (), (1,), (1,), 4),              # batch counts differ
+    ((2, 32), (2, 32), (2,), (0,), (1,), (1,), 4),            # batch index out of bounds
+    ((2, 32), (3, 32), (0,), (0,), (1,), (1,), 5),            # batch extents differ
+    ((2, 32), (2, 64), (), (), (1,), (1,), 5),                # contracting sizes differ
+    ((2, 32), (2, 32), (1,), (1,), (1,), (1,), 4),            # contracting overlaps batch
+    ((2, 32, 32), (2, 32), (), (), (1, 2), (1,), 4),          # two contracting dims
+    ((2, 48), (2, 48), (), (), (1,), (1,), 5),                # K not a multiple of 32
+    ((2, 2, 32), (2, 2, 32), (0, 0), (0, 1), (2,), (2,), 4),  # repeated batch dim
+    ((2, 32), (2, 32), (), (), (5,), (1,), 4),                # contracting index out of bounds
+    ((2, 32), (2, 32), (), (), (-3,), (1,), 4),               # negative index past the rank
+])
+def test_dot_dimension_errors(mx, lshape, rshape, lb, rb, lc, rc, status):
+    dims = mx.make_dot_dims(lb, rb, lc, rc)
+    with pytest.raises(mx.MxError) as e:
+        mx.mx_block_scaled_dot_shape(lshape, rshape, dims)
+    assert e.value.status == status
+    with pytest.raises(mx.MxError) as e:
+        mx.mx_block_scaled_dot_workspace(lshape, rshape, dims)
+    assert e.value.status == status
+
+
+@pytest.mark.parametrize("lshape,rshape,lb,rb,lc,rc,shape", [
+    ((3, 64), (5, 64), (), (), (1,), (1,), (3, 5)),
+    ((3, 64), (64, 5), (), (), (1,), (0,), (3, 5)),
+    ((2, 3, 4, 32), (32, 3, 2, 5), (0, 1), (2, 1), (3,), (0,), (2, 3, 4, 5)),
+    ((2, 32, 3, 2), (3, 32, 2), (0,), (2,), (1,), (1,), (2, 3, 2, 3)),
+    ((130, 2, 64), (2, 72, 64), (-2,), (0,), (-1,), (-1,), (2, 130, 72)),
+])
+def test_dot_result_shape(mx, lshape, rshape, lb, rb, lc, rc, shape):
+    assert mx.mx_block_scaled_dot_shape(lshape, rshape, mx.make_dot_dims(lb, rb, lc, rc)) == shape
+
+
+def test_dot_workspace_counts_only_needed_copies(mx):
+    sf = lambda mn, k: -(-mn // 128) * -(-k // 128) * 512  # noqa: E731
+    r256 = lambda n: -(-n // 256) * 256  # noqa: E731
+    d = mx.make_dot_dims((0,), (0,), (2,), (2,))
+    # both operands already [batch, rows, K]: only the SF scales
+    assert mx.mx_block_scaled_dot_workspace((4, 200, 256), (4, 300, 256), d) == r256(4 * sf(200, 256)) + \
+        r256(4 * sf(300, 256))
+    # rhs stored [batch, K, N]: a canonical copy of it and of its scales too
+    d = mx.make_dot_dims((0,), (0,), (2,), (1,))
+    assert mx.mx_block_scaled_dot_workspace((4, 200, 256), (4, 256, 300), d) == r256(4 * 300 * 256) + \
+        r256(4 * 300 * 8) + r256(4 * sf(200, 256)) + r256(4 * sf(300, 256))
+
+
+def test_dot_argument_errors(lib, mx):
+    import ctypes as ct
+    dims = mx.make_dot_dims((0,), (0,), (2,), (2,))
+    shape = (ct.c_int64 * 3)(2, 128, 128)
+    call = lambda **kw: lib.mx_block_scaled_dot(  # noqa: E731
+        kw.get("lhs", FAKE), shape, 3, FAKE, kw.get("rhs", FAKE), shape, 3, FAKE, ct.byref(dims),
+        kw.get("elem", 4), kw.get("out_dtype", 3), kw.get("out", FAKE), kw.get("ws", FAKE),
+        kw.get("ws_bytes", 1 << 30), None)
+    assert call(elem=6) == 2
+    assert call(out_dtype=4) == 2
+    assert call(lhs=None) == 1
+    assert call(lhs=FAKE_MISALIGNED) == 6   # read in place by TMA
+    assert call(out=FAKE_ODD) == 6
+    assert call(ws_bytes=16) == 7
+    assert call(ws=None) == 7
+    assert lib.mx_block_scaled_dot(FAKE, shape, 3, FAKE, FAKE, shape, 3, FAKE, None, 4, 3, FAKE, FAKE, 1 << 30,
+                                   None) == 1
