@@ -12,7 +12,10 @@ A step is one pass of the whole hot path over its synthetic inputs:
   fp4    QuantizeMX [16384, 16384] bf16 -> e2m1, 8x4, packed, interleaved;
   dequant  MX dequantize of [8192, 8192] e4m3fn codes with 8x4 scales to bf16;
   fused  activation quantize + ScaledMatmul, X [16384, 8192] bf16 times a
-         pre-quantized e4m3fn weight W [8192, 28672] -> bf16.
+         pre-quantized e4m3fn weight W [8192, 28672] -> bf16;
+  dot    batched block-scaled dot, 16 problems of 2048^3 e4m3fn -> bf16:
+         rhs stored [B, N, K] (read in place) and [B, K, N] (through the
+         transposing copy), one call each.
 The headline `value` is QuantizeMX GB/s over the sweep (algorithmic bytes:
 2 read + 1 written + 1/32 scale written per element); `scaled_matmul`,
 `fp4_quantize` and `fused` carry the other workloads with their own rooflines.
@@ -52,6 +55,8 @@ GEMM_N = 8192
 GEMM_FLOP = 2 * GEMM_N ** 3
 FUSED = (16384, 28672, 8192)
 FUSED_FLOP = 2 * FUSED[0] * FUSED[1] * FUSED[2]
+DOT = (16, 2048, 2048, 2048)  # batch, M, N, K
+DOT_FLOP = 2 * DOT[0] * DOT[1] * DOT[2] * DOT[3]
 # nominal dense MXFP8 : bf16 tensor ratio (4.5 : 2.25 PFLOP/s)
 FP8_OVER_BF16 = 2.0
 
@@ -217,6 +222,22 @@ class Api:
                 raise mx.MxError(st, "mx_scaled_matmul")
         return call
 
+    def dot(self, lhs, rhs, ls, rs, dims, fmt, out_dtype, out, work):
+        mx, ct = self.mx, self.ct
+        lshape, rshape = mx._dims_array(lhs.shape), mx._dims_array(rhs.shape)
+        args = (ct.c_void_p(lhs.data_ptr()), lshape, lhs.dim(), ct.c_void_p(ls.data_ptr()),
+                ct.c_void_p(rhs.data_ptr()), rshape, rhs.dim(), ct.c_void_p(rs.data_ptr()), ct.byref(dims),
+                mx.DTYPES[fmt], mx.DTYPES[out_dtype], ct.c_void_p(out.data_ptr()), ct.c_void_p(work.data_ptr()),
+                work.numel(), self.stream())
+        fn = self.lib.mx_block_scaled_dot
+
+        def call():
+            st = fn(*args)
+            if st:
+                raise mx.MxError(st, "mx_block_scaled_dot")
+        call.keep = (dims, lshape, rshape)
+        return call
+
     def fused(self, x, wt, wsf, fmt, out_dtype, c, work):
         mx, ct = self.mx, self.ct
         M, K = x.shape
@@ -359,6 +380,42 @@ class Fused:
         timer.run("fused", self.op)
 
 
+class Dot:
+    """Batched block-scaled dot, 16 x (2048 x 2048 x 2048), e4m3fn -> bf16.
+    Operands: bf16 N(0,1) * 2^U(-8,8) per row, quantized along K (1x32,
+    plain scales) before timing; the [B, K, N] copy of rhs is made once by
+    a device transpose, also before timing."""
+    CASES = ("rhs_bnk", "rhs_bkn")
+
+    def __init__(self, torch, mx, api):
+        B, M, N, K = DOT
+        a_bits, b_bits = syn.gemm_operands(B * M, B * N, K, seed=0)
+        a = dev_bits(torch, a_bits, "bf16")
+        b = dev_bits(torch, b_bits, "bf16")
+        del a_bits, b_bits
+        qa, sa = mx.mx_quantize(a, "e4m3fn", geometry="1x32", dim=-1)
+        qb, sb = mx.mx_quantize(b, "e4m3fn", geometry="1x32", dim=-1)
+        del a, b
+        lhs, ls = qa.view(B, M, K), sa.view(B, M, K // 32)
+        rhs, rs = qb.view(B, N, K), sb.view(B, N, K // 32)
+        rhs_kn = rhs.transpose(1, 2).contiguous()
+        rs_kn = rs.transpose(1, 2).contiguous()
+        self.out = torch.empty((B, M, N), dtype=torch.bfloat16, device="cuda")
+        d_nk = mx.make_dot_dims((0,), (0,), (2,), (2,))
+        d_kn = mx.make_dot_dims((0,), (0,), (2,), (1,))
+        w = max(mx.mx_block_scaled_dot_workspace(lhs.shape, rhs.shape, d_nk),
+                mx.mx_block_scaled_dot_workspace(lhs.shape, rhs_kn.shape, d_kn))
+        self.work = torch.empty(w, dtype=torch.uint8, device="cuda")
+        self.keep = (lhs, ls, rhs, rs, rhs_kn, rs_kn)
+        self.ops = [("dot_rhs_bnk", api.dot(lhs, rhs, ls, rs, d_nk, "e4m3fn", "bf16", self.out, self.work)),
+                    ("dot_rhs_bkn", api.dot(lhs, rhs_kn, ls, rs_kn, d_kn, "e4m3fn", "bf16", self.out, self.work))]
+        self.launches = 3 + 5  # repack x2 + GEMM; permute x2 + repack x2 + GEMM
+
+    def step(self, timer):
+        for label, fn in self.ops:
+            timer.run(label, fn)
+
+
 # ------------------------------------------------------------- CPU oracle
 
 def oracle_sweep_sample(rows=2048, repeats=1):
@@ -469,7 +526,7 @@ def main():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="mx", choices=["mx", "reference"])
-    ap.add_argument("--workload", default="all", choices=["all", "sweep", "gemm", "fp4", "fused", "dequant"])
+    ap.add_argument("--workload", default="all", choices=["all", "sweep", "gemm", "fp4", "fused", "dequant", "dot"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--reference-rows", type=int, default=1024,
                     help="rows of each [rows, 8192] sweep slice the reference arm quantizes per step")
@@ -487,8 +544,8 @@ def main():
 
     peaks = load_peaks()
     parts = {}
-    want = ["sweep", "gemm", "fp4", "dequant", "fused"] if args.workload == "all" else [args.workload]
-    builders = {"sweep": Sweep, "gemm": Gemm, "fp4": Fp4, "dequant": Dequant, "fused": Fused}
+    want = ["sweep", "gemm", "fp4", "dequant", "fused", "dot"] if args.workload == "all" else [args.workload]
+    builders = {"sweep": Sweep, "gemm": Gemm, "fp4": Fp4, "dequant": Dequant, "fused": Fused, "dot": Dot}
     api = Api(torch, mx)
     for name in want:
         parts[name] = builders[name](torch, mx, api)
@@ -596,6 +653,23 @@ def main():
                          "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": round(peak_fp8, 1),
                                       "unit": "TFLOP/s", "frac": round(tf / peak_fp8, 4),
                                       "peak_source": f"{peaks['src']} bf16 burst x {FP8_OVER_BF16}"}}
+
+    if "dot" in parts:
+        peak_fp8 = peaks["bf16"] * FP8_OVER_BF16
+        cases = {}
+        for c in Dot.CASES:
+            ms = timer.avg_ms(f"dot_{c}")
+            cases[c] = {"tflops": round(DOT_FLOP / (ms * 1e-3) / 1e12, 1), "ms": round(ms, 4)}
+        best = cases["rhs_bnk"]["tflops"]
+        line["block_scaled_dot"] = {
+            "value": best, "unit": "TFLOP/s",
+            "config": "16 x 2048^3 e4m3fn -> bf16, batch dim 0, K innermost on lhs; rhs [B,N,K] in place or "
+                      "[B,K,N] via the transposing copy; whole call (permute + repack + GEMM)",
+            "cases": cases,
+            "roofline": {"bound": "tensor", "kernel": "mx_gemm_2sm_kernel", "achieved": best,
+                         "peak": round(peak_fp8, 1), "unit": "TFLOP/s", "frac": round(best / peak_fp8, 4),
+                         "peak_source": f"{peaks['src']} bf16 burst x {FP8_OVER_BF16}",
+                         "note": "achieved over the whole call, repack launches included"}}
 
     # end to end through the public API with host buffers: pinned host input
     # -> device, QuantizeMX, data and scales -> pinned host, every step

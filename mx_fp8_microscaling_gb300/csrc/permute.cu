@@ -7,10 +7,13 @@
 //   rows       the innermost destination axis is contiguous in the source:
 //              each block copies whole rows (16-byte accesses when aligned);
 //              the source offset of a row is found once per row.
-//   transpose  otherwise: 64 x 64 tiles between the destination's innermost
-//              axis and the axis that is contiguous in the source, staged
-//              through shared memory so both the loads and the stores run
-//              along contiguous bytes.
+//   transpose  otherwise: each warp moves a 64 x 32-byte tile between the
+//              axis that is contiguous in the source (i) and the
+//              destination's innermost axis (j).  A lane loads 16 words
+//              (4 bytes of i from 16 rows of j), transposes them in registers
+//              with byte permutes and stores 4 rows of 16 bytes: both sides
+//              touch whole 32-byte sectors, and no shared memory is needed.
+//              Tiles at the edges, or unaligned ones, go byte by byte.
 
 #include <cstdint>
 
@@ -20,7 +23,6 @@ namespace mx {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kTile = 64;
 
 struct Dims {
     int rank;
@@ -58,16 +60,34 @@ __global__ void __launch_bounds__(kThreads) permute_rows(const uint8_t* __restri
     }
 }
 
-// Tiles between destination axes `ai` (contiguous in the source) and the
-// innermost destination axis; every other axis indexes whole tiles.
+// 4 x 4 byte transpose: out[m] byte k = in[k] byte m.
+__device__ __forceinline__ void transpose4x4(const uint32_t (&in)[4], uint32_t (&out)[4]) {
+    const uint32_t lo01 = __byte_perm(in[0], in[1], 0x5140), hi01 = __byte_perm(in[0], in[1], 0x7362);
+    const uint32_t lo23 = __byte_perm(in[2], in[3], 0x5140), hi23 = __byte_perm(in[2], in[3], 0x7362);
+    out[0] = __byte_perm(lo01, lo23, 0x5410);
+    out[1] = __byte_perm(lo01, lo23, 0x7632);
+    out[2] = __byte_perm(hi01, hi23, 0x5410);
+    out[3] = __byte_perm(hi01, hi23, 0x7632);
+}
+
+constexpr int kTileI = 64;  // bytes of the source-contiguous axis per warp tile
+constexpr int kTileJ = 32;  // bytes of the destination-contiguous axis per warp tile
+
+// Warp tiles between destination axis `ai` (contiguous in the source) and
+// the innermost destination axis; every other axis indexes whole tiles.
+// `aligned`: source rows and destination rows allow 4- / 16-byte accesses.
 __global__ void __launch_bounds__(kThreads) permute_transpose(const uint8_t* __restrict__ src,
                                                               uint8_t* __restrict__ dst, Dims d, int ai,
-                                                              int64_t tiles_i, int64_t tiles_j, int64_t units) {
-    __shared__ uint8_t tile[kTile][kTile + 4];
+                                                              int64_t tiles_i, int64_t tiles_j, int64_t units,
+                                                              int aligned) {
     const int aj = d.rank - 1;
     const int64_t ni = d.dst_dims[ai], nj = d.dst_dims[aj];
     const int64_t sj = d.src_stride[aj], di = d.dst_stride[ai];
-    for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
+    const int lane = threadIdx.x & 31;
+    const int bq = lane & 15, half = lane >> 4;
+    const int64_t warps = static_cast<int64_t>(gridDim.x) * (kThreads / 32);
+    for (int64_t u = static_cast<int64_t>(blockIdx.x) * (kThreads / 32) + (threadIdx.x >> 5); u < units;
+         u += warps) {
         int64_t rest = u;
         const int64_t tj = rest % tiles_j;
         rest /= tiles_j;
@@ -83,17 +103,28 @@ __global__ void __launch_bounds__(kThreads) permute_transpose(const uint8_t* __r
             dbase += idx * d.dst_stride[a];
             rest = q;
         }
-        const int64_t i0 = ti * kTile, j0 = tj * kTile;
-        const int col = threadIdx.x % kTile;
-        __syncthreads();  // the previous unit's reads of `tile` are done
-        for (int row = threadIdx.x / kTile; row < kTile; row += kThreads / kTile) {
-            // row: j within the tile; col: i (contiguous in the source)
-            if (i0 + col < ni && j0 + row < nj) tile[row][col] = src[sbase + (i0 + col) + (j0 + row) * sj];
-        }
-        __syncthreads();
-        for (int row = threadIdx.x / kTile; row < kTile; row += kThreads / kTile) {
-            // row: i within the tile; col: j (contiguous in the destination)
-            if (i0 + row < ni && j0 + col < nj) dst[dbase + (i0 + row) * di + (j0 + col)] = tile[col][row];
+        const int64_t i = ti * kTileI + 4 * bq;    // this lane's 4 bytes of i
+        const int64_t j = tj * kTileJ + 16 * half; // this lane's 16 rows of j
+        const bool full = (ti + 1) * kTileI <= ni && (tj + 1) * kTileJ <= nj;
+        if (aligned && full) {
+            const uint8_t* s = src + sbase + i + j * sj;
+            uint32_t w[16];
+#pragma unroll
+            for (int r = 0; r < 16; ++r) w[r] = *reinterpret_cast<const uint32_t*>(s + r * sj);
+            uint32_t o[4][4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const uint32_t in[4] = {w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]};
+                transpose4x4(in, o[k]);
+            }
+            uint8_t* o_row = dst + dbase + i * di + j;
+#pragma unroll
+            for (int m = 0; m < 4; ++m)
+                *reinterpret_cast<uint4*>(o_row + m * di) = make_uint4(o[0][m], o[1][m], o[2][m], o[3][m]);
+        } else {
+            for (int m = 0; m < 4; ++m)
+                for (int r = 0; r < 16; ++r)
+                    if (i + m < ni && j + r < nj) dst[dbase + (i + m) * di + j + r] = src[sbase + (i + m) + (j + r) * sj];
         }
     }
 }
@@ -138,12 +169,18 @@ cudaError_t launch_permute_bytes(const PermuteArgs& a, cudaStream_t stream) {
     for (int i = 0; i < d.rank - 1; ++i)
         if (d.src_stride[i] == 1) ai = i;
     if (ai < 0) return cudaErrorInvalidValue;  // not a permutation of a dense tensor
-    const int64_t tiles_i = (d.dst_dims[ai] + kTile - 1) / kTile;
-    const int64_t tiles_j = (d.dst_dims[d.rank - 1] + kTile - 1) / kTile;
+    const int64_t tiles_i = (d.dst_dims[ai] + kTileI - 1) / kTileI;
+    const int64_t tiles_j = (d.dst_dims[d.rank - 1] + kTileJ - 1) / kTileJ;
     const int64_t units = total / (d.dst_dims[ai] * d.dst_dims[d.rank - 1]) * tiles_i * tiles_j;
-    const int64_t grid = units < cap ? units : cap;
+    // 4-byte source loads along i, 16-byte destination stores along j
+    bool aligned = (reinterpret_cast<uintptr_t>(a.src) & 3u) == 0 && (reinterpret_cast<uintptr_t>(a.dst) & 15u) == 0 &&
+                   d.src_stride[d.rank - 1] % 4 == 0 && d.dst_stride[ai] % 16 == 0;
+    for (int i = 0; i < d.rank - 1; ++i)
+        if (i != ai) aligned = aligned && d.src_stride[i] % 4 == 0 && d.dst_stride[i] % 16 == 0;
+    const int64_t warps = (units + 7) / 8;
+    const int64_t grid = warps < cap ? warps : cap;
     permute_transpose<<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(a.src, a.dst, d, ai, tiles_i, tiles_j,
-                                                                            units);
+                                                                            units, aligned ? 1 : 0);
     return cudaGetLastError();
 }
 

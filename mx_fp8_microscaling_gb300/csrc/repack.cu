@@ -9,9 +9,11 @@
 // ordered row-tile-major: tile (t_mn, t_k) at ((t_mn * ceil(k/128)) + t_k) * 512.
 // Padding rows/columns are written as 0.
 //
-// One thread writes one 32-bit word (the four K-block scales of one row), so
-// stores are fully coalesced; the reads gather four rows 32 apart.  A batch of
-// problems is one launch: their SF layouts are written back to back.
+// A block takes 128 rows x up to 64 scale columns (16 tiles): it reads the
+// rows' contiguous 64-byte segments (16-byte loads where aligned) into shared
+// memory and writes the 16 tiles, which are contiguous in the output, with
+// 16-byte stores.  A batch of problems is one launch: their SF layouts are
+// written back to back.
 
 #include <cstdint>
 
@@ -20,28 +22,52 @@
 namespace mx {
 namespace {
 
-__global__ void __launch_bounds__(256) repack_sf_kernel(const uint8_t* __restrict__ plain, int64_t mn,
-                                                       int64_t kb, int64_t ld, int64_t ntk, int64_t nwords,
-                                                       int64_t plain_batch_stride, int64_t batch,
-                                                       uint32_t* __restrict__ sf) {
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    const int64_t total = nwords * batch;
-    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total; i += stride) {
-        const int64_t b = batch == 1 ? 0 : i / nwords;
-        const int64_t w = i - b * nwords;
+constexpr int kRepackThreads = 256;
+constexpr int kTilesPerBlock = 16;                 // 64 scale columns
+constexpr int kCols = 4 * kTilesPerBlock;
+
+__global__ void __launch_bounds__(kRepackThreads) repack_sf_kernel(const uint8_t* __restrict__ plain, int64_t mn,
+                                                                  int64_t kb, int64_t ld, int64_t ntm, int64_t ntk,
+                                                                  int64_t plain_batch_stride, int64_t batch,
+                                                                  uint8_t* __restrict__ sf, int vec_ok) {
+    __shared__ __align__(16) uint8_t rows[128][kCols + 16];
+    const int64_t nchunk = (ntk + kTilesPerBlock - 1) / kTilesPerBlock;
+    const int64_t units = batch * ntm * nchunk;
+    const int64_t sf_batch_bytes = ntm * ntk * 512;
+    for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
+        const int64_t chunk = u % nchunk;
+        const int64_t tm = (u / nchunk) % ntm;
+        const int64_t b = u / (nchunk * ntm);
         const uint8_t* src = plain + b * plain_batch_stride;
-        const int64_t tile = w >> 7;          // 128 words per 512-byte tile
-        const int within = static_cast<int>(w & 127);
-        const int64_t tm = tile / ntk, tk = tile - (tile / ntk) * ntk;
-        const int64_t r = tm * 128 + (within >> 2) + 32 * (within & 3);
-        const int64_t c0 = tk * 4;
-        uint32_t word = 0;
-        if (r < mn) {
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-                if (c0 + j < kb) word |= static_cast<uint32_t>(src[r * ld + c0 + j]) << (8 * j);
+        const int64_t c0 = chunk * kCols;                  // first scale column
+        const int tiles = static_cast<int>(ntk - chunk * kTilesPerBlock < kTilesPerBlock
+                                               ? ntk - chunk * kTilesPerBlock
+                                               : kTilesPerBlock);
+        __syncthreads();  // the previous unit's reads of `rows` are done
+        // rows tm*128 .. +127, columns c0 .. c0+63 (0 past the matrix)
+        for (int i = threadIdx.x; i < 128 * (kCols / 16); i += kRepackThreads) {
+            const int rr = i / (kCols / 16), seg = i % (kCols / 16);
+            const int64_t r = tm * 128 + rr, c = c0 + 16 * seg;
+            uint8_t* dst = &rows[rr][16 * seg];
+            if (r < mn && c < kb && vec_ok && c + 16 <= kb) {
+                *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src + r * ld + c);
+            } else {
+                for (int j = 0; j < 16; ++j) dst[j] = (r < mn && c + j < kb) ? src[r * ld + c + j] : uint8_t(0);
+            }
         }
-        sf[i] = word;
+        __syncthreads();
+        // tile t, 16-byte group q holds the 4-column words of rows q, q+32,
+        // q+64, q+96
+        uint4* out = reinterpret_cast<uint4*>(sf + b * sf_batch_bytes + (tm * ntk + chunk * kTilesPerBlock) * 512);
+        for (int i = threadIdx.x; i < tiles * 32; i += kRepackThreads) {
+            const int t = i >> 5, q = i & 31;
+            uint4 v;
+            v.x = *reinterpret_cast<const uint32_t*>(&rows[q][4 * t]);
+            v.y = *reinterpret_cast<const uint32_t*>(&rows[q + 32][4 * t]);
+            v.z = *reinterpret_cast<const uint32_t*>(&rows[q + 64][4 * t]);
+            v.w = *reinterpret_cast<const uint32_t*>(&rows[q + 96][4 * t]);
+            out[i] = v;
+        }
     }
 }
 
@@ -56,14 +82,16 @@ cudaError_t launch_repack_scales_batched(const uint8_t* plain, int64_t mn, int64
                                          int64_t plain_batch_stride, int64_t batch, uint8_t* sf,
                                          cudaStream_t stream) {
     const int64_t kb = k / 32;
+    const int64_t ntm = (mn + 127) / 128;
     const int64_t ntk = (kb + 3) / 4;
-    const int64_t nwords = static_cast<int64_t>(sf_layout_bytes(mn, k) / 4);
-    if (nwords == 0 || batch == 0) return cudaSuccess;
-    int64_t blocks = (nwords * batch + 255) / 256;
+    if (ntm == 0 || ntk == 0 || batch == 0) return cudaSuccess;
+    const int64_t units = batch * ntm * ((ntk + kTilesPerBlock - 1) / kTilesPerBlock);
     const int64_t cap = static_cast<int64_t>(device_sm_count()) * 8;
-    if (blocks > cap) blocks = cap;
-    repack_sf_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-        plain, mn, kb, ld_plain, ntk, nwords, plain_batch_stride, batch, reinterpret_cast<uint32_t*>(sf));
+    const int64_t blocks = units < cap ? units : cap;
+    const int vec_ok = (reinterpret_cast<uintptr_t>(plain) & 15u) == 0 && ld_plain % 16 == 0 &&
+                       plain_batch_stride % 16 == 0;
+    repack_sf_kernel<<<static_cast<unsigned>(blocks), kRepackThreads, 0, stream>>>(
+        plain, mn, kb, ld_plain, ntm, ntk, plain_batch_stride, batch, sf, vec_ok);
     return cudaGetLastError();
 }
 
