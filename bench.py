@@ -13,6 +13,8 @@ A step is one pass of the whole hot path over its synthetic inputs:
   dequant  MX dequantize of [8192, 8192] e4m3fn codes with 8x4 scales to bf16;
   fused  activation quantize + ScaledMatmul, X [16384, 8192] bf16 times a
          pre-quantized e4m3fn weight W [8192, 28672] -> bf16;
+  gemm_fp4  MXFP4 ScaledMatmul 8192^3 (e2m1 operands quantized along K in
+         the tensor-core nibble order, repacked scales) -> bf16;
   dot    batched block-scaled dot, 16 problems of 2048^3 e4m3fn -> bf16:
          rhs stored [B, N, K] (read in place) and [B, K, N] (through the
          transposing copy), one call each.
@@ -57,8 +59,9 @@ FUSED = (16384, 28672, 8192)
 FUSED_FLOP = 2 * FUSED[0] * FUSED[1] * FUSED[2]
 DOT = (16, 2048, 2048, 2048)  # batch, M, N, K
 DOT_FLOP = 2 * DOT[0] * DOT[1] * DOT[2] * DOT[3]
-# nominal dense MXFP8 : bf16 tensor ratio (4.5 : 2.25 PFLOP/s)
+# nominal dense MXFP8 : bf16 and FP4 : bf16 tensor ratios (4.5 and 13.5 : 2.25 PFLOP/s)
 FP8_OVER_BF16 = 2.0
+FP4_OVER_BF16 = 6.0
 
 
 def load_peaks():
@@ -182,10 +185,10 @@ class Api:
     def stream(self):
         return self.ct.c_void_p(self.torch.cuda.current_stream().cuda_stream)
 
-    def quantize(self, x, fmt, geometry, dim, layout, data, scale):
+    def quantize(self, x, fmt, geometry, dim, layout, data, scale, **cfg_kw):
         mx, ct = self.mx, self.ct
         rows, cols, ld = mx._view2d(x, dim)
-        cfg = mx.make_cfg(geometry, dim, layout)
+        cfg = mx.make_cfg(geometry, dim, layout, **cfg_kw)
         args = (ct.c_void_p(x.data_ptr()), mx.DTYPES[mx._in_dtype(x)], rows, cols, ld, mx.DTYPES[fmt],
                 ct.byref(cfg), ct.c_void_p(data.data_ptr()), ct.c_void_p(scale.data_ptr()), self.stream())
         fn = self.lib.mx_quantize
@@ -380,6 +383,39 @@ class Fused:
         timer.run("fused", self.op)
 
 
+class GemmFp4:
+    """MXFP4 ScaledMatmul 8192^3 -> bf16: quantize A and Bt to e2m1 (1x32
+    along K, element 2i in the low nibble), repack both scale tensors, GEMM."""
+
+    def __init__(self, torch, mx, api):
+        n = GEMM_N
+        a_bits, b_bits = syn.gemm_operands(n, n, n, seed=0)
+        self.a = dev_bits(torch, a_bits, "bf16")
+        self.b = dev_bits(torch, b_bits, "bf16")
+        del a_bits, b_bits
+        self.qa = torch.empty(n * n // 2, dtype=torch.uint8, device="cuda")
+        self.qb = torch.empty(n * n // 2, dtype=torch.uint8, device="cuda")
+        self.sa = torch.empty(n * n // 32, dtype=torch.uint8, device="cuda")
+        self.sb = torch.empty(n * n // 32, dtype=torch.uint8, device="cuda")
+        sfb = mx.mx_sf_layout_bytes(n, n)
+        self.sfa = torch.empty(sfb, dtype=torch.uint8, device="cuda")
+        self.sfb = torch.empty(sfb, dtype=torch.uint8, device="cuda")
+        self.c = torch.empty((n, n), dtype=torch.bfloat16, device="cuda")
+        self.ops = [("fp4_quantize_operands", api.quantize(self.a, "e2m1", "1x32", -1, "plain", self.qa, self.sa,
+                                                          fp4_lane_stride=1, fp4_nibble_parity=1)),
+                    ("fp4_quantize_operands", api.quantize(self.b, "e2m1", "1x32", -1, "plain", self.qb, self.sb,
+                                                          fp4_lane_stride=1, fp4_nibble_parity=1)),
+                    ("fp4_repack", api.repack(self.sa.view(n, n // 32), n, self.sfa)),
+                    ("fp4_repack", api.repack(self.sb.view(n, n // 32), n, self.sfb)),
+                    ("gemm_fp4", api.matmul_sf(self.qa.view(n, n // 2), self.qb.view(n, n // 2), self.sfa, self.sfb,
+                                               "e2m1", "bf16", self.c, n))]
+        self.launches = 5
+
+    def step(self, timer):
+        for label, fn in self.ops:
+            timer.run(label, fn)
+
+
 class Dot:
     """Batched block-scaled dot, 16 x (2048 x 2048 x 2048), e4m3fn -> bf16.
     Operands: bf16 N(0,1) * 2^U(-8,8) per row, quantized along K (1x32,
@@ -526,7 +562,8 @@ def main():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="mx", choices=["mx", "reference"])
-    ap.add_argument("--workload", default="all", choices=["all", "sweep", "gemm", "fp4", "fused", "dequant", "dot"])
+    ap.add_argument("--workload", default="all",
+                    choices=["all", "sweep", "gemm", "fp4", "fused", "dequant", "dot", "gemm_fp4"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--reference-rows", type=int, default=1024,
                     help="rows of each [rows, 8192] sweep slice the reference arm quantizes per step")
@@ -544,8 +581,10 @@ def main():
 
     peaks = load_peaks()
     parts = {}
-    want = ["sweep", "gemm", "fp4", "dequant", "fused", "dot"] if args.workload == "all" else [args.workload]
-    builders = {"sweep": Sweep, "gemm": Gemm, "fp4": Fp4, "dequant": Dequant, "fused": Fused, "dot": Dot}
+    want = (["sweep", "gemm", "fp4", "dequant", "fused", "dot", "gemm_fp4"] if args.workload == "all"
+            else [args.workload])
+    builders = {"sweep": Sweep, "gemm": Gemm, "fp4": Fp4, "dequant": Dequant, "fused": Fused, "dot": Dot,
+                "gemm_fp4": GemmFp4}
     api = Api(torch, mx)
     for name in want:
         parts[name] = builders[name](torch, mx, api)
@@ -654,6 +693,19 @@ def main():
                                       "unit": "TFLOP/s", "frac": round(tf / peak_fp8, 4),
                                       "peak_source": f"{peaks['src']} bf16 burst x {FP8_OVER_BF16}"}}
 
+    if "gemm_fp4" in parts:
+        ms = timer.avg_ms("gemm_fp4")
+        tf = GEMM_FLOP / (ms * 1e-3) / 1e12
+        peak_fp4 = peaks["bf16"] * FP4_OVER_BF16
+        pipe_ms = (timer.totals["fp4_quantize_operands"] + timer.totals["fp4_repack"]
+                   + timer.totals["gemm_fp4"]) / timer.counts["gemm_fp4"]
+        line["scaled_matmul_fp4"] = {
+            "value": round(tf, 1), "unit": "TFLOP/s", "ms": round(ms, 4),
+            "config": "M=N=K=8192 e2m1 x e2m1 (kind::mxf4), E8M0 per 32 along K -> bf16",
+            "pipeline_tflops_incl_quantize_repack": round(GEMM_FLOP / (pipe_ms * 1e-3) / 1e12, 1),
+            "roofline": {"bound": "tensor", "kernel": "mx_gemm_2sm_kernel<true>", "achieved": round(tf, 1),
+                         "peak": round(peak_fp4, 1), "unit": "TFLOP/s", "frac": round(tf / peak_fp4, 4),
+                         "peak_source": f"{peaks['src']} bf16 burst x {FP4_OVER_BF16} (nominal FP4/bf16)"}}
     if "dot" in parts:
         peak_fp8 = peaks["bf16"] * FP8_OVER_BF16
         cases = {}

@@ -218,13 +218,17 @@ mx_status mx_scaled_matmul_workspace(int64_t M, int64_t N, int64_t K, int scales
  *
  * accumulated in f32 on the tensor cores, written as f32 or bf16
  * (round to nearest even).
- *   a, bt        device FP8 codes, A [M, K] and Bt [N, K] (= rhs^T), dense,
- *                16-byte aligned; both of `elem_dtype`
+ *   a, bt        device codes, A [M, K] and Bt [N, K] (= rhs^T), dense,
+ *                16-byte aligned; both of `elem_dtype`.  MX_E2M1 operands
+ *                are packed two a byte, element 2i in the low nibble
+ *                (mx_quantize with fp4_lane_stride 1, fp4_nibble_parity 1):
+ *                rows of K/2 bytes
  *   a_scale,     device E8M0: plain [M, K/32] / [N, K/32] dense row-major
  *   b_scale      (scales_are_sf_layout = 0), or already in the SF layout of
  *                mx_repack_scales (scales_are_sf_layout = 1)
  *   elem_dtype   MX_E4M3FN | MX_E5M2 (ScaledMatmul_e4m3fn_e4m3fn_* /
- *                ScaledMatmul_e5m2_e5m2_*)
+ *                ScaledMatmul_e5m2_e5m2_*) | MX_E2M1 (MXFP4: an extension;
+ *                the pages' ScaledMatmul takes FP8 only)
  *   M, N, K      M, N >= 1; K >= 32 and K % 32 == 0
  *   out_dtype    MX_F32 | MX_BF16
  *   c, ldc       device [M, ldc] output, ldc >= N, element aligned (16-byte
@@ -279,7 +283,9 @@ mx_status mx_fused_quantize_matmul_workspace(int64_t M, int64_t N, int64_t K, si
  * Wt [N, K] with SF-layout scales.  The result equals QuantizeMX(X) followed
  * by mx_scaled_matmul bit for bit in the quantized operand.
  *   x, x_dtype   device [M, ld_x] MX_BF16 | MX_F16
- *   wt, w_scale_sf  device FP8 [N, K] and SF-layout scales (mx_repack_scales)
+ *   wt, w_scale_sf  device codes [N, K] and SF-layout scales (mx_repack_scales);
+ *                for MX_E2M1 X is packed in the tensor-core nibble order
+ *                (element 2i low) and so must Wt be
  *   other arguments as mx_scaled_matmul; workspace per
  *   mx_fused_quantize_matmul_workspace.
  */
@@ -332,7 +338,9 @@ mx_status mx_block_scaled_dot_workspace(const int64_t* lhs_dims, int lhs_rank, c
  *               contracting one divided by 32 (what mx_quantize writes for
  *               1x32 blocks along that axis, plain layout)
  *   dims        dot dimension numbers
- *   elem_dtype  MX_E4M3FN | MX_E5M2 (both operands)
+ *   elem_dtype  MX_E4M3FN | MX_E5M2 | MX_E2M1 (both operands; e2m1 packed
+ *               as for mx_scaled_matmul, which needs the contracting axis
+ *               innermost in both operands, else MX_ERR_UNSUPPORTED_DTYPE)
  *   out_dtype   MX_F32 | MX_BF16 (round to nearest even); `out` is dense in
  *               the order of mx_block_scaled_dot_shape, caller-owned
  *   workspace   device, 16-byte aligned, mx_block_scaled_dot_workspace bytes

@@ -234,10 +234,11 @@ def mx_scaled_matmul(a: torch.Tensor, bt: torch.Tensor, a_scale: torch.Tensor, b
                      elem_dtype: str = "e4m3fn", out_dtype: str = "f32", *, scales_are_sf_layout: bool = False,
                      out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
                      K: int | None = None, stream=None) -> torch.Tensor:
-    """C = ScaledMatmul(A [M,K], Bt [N,K]) with E8M0 scales, f32 or bf16 out."""
+    """C = ScaledMatmul(A [M,K], Bt [N,K]) with E8M0 scales, f32 or bf16 out.
+    e2m1 operands are packed two a byte ([M, K/2] bytes)."""
     M, Kb = a.shape
     N = bt.shape[0]
-    K = Kb if K is None else K
+    K = (2 * Kb if elem_dtype == "e2m1" else Kb) if K is None else K
     if out is None:
         out = torch.empty((M, N), dtype=torch.float32 if out_dtype == "f32" else torch.bfloat16, device=a.device)
     ws_bytes = mx_scaled_matmul_workspace(M, N, K, scales_are_sf_layout)
@@ -259,7 +260,7 @@ def mx_scaled_matmul_noalloc(a: torch.Tensor, bt: torch.Tensor, a_scale: torch.T
     include/mx.h).  The output tensor is still the caller's."""
     M, Kb = a.shape
     N = bt.shape[0]
-    K = Kb if K is None else K
+    K = (2 * Kb if elem_dtype == "e2m1" else Kb) if K is None else K
     if out is None:
         out = torch.empty((M, N), dtype=torch.float32 if out_dtype == "f32" else torch.bfloat16, device=a.device)
     _check(_lib.mx_scaled_matmul_noalloc(_dev_ptr(a), _dev_ptr(bt), _dev_ptr(a_scale), _dev_ptr(b_scale),
@@ -308,19 +309,23 @@ def mx_block_scaled_dot(lhs: torch.Tensor, rhs: torch.Tensor, lhs_scale: torch.T
                         lhs_contract=(-1,), rhs_contract=(-1,), out: torch.Tensor | None = None,
                         workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """block_scaled_dot with dot dimension numbers; operands are dense uint8
-    code tensors, scales their shape with the contracting extent / 32."""
+    code tensors, scales their shape with the contracting extent / 32.  e2m1
+    operands are packed two a byte along their last (contracting) axis."""
     for t in (lhs, rhs, lhs_scale, rhs_scale):
         if not t.is_contiguous():
             raise ValueError("mx_block_scaled_dot takes dense (contiguous) tensors")
     dims = make_dot_dims(lhs_batch, rhs_batch, lhs_contract, rhs_contract)
-    shape = mx_block_scaled_dot_shape(lhs.shape, rhs.shape, dims)
+    lshape, rshape = tuple(lhs.shape), tuple(rhs.shape)
+    if elem_dtype == "e2m1":  # logical extents: two elements a byte along the last axis
+        lshape, rshape = lshape[:-1] + (2 * lshape[-1],), rshape[:-1] + (2 * rshape[-1],)
+    shape = mx_block_scaled_dot_shape(lshape, rshape, dims)
     if out is None:
         out = torch.empty(shape, dtype=torch.float32 if out_dtype == "f32" else torch.bfloat16, device=lhs.device)
-    ws_bytes = mx_block_scaled_dot_workspace(lhs.shape, rhs.shape, dims)
+    ws_bytes = mx_block_scaled_dot_workspace(lshape, rshape, dims)
     if workspace is None and ws_bytes:
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=lhs.device)
-    _check(_lib.mx_block_scaled_dot(_dev_ptr(lhs), _dims_array(lhs.shape), lhs.dim(), _dev_ptr(lhs_scale),
-                                    _dev_ptr(rhs), _dims_array(rhs.shape), rhs.dim(), _dev_ptr(rhs_scale),
+    _check(_lib.mx_block_scaled_dot(_dev_ptr(lhs), _dims_array(lshape), lhs.dim(), _dev_ptr(lhs_scale),
+                                    _dev_ptr(rhs), _dims_array(rshape), rhs.dim(), _dev_ptr(rhs_scale),
                                     ctypes.byref(dims), DTYPES[elem_dtype], DTYPES[out_dtype], _dev_ptr(out),
                                     _dev_ptr(workspace), workspace.numel() if workspace is not None else 0,
                                     _stream(stream)),

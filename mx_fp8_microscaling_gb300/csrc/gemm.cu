@@ -26,6 +26,10 @@
 //               convert (f32, or bf16 round-to-nearest-even) and store rows to
 //               global memory while the next tile's main loop runs.
 //
+// Both kernels also run MXFP4 (packed e2m1 operands, kind::mxf4 with
+// scale_vec::2X, K = 64 per MMA): a 128-byte stage row then holds 256 K
+// elements and two scale tiles along K.
+//
 //   mx_gemm_kernel      1 SM per 128 x 256 tile (M = 128 MMA), 4 stages of
 //                       A 16 KB + B 32 KB + scales 1.5 KB.  Used for M <= 128.
 //   mx_gemm_2sm_kernel  a cluster of 2 CTAs per 256 x 256 tile with the pair
@@ -69,6 +73,8 @@ constexpr int NUM_EPI_WARPS = 8;
 constexpr int NUM_THREADS = 64 + NUM_EPI_WARPS * 32;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TMEM_SF = 256;
+// scale-factor columns per stage: FP8 A 4 + B 8; FP4 (two K groups) A 8 + B 16
+__host__ __device__ constexpr uint32_t sf_cols(bool fp4) { return fp4 ? 32u : 16u; }
 
 struct KParams {
     const uint8_t* sfa;
@@ -78,7 +84,8 @@ struct KParams {
     int M, N, K;
     int out_bf16;
     int vec_store;       // 16-byte row stores allowed (aligned c and pitch)
-    int num_m_tiles, num_n_tiles, num_kb;
+    int num_m_tiles, num_n_tiles, num_kb;  // num_kb: K stages (128 FP8 or 256 FP4 elements each)
+    int sf_ntk;          // 512-byte scale tiles along K per 128 rows (one per 128 elements)
     int num_sf_n_tiles;  // 128-row scale tiles of B
     int batch;           // independent problems; tiles run batch-major
     int64_t c_batch_stride;   // elements between consecutive C matrices
@@ -166,26 +173,30 @@ constexpr int BM = 128, BN = 256;
 constexpr int STAGES = 4;
 constexpr uint32_t A_STAGE = BM * BK;   // 16 KB
 constexpr uint32_t B_STAGE = BN * BK;   // 32 KB
-constexpr uint32_t SFA_STAGE = 512;
-constexpr uint32_t SFB_STAGE = 1024;
 constexpr uint32_t OFF_A = 0;
 constexpr uint32_t OFF_B = OFF_A + STAGES * A_STAGE;
 constexpr uint32_t OFF_SFA = OFF_B + STAGES * B_STAGE;
-constexpr uint32_t OFF_SFB = OFF_SFA + STAGES * SFA_STAGE;
-constexpr uint32_t OFF_BAR = OFF_SFB + STAGES * SFB_STAGE;
+// scale tiles per stage: one 512-byte tile per 128 rows per 128 K elements
+// (FP8 stages span 128 K elements, FP4 stages 256)
+__host__ __device__ constexpr uint32_t sfa_stage(bool fp4) { return fp4 ? 1024u : 512u; }
+__host__ __device__ constexpr uint32_t sfb_stage(bool fp4) { return 2 * sfa_stage(fp4); }
+__host__ __device__ constexpr uint32_t off_sfb(bool fp4) { return OFF_SFA + STAGES * sfa_stage(fp4); }
+__host__ __device__ constexpr uint32_t off_bar(bool fp4) { return off_sfb(fp4) + STAGES * sfb_stage(fp4); }
 constexpr int NUM_BARS = 3 * STAGES + 4;  // full, empty, sf_full [S]; tmem_full, tmem_empty, mma_done, sf_done
-constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
-constexpr uint32_t SMEM_BYTES = OFF_MISC + 16;
-constexpr uint32_t SMEM_ALLOC = SMEM_BYTES + 1024;  // slack to align the base to 1024
-constexpr uint32_t STAGE_TX = A_STAGE + B_STAGE + SFA_STAGE + SFB_STAGE;
+__host__ __device__ constexpr uint32_t off_misc(bool fp4) { return off_bar(fp4) + NUM_BARS * 8; }
+__host__ __device__ constexpr uint32_t smem_alloc(bool fp4) { return off_misc(fp4) + 16 + 1024; }  // slack to align the base
 constexpr int SF_WARP = 10;              // warp that copies scale factors to tensor memory
 constexpr int THREADS = NUM_THREADS + 32;
 }  // namespace sm1
 
+template <bool FP4>
 __global__ void __launch_bounds__(sm1::THREADS, 1)
     mx_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                    const KParams p) {
     using namespace sm1;
+    constexpr uint32_t SFA_STAGE = sfa_stage(FP4), SFB_STAGE = sfb_stage(FP4);
+    constexpr uint32_t OFF_SFB = off_sfb(FP4), OFF_BAR = off_bar(FP4), OFF_MISC = off_misc(FP4);
+    constexpr uint32_t SF_COLS = sf_cols(FP4);
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sb = smem_u32(smem);
@@ -244,15 +255,19 @@ __global__ void __launch_bounds__(sm1::THREADS, 1)
                         break;
                     }
                     const uint32_t fb = full_bar(stage);
-                    mbar_arrive_expect_tx(fb, STAGE_TX);
+                    // first scale tile of the stage along K; an FP4 stage takes
+                    // two unless K ends inside it
+                    const int t0 = FP4 ? 2 * kb : kb;
+                    const uint32_t sf_bytes = (FP4 && t0 + 1 < p.sf_ntk) ? 1024u : 512u;
+                    mbar_arrive_expect_tx(fb, A_STAGE + B_STAGE + 3u * sf_bytes);
                     tma_load_3d(sb + OFF_A + stage * A_STAGE, &tmap_a, fb, kb * BK, mt * BM, b);
                     tma_load_3d(sb + OFF_B + stage * B_STAGE, &tmap_b, fb, kb * BK, nt * BN, b);
                     bulk_load(sb + OFF_SFA + stage * SFA_STAGE,
-                              sfa + (static_cast<size_t>(mt) * p.num_kb + kb) * 512u, 512u, fb);
+                              sfa + (static_cast<size_t>(mt) * p.sf_ntk + t0) * 512u, sf_bytes, fb);
                     bulk_load(sb + OFF_SFB + stage * SFB_STAGE,
-                              sfb + (static_cast<size_t>(nsf0) * p.num_kb + kb) * 512u, 512u, fb);
-                    bulk_load(sb + OFF_SFB + stage * SFB_STAGE + 512u,
-                              sfb + (static_cast<size_t>(nsf1) * p.num_kb + kb) * 512u, 512u, fb);
+                              sfb + (static_cast<size_t>(nsf0) * p.sf_ntk + t0) * 512u, sf_bytes, fb);
+                    bulk_load(sb + OFF_SFB + stage * SFB_STAGE + SFB_STAGE / 2,
+                              sfb + (static_cast<size_t>(nsf1) * p.sf_ntk + t0) * 512u, sf_bytes, fb);
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
@@ -285,16 +300,29 @@ __global__ void __launch_bounds__(sm1::THREADS, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t sfa_t = tmem_base + TMEM_SF + 16u * stage;
-                    const uint32_t sfb_t = sfa_t + 4u;
+                    const uint32_t sf_t = tmem_base + TMEM_SF + SF_COLS * stage;
                     const uint32_t sa = sb + OFF_A + stage * A_STAGE;
                     const uint32_t sbb = sb + OFF_B + stage * B_STAGE;
+                    if constexpr (FP4) {
+                        // 4 MMAs of K = 64; K group g = kk / 2 has its own scale
+                        // columns, bytes {0,1} / {2,3} of them by scale data ID
+                        const int kk_end = (kb * 256 + 128 < p.K) ? 4 : 2;
 #pragma unroll
-                    for (int kk = 0; kk < BK / 32; ++kk) {
-                        const uint32_t idesc = p.idesc | (static_cast<uint32_t>(kk) << 4) |
-                                               (static_cast<uint32_t>(kk) << 29);
-                        tc_mma_mxf8(tmem_base, sdesc_kmajor_sw128(sa + kk * 32), sdesc_kmajor_sw128(sbb + kk * 32),
-                                    idesc, sfa_t, sfb_t, (kb | kk) != 0);
+                        for (int kk = 0; kk < 4; ++kk) {
+                            if (kk >= kk_end) break;
+                            const uint32_t id = 2u * static_cast<uint32_t>(kk & 1);
+                            tc_mma_mxf4(tmem_base, sdesc_kmajor_sw128(sa + kk * 32),
+                                        sdesc_kmajor_sw128(sbb + kk * 32), p.idesc | (id << 4) | (id << 29),
+                                        sf_t + 4u * (kk >> 1), sf_t + 8u + 8u * (kk >> 1), (kb | kk) != 0);
+                        }
+                    } else {
+#pragma unroll
+                        for (int kk = 0; kk < BK / 32; ++kk) {
+                            const uint32_t idesc = p.idesc | (static_cast<uint32_t>(kk) << 4) |
+                                                   (static_cast<uint32_t>(kk) << 29);
+                            tc_mma_mxf8(tmem_base, sdesc_kmajor_sw128(sa + kk * 32),
+                                        sdesc_kmajor_sw128(sbb + kk * 32), idesc, sf_t, sf_t + 4u, (kb | kk) != 0);
+                        }
                     }
                     tc_commit(empty_bar(stage));
                     if (++stage == STAGES) {
@@ -324,12 +352,23 @@ __global__ void __launch_bounds__(sm1::THREADS, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t sfa_t = tmem_base + TMEM_SF + 16u * stage;
+                    const uint32_t sf_t = tmem_base + TMEM_SF + SF_COLS * stage;
                     const uint32_t s_sfa = sb + OFF_SFA + stage * SFA_STAGE;
                     const uint32_t s_sfb = sb + OFF_SFB + stage * SFB_STAGE;
-                    tc_cp_32x128b_warpx4(sfa_t, sdesc_sf_tile(s_sfa));
-                    tc_cp_32x128b_warpx4(sfa_t + 4u, sdesc_sf_tile(s_sfb));
-                    tc_cp_32x128b_warpx4(sfa_t + 8u, sdesc_sf_tile(s_sfb + 512u));
+                    if constexpr (FP4) {
+                        // A: K groups at +0, +4; B: K group g at +8 + 8g (rows
+                        // 0-127, then 128-255 four columns on)
+                        tc_cp_32x128b_warpx4(sf_t, sdesc_sf_tile(s_sfa));
+                        tc_cp_32x128b_warpx4(sf_t + 4u, sdesc_sf_tile(s_sfa + 512u));
+                        tc_cp_32x128b_warpx4(sf_t + 8u, sdesc_sf_tile(s_sfb));
+                        tc_cp_32x128b_warpx4(sf_t + 12u, sdesc_sf_tile(s_sfb + 1024u));
+                        tc_cp_32x128b_warpx4(sf_t + 16u, sdesc_sf_tile(s_sfb + 512u));
+                        tc_cp_32x128b_warpx4(sf_t + 20u, sdesc_sf_tile(s_sfb + 1536u));
+                    } else {
+                        tc_cp_32x128b_warpx4(sf_t, sdesc_sf_tile(s_sfa));
+                        tc_cp_32x128b_warpx4(sf_t + 4u, sdesc_sf_tile(s_sfb));
+                        tc_cp_32x128b_warpx4(sf_t + 8u, sdesc_sf_tile(s_sfb + 512u));
+                    }
                     tc_commit(sf_full_bar(stage));
                     if (++stage == STAGES) {
                         stage = 0;
@@ -380,30 +419,34 @@ constexpr int BM = 256, BN = 256;        // pair tile; each CTA holds 128 rows o
 constexpr int STAGES = 6;
 constexpr uint32_t A_STAGE = 128 * BK;   // 16 KB
 constexpr uint32_t B_STAGE = 128 * BK;   // 16 KB
-constexpr uint32_t SFA_STAGE = 512;      // this CTA's 128 rows of A
-constexpr uint32_t SFB_STAGE = 1024;     // all 256 rows of B (both CTAs need them)
 constexpr uint32_t OFF_A = 0;
 constexpr uint32_t OFF_B = OFF_A + STAGES * A_STAGE;
 constexpr uint32_t OFF_SFA = OFF_B + STAGES * B_STAGE;
-constexpr uint32_t OFF_SFB = OFF_SFA + STAGES * SFA_STAGE;
-constexpr uint32_t OFF_BAR = OFF_SFB + STAGES * SFB_STAGE;
+// this CTA's 128 rows of A; all 256 rows of B (both CTAs need them)
+__host__ __device__ constexpr uint32_t sfa_stage(bool fp4) { return fp4 ? 1024u : 512u; }
+__host__ __device__ constexpr uint32_t sfb_stage(bool fp4) { return 2 * sfa_stage(fp4); }
+__host__ __device__ constexpr uint32_t off_sfb(bool fp4) { return OFF_SFA + STAGES * sfa_stage(fp4); }
+__host__ __device__ constexpr uint32_t off_bar(bool fp4) { return off_sfb(fp4) + STAGES * sfb_stage(fp4); }
 constexpr int NUM_BARS = 3 * STAGES + 4;  // full, empty, sf_full [S]; tmem_full, tmem_empty, mma_done, sf_done
-constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
-constexpr uint32_t SMEM_BYTES = OFF_MISC + 16;
-constexpr uint32_t SMEM_ALLOC = SMEM_BYTES + 1024;
-constexpr uint32_t CTA_TX = A_STAGE + B_STAGE + SFA_STAGE + SFB_STAGE;
-constexpr uint32_t PAIR_TX = 2 * CTA_TX;
+__host__ __device__ constexpr uint32_t off_misc(bool fp4) { return off_bar(fp4) + NUM_BARS * 8; }
+__host__ __device__ constexpr uint32_t smem_alloc(bool fp4) { return off_misc(fp4) + 16 + 1024; }
+__host__ __device__ constexpr uint32_t pair_tx(bool fp4) { return 2 * (A_STAGE + B_STAGE + sfa_stage(fp4) + sfb_stage(fp4)); }
 constexpr int SF_WARP = 10;              // warp that copies scale factors to tensor memory
 constexpr int THREADS = NUM_THREADS + 32;
 }  // namespace sm2
 
 // Scale-factor buffers are read by TMA as [2 * tiles, 256] bytes: a 512-byte
 // tile t is rows 2t and 2t+1 (box 256 x 2); tiles past the end read as zeros.
+template <bool FP4>
 __global__ void __launch_bounds__(sm2::THREADS, 1)
     mx_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                        const __grid_constant__ CUtensorMap tmap_sfa, const __grid_constant__ CUtensorMap tmap_sfb,
                        const KParams p) {
     using namespace sm2;
+    constexpr uint32_t SFA_STAGE = sfa_stage(FP4), SFB_STAGE = sfb_stage(FP4);
+    constexpr uint32_t OFF_SFB = off_sfb(FP4), OFF_BAR = off_bar(FP4), OFF_MISC = off_misc(FP4);
+    constexpr uint32_t SF_COLS = sf_cols(FP4);
+    constexpr uint32_t PAIR_TX = pair_tx(FP4);
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sb = smem_u32(smem);
@@ -462,9 +505,9 @@ __global__ void __launch_bounds__(sm2::THREADS, 1)
                 // scale tiles past this problem's last one belong to rows past
                 // M / N (the next problem's tiles, or zeros past the buffer):
                 // their products land in rows the epilogue never stores
-                const int64_t sfa_tile = b * p.sfa_batch_tiles + (2 * mt + static_cast<int>(rank)) * p.num_kb;
-                const int64_t sfb_tile0 = b * p.sfb_batch_tiles + (2 * nt) * p.num_kb;
-                const int64_t sfb_tile1 = sfb_tile0 + p.num_kb;
+                const int64_t sfa_tile = b * p.sfa_batch_tiles + (2 * mt + static_cast<int>(rank)) * p.sf_ntk;
+                const int64_t sfb_tile0 = b * p.sfb_batch_tiles + (2 * nt) * p.sf_ntk;
+                const int64_t sfb_tile1 = sfb_tile0 + p.sf_ntk;
                 for (int kb = 0; kb < p.num_kb; ++kb) {
                     if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, p.timeout_ns, &g_mx_status)) {
                         ok = false;
@@ -474,12 +517,15 @@ __global__ void __launch_bounds__(sm2::THREADS, 1)
                     if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), PAIR_TX);
                     tma_load_3d_pair(sb + OFF_A + stage * A_STAGE, &tmap_a, fb, kb * BK, a_row, b);
                     tma_load_3d_pair(sb + OFF_B + stage * B_STAGE, &tmap_b, fb, kb * BK, b_row, b);
+                    // an FP4 stage's box covers two scale tiles along K; a
+                    // tile past K (or past the buffer) feeds no MMA
+                    const int t0 = FP4 ? 2 * kb : kb;
                     tma_load_2d_pair(sb + OFF_SFA + stage * SFA_STAGE, &tmap_sfa, fb, 0,
-                                     static_cast<int>(2 * (sfa_tile + kb)));
+                                     static_cast<int>(2 * (sfa_tile + t0)));
                     tma_load_2d_pair(sb + OFF_SFB + stage * SFB_STAGE, &tmap_sfb, fb, 0,
-                                     static_cast<int>(2 * (sfb_tile0 + kb)));
-                    tma_load_2d_pair(sb + OFF_SFB + stage * SFB_STAGE + 512u, &tmap_sfb, fb, 0,
-                                     static_cast<int>(2 * (sfb_tile1 + kb)));
+                                     static_cast<int>(2 * (sfb_tile0 + t0)));
+                    tma_load_2d_pair(sb + OFF_SFB + stage * SFB_STAGE + SFB_STAGE / 2, &tmap_sfb, fb, 0,
+                                     static_cast<int>(2 * (sfb_tile1 + t0)));
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
@@ -515,16 +561,28 @@ __global__ void __launch_bounds__(sm2::THREADS, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t sfa_t = tmem_base + TMEM_SF + 16u * stage;
-                    const uint32_t sfb_t = sfa_t + 4u;
+                    const uint32_t sf_t = tmem_base + TMEM_SF + SF_COLS * stage;
                     const uint32_t sa = sb + OFF_A + stage * A_STAGE;
                     const uint32_t sbb = sb + OFF_B + stage * B_STAGE;
+                    if constexpr (FP4) {
+                        const int kk_end = (kb * 256 + 128 < p.K) ? 4 : 2;
 #pragma unroll
-                    for (int kk = 0; kk < BK / 32; ++kk) {
-                        const uint32_t idesc = p.idesc | (static_cast<uint32_t>(kk) << 4) |
-                                               (static_cast<uint32_t>(kk) << 29);
-                        tc_mma_mxf8_pair(tmem_base, sdesc_kmajor_sw128(sa + kk * 32),
-                                         sdesc_kmajor_sw128(sbb + kk * 32), idesc, sfa_t, sfb_t, (kb | kk) != 0);
+                        for (int kk = 0; kk < 4; ++kk) {
+                            if (kk >= kk_end) break;
+                            const uint32_t id = 2u * static_cast<uint32_t>(kk & 1);
+                            tc_mma_mxf4_pair(tmem_base, sdesc_kmajor_sw128(sa + kk * 32),
+                                             sdesc_kmajor_sw128(sbb + kk * 32), p.idesc | (id << 4) | (id << 29),
+                                             sf_t + 4u * (kk >> 1), sf_t + 8u + 8u * (kk >> 1), (kb | kk) != 0);
+                        }
+                    } else {
+#pragma unroll
+                        for (int kk = 0; kk < BK / 32; ++kk) {
+                            const uint32_t idesc = p.idesc | (static_cast<uint32_t>(kk) << 4) |
+                                                   (static_cast<uint32_t>(kk) << 29);
+                            tc_mma_mxf8_pair(tmem_base, sdesc_kmajor_sw128(sa + kk * 32),
+                                             sdesc_kmajor_sw128(sbb + kk * 32), idesc, sf_t, sf_t + 4u,
+                                             (kb | kk) != 0);
+                        }
                     }
                     tc_commit_pair_mc(empty_bar(stage), 3);
                     if (++stage == STAGES) {
@@ -555,12 +613,21 @@ __global__ void __launch_bounds__(sm2::THREADS, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t sfa_t = tmem_base + TMEM_SF + 16u * stage;
+                    const uint32_t sf_t = tmem_base + TMEM_SF + SF_COLS * stage;
                     const uint32_t s_sfa = sb + OFF_SFA + stage * SFA_STAGE;
                     const uint32_t s_sfb = sb + OFF_SFB + stage * SFB_STAGE;
-                    tc_cp_pair_32x128b_warpx4(sfa_t, sdesc_sf_tile(s_sfa));
-                    tc_cp_pair_32x128b_warpx4(sfa_t + 4u, sdesc_sf_tile(s_sfb));
-                    tc_cp_pair_32x128b_warpx4(sfa_t + 8u, sdesc_sf_tile(s_sfb + 512u));
+                    if constexpr (FP4) {
+                        tc_cp_pair_32x128b_warpx4(sf_t, sdesc_sf_tile(s_sfa));
+                        tc_cp_pair_32x128b_warpx4(sf_t + 4u, sdesc_sf_tile(s_sfa + 512u));
+                        tc_cp_pair_32x128b_warpx4(sf_t + 8u, sdesc_sf_tile(s_sfb));
+                        tc_cp_pair_32x128b_warpx4(sf_t + 12u, sdesc_sf_tile(s_sfb + 1024u));
+                        tc_cp_pair_32x128b_warpx4(sf_t + 16u, sdesc_sf_tile(s_sfb + 512u));
+                        tc_cp_pair_32x128b_warpx4(sf_t + 20u, sdesc_sf_tile(s_sfb + 1536u));
+                    } else {
+                        tc_cp_pair_32x128b_warpx4(sf_t, sdesc_sf_tile(s_sfa));
+                        tc_cp_pair_32x128b_warpx4(sf_t + 4u, sdesc_sf_tile(s_sfb));
+                        tc_cp_pair_32x128b_warpx4(sf_t + 8u, sdesc_sf_tile(s_sfb + 512u));
+                    }
                     tc_commit_pair_mc(sf_full_bar(stage), 1);
                     if (++stage == STAGES) {
                         stage = 0;
@@ -639,12 +706,14 @@ bool make_operand_map(CUtensorMap* map, const void* base, int64_t rows, int64_t 
 }
 
 // A scale-factor buffer of `tiles` 512-byte tiles as [2 * tiles, 256] bytes, box 256 x 2.
-bool make_sf_map(CUtensorMap* map, const void* base, int64_t tiles) {
+// Tiles past the end read as zeros.  A box is `box_tiles` consecutive tiles
+// (1 for FP8 stages, 2 for FP4 stages).
+bool make_sf_map(CUtensorMap* map, const void* base, int64_t tiles, uint32_t box_tiles) {
     auto enc = tensor_map_encoder();
     if (!enc) return false;
     cuuint64_t dims[2] = {256, static_cast<cuuint64_t>(2 * tiles)};
     cuuint64_t strides[1] = {256};
-    cuuint32_t box[2] = {256, 2};
+    cuuint32_t box[2] = {256, 2 * box_tiles};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -656,7 +725,14 @@ uint64_t g_timeout_ns = 2000000000ull;
 int g_fault_skip_producer = 0;
 int g_variant = 0;  // 0 automatic, 1 force the 1-SM kernel, 2 force the 2-SM kernel
 
+bool is_fp4(const GemmArgs& g) { return g.elem_fmt == kE2M1; }
+
+// Bytes of one K-contiguous operand row.
+int64_t row_bytes(const GemmArgs& g) { return is_fp4(g) ? g.K / 2 : g.K; }
+
 KParams base_params(const GemmArgs& g, int bm, int bn) {
+    const bool fp4 = is_fp4(g);
+    const int64_t stage_k = fp4 ? 2 * BK : BK;  // elements per 128-byte stage row
     KParams p{};
     p.sfa = g.sfa;
     p.sfb = g.sfb;
@@ -669,43 +745,47 @@ KParams base_params(const GemmArgs& g, int bm, int bn) {
     p.vec_store = g.vec_store;
     p.num_m_tiles = static_cast<int>((g.M + bm - 1) / bm);
     p.num_n_tiles = static_cast<int>((g.N + bn - 1) / bn);
-    p.num_kb = static_cast<int>((g.K + BK - 1) / BK);
+    p.num_kb = static_cast<int>((g.K + stage_k - 1) / stage_k);
+    p.sf_ntk = static_cast<int>((g.K + 127) / 128);
     p.num_sf_n_tiles = static_cast<int>((g.N + 127) / 128);
     p.batch = static_cast<int>(g.batch);
     p.c_batch_stride = g.c_batch_stride;
-    p.sfa_batch_tiles = ((g.M + 127) / 128) * static_cast<int64_t>(p.num_kb);
-    p.sfb_batch_tiles = ((g.N + 127) / 128) * static_cast<int64_t>(p.num_kb);
+    p.sfa_batch_tiles = ((g.M + 127) / 128) * static_cast<int64_t>(p.sf_ntk);
+    p.sfb_batch_tiles = ((g.N + 127) / 128) * static_cast<int64_t>(p.sf_ntk);
     p.group_m = 16;
-    p.idesc = make_idesc_mxf8(g.elem_fmt, g.elem_fmt, bm, bn);
+    p.idesc = fp4 ? make_idesc_mxf4(bm, bn) : make_idesc_mxf8(g.elem_fmt, g.elem_fmt, bm, bn);
     p.timeout_ns = g_timeout_ns;
     p.skip_producer = g_fault_skip_producer;
     return p;
 }
 
+template <bool FP4>
 cudaError_t launch_1sm(const GemmArgs& g, cudaStream_t stream) {
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once, [] {
-        attr_err = cudaFuncSetAttribute(mx_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, sm1::SMEM_ALLOC);
+        attr_err = cudaFuncSetAttribute(mx_gemm_kernel<FP4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        sm1::smem_alloc(FP4));
     });
     if (attr_err != cudaSuccess) return attr_err;
     CUtensorMap ma, mb;
-    if (!make_operand_map(&ma, g.a, g.M, g.K, sm1::BM, g.batch, g.a_batch_stride) ||
-        !make_operand_map(&mb, g.bt, g.N, g.K, sm1::BN, g.batch, g.b_batch_stride))
+    if (!make_operand_map(&ma, g.a, g.M, row_bytes(g), sm1::BM, g.batch, g.a_batch_stride) ||
+        !make_operand_map(&mb, g.bt, g.N, row_bytes(g), sm1::BN, g.batch, g.b_batch_stride))
         return cudaErrorInvalidValue;
     KParams p = base_params(g, sm1::BM, sm1::BN);
     const int tiles = p.batch * p.num_m_tiles * p.num_n_tiles;
     const int sms = device_sm_count();
     const int grid = tiles < sms ? tiles : sms;
-    mx_gemm_kernel<<<grid, sm1::THREADS, sm1::SMEM_ALLOC, stream>>>(ma, mb, p);
+    mx_gemm_kernel<FP4><<<grid, sm1::THREADS, sm1::smem_alloc(FP4), stream>>>(ma, mb, p);
     return cudaGetLastError();
 }
 
-void pair_launch_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, int clusters, cudaStream_t stream) {
+void pair_launch_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, int clusters, bool fp4,
+                        cudaStream_t stream) {
     *cfg = cudaLaunchConfig_t{};
     cfg->gridDim = dim3(2 * clusters, 1, 1);
     cfg->blockDim = dim3(sm2::THREADS, 1, 1);
-    cfg->dynamicSmemBytes = sm2::SMEM_ALLOC;
+    cfg->dynamicSmemBytes = sm2::smem_alloc(fp4);
     cfg->stream = stream;
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
@@ -716,6 +796,7 @@ void pair_launch_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, int 
 }
 
 // Co-resident 2-CTA clusters of the pair kernel on the current device (cached).
+template <bool FP4>
 int max_pair_clusters() {
     static std::mutex mu;
     static int cached[64] = {};
@@ -725,38 +806,39 @@ int max_pair_clusters() {
     if (cached[dev] == 0) {
         cudaLaunchConfig_t cfg;
         cudaLaunchAttribute attr[1];
-        pair_launch_config(&cfg, attr, device_sm_count() / 2, nullptr);
+        pair_launch_config(&cfg, attr, device_sm_count() / 2, FP4, nullptr);
         int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, mx_gemm_2sm_kernel, &cfg) != cudaSuccess || n <= 0)
+        if (cudaOccupancyMaxActiveClusters(&n, mx_gemm_2sm_kernel<FP4>, &cfg) != cudaSuccess || n <= 0)
             n = device_sm_count() / 2;
         cached[dev] = n > 0 ? n : 1;
     }
     return cached[dev];
 }
 
+template <bool FP4>
 cudaError_t launch_2sm(const GemmArgs& g, cudaStream_t stream) {
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once, [] {
-        attr_err =
-            cudaFuncSetAttribute(mx_gemm_2sm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, sm2::SMEM_ALLOC);
+        attr_err = cudaFuncSetAttribute(mx_gemm_2sm_kernel<FP4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        sm2::smem_alloc(FP4));
     });
     if (attr_err != cudaSuccess) return attr_err;
     CUtensorMap ma, mb, msa, msb;
     const int64_t sfa_tiles = g.batch * ((g.M + 127) / 128) * ((g.K + 127) / 128);
     const int64_t sfb_tiles = g.batch * ((g.N + 127) / 128) * ((g.K + 127) / 128);
-    if (!make_operand_map(&ma, g.a, g.M, g.K, 128, g.batch, g.a_batch_stride) ||
-        !make_operand_map(&mb, g.bt, g.N, g.K, 128, g.batch, g.b_batch_stride) ||
-        !make_sf_map(&msa, g.sfa, sfa_tiles) || !make_sf_map(&msb, g.sfb, sfb_tiles))
+    if (!make_operand_map(&ma, g.a, g.M, row_bytes(g), 128, g.batch, g.a_batch_stride) ||
+        !make_operand_map(&mb, g.bt, g.N, row_bytes(g), 128, g.batch, g.b_batch_stride) ||
+        !make_sf_map(&msa, g.sfa, sfa_tiles, FP4 ? 2 : 1) || !make_sf_map(&msb, g.sfb, sfb_tiles, FP4 ? 2 : 1))
         return cudaErrorInvalidValue;
     KParams p = base_params(g, sm2::BM, sm2::BN);
     const int tiles = p.batch * p.num_m_tiles * p.num_n_tiles;
-    const int cap = max_pair_clusters();
+    const int cap = max_pair_clusters<FP4>();
     const int clusters = tiles < cap ? tiles : cap;
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[1];
-    pair_launch_config(&cfg, attr, clusters, stream);
-    return cudaLaunchKernelEx(&cfg, mx_gemm_2sm_kernel, ma, mb, msa, msb, p);
+    pair_launch_config(&cfg, attr, clusters, FP4, stream);
+    return cudaLaunchKernelEx(&cfg, mx_gemm_2sm_kernel<FP4>, ma, mb, msa, msb, p);
 }
 
 }  // namespace
@@ -770,7 +852,8 @@ void set_gemm_variant(int variant) { g_variant = variant; }
 
 cudaError_t launch_scaled_matmul(const GemmArgs& g, cudaStream_t stream) {
     const bool pair = g_variant == 2 || (g_variant == 0 && g.M > 128);
-    return pair ? launch_2sm(g, stream) : launch_1sm(g, stream);
+    if (is_fp4(g)) return pair ? launch_2sm<true>(g, stream) : launch_1sm<true>(g, stream);
+    return pair ? launch_2sm<false>(g, stream) : launch_1sm<false>(g, stream);
 }
 
 cudaError_t read_and_clear_device_status(int* status) {

@@ -412,10 +412,17 @@ mx_status mx_scaled_matmul_workspace(int64_t M, int64_t N, int64_t K, int scales
     return MX_OK;
 }
 
+static int gemm_fmt(mx_dtype elem_dtype) {
+    return elem_dtype == MX_E4M3FN ? kE4M3 : (elem_dtype == MX_E5M2 ? kE5M2 : kE2M1);
+}
+
+// Bytes of `k` elements of a K-contiguous operand row.
+static int64_t elem_bytes(mx_dtype elem_dtype, int64_t k) { return elem_dtype == MX_E2M1 ? k / 2 : k; }
+
 static mx_status check_matmul(const void* a, const void* bt, const uint8_t* a_scale, const uint8_t* b_scale,
                               mx_dtype elem_dtype, int64_t M, int64_t N, int64_t K, mx_dtype out_dtype, void* c,
                               int64_t ldc) {
-    if (elem_dtype != MX_E4M3FN && elem_dtype != MX_E5M2) return MX_ERR_UNSUPPORTED_DTYPE;
+    if (elem_dtype != MX_E4M3FN && elem_dtype != MX_E5M2 && elem_dtype != MX_E2M1) return MX_ERR_UNSUPPORTED_DTYPE;
     if (out_dtype != MX_F32 && out_dtype != MX_BF16) return MX_ERR_UNSUPPORTED_DTYPE;
     if (M < 0 || N < 0 || K < 0) return MX_ERR_INVALID_ARG;
     if (K < 32 || K % 32 != 0) return MX_ERR_SHAPE;
@@ -466,12 +473,12 @@ mx_status mx_scaled_matmul(const void* a, const void* bt, const uint8_t* a_scale
     g.K = K;
     g.c = c;
     g.ldc = ldc;
-    g.elem_fmt = elem_dtype == MX_E4M3FN ? kE4M3 : kE5M2;
+    g.elem_fmt = gemm_fmt(elem_dtype);
     g.out_bf16 = out_dtype == MX_BF16;
     g.vec_store = aligned16(c) && (ldc * (out_dtype == MX_F32 ? 4 : 2)) % 16 == 0;
     g.batch = 1;
-    g.a_batch_stride = M * K;
-    g.b_batch_stride = N * K;
+    g.a_batch_stride = M * elem_bytes(elem_dtype, K);
+    g.b_batch_stride = N * elem_bytes(elem_dtype, K);
     g.c_batch_stride = M * ldc;
     return from_cuda(launch_scaled_matmul(g, s));
 }
@@ -506,6 +513,10 @@ mx_status mx_fused_quantize_matmul(const void* x, mx_dtype x_dtype, int64_t ld_x
     cfg.geometry = MX_GEOM_1X32;
     cfg.dim = -1;
     cfg.scale_layout = MX_SCALE_TC_SF;
+    if (elem_dtype == MX_E2M1) {  // the tensor cores' nibble order: element 2i in the low nibble
+        cfg.fp4_lane_stride = 1;
+        cfg.fp4_nibble_parity = 1;
+    }
     st = mx_quantize(x, x_dtype, M, K, ld_x, elem_dtype, &cfg, xq, xs, stream);
     if (st != MX_OK) return st;
     return mx_scaled_matmul(xq, wt, xs, w_scale_sf, 1, elem_dtype, M, N, K, out_dtype, c, ldc, nullptr, 0, stream);
@@ -541,8 +552,11 @@ mx_status mx_block_scaled_dot(const void* lhs, const int64_t* lhs_dims, int lhs_
     DotPlan P;
     mx_status st = plan_dot(lhs_dims, lhs_rank, rhs_dims, rhs_rank, dims, &P);
     if (st != MX_OK) return st;
-    if (elem_dtype != MX_E4M3FN && elem_dtype != MX_E5M2) return MX_ERR_UNSUPPORTED_DTYPE;
+    if (elem_dtype != MX_E4M3FN && elem_dtype != MX_E5M2 && elem_dtype != MX_E2M1) return MX_ERR_UNSUPPORTED_DTYPE;
     if (out_dtype != MX_F32 && out_dtype != MX_BF16) return MX_ERR_UNSUPPORTED_DTYPE;
+    // packed e2m1 pairs run along the contracting axis: it must be innermost
+    const bool fp4 = elem_dtype == MX_E2M1;
+    if (fp4 && (P.lc != lhs_rank - 1 || P.rc != rhs_rank - 1)) return MX_ERR_UNSUPPORTED_DTYPE;
     if (P.batch == 0 || P.M == 0 || P.N == 0) return MX_OK;
     if (!lhs || !rhs || !lhs_scale || !rhs_scale || !out) return MX_ERR_INVALID_ARG;
     const uintptr_t esize = out_dtype == MX_F32 ? 4 : 2;
@@ -559,14 +573,15 @@ mx_status mx_block_scaled_dot(const void* lhs, const int64_t* lhs_dims, int lhs_
     const uint8_t* bt = static_cast<const uint8_t*>(rhs);
     const uint8_t* sb = static_cast<const uint8_t*>(rhs_scale);
     cudaError_t e = cudaSuccess;
+    const int64_t code_div = fp4 ? 2 : 1;  // elements per byte along the contracting axis
     if (!P.lcanon) {
-        e = permute_operand(lhs, lhs_dims, lhs_rank, P.lperm, P.lc, 1, ws + P.off_lq, s);
+        e = permute_operand(lhs, lhs_dims, lhs_rank, P.lperm, P.lc, code_div, ws + P.off_lq, s);
         if (e == cudaSuccess) e = permute_operand(lhs_scale, lhs_dims, lhs_rank, P.lperm, P.lc, 32, ws + P.off_ls, s);
         a = ws + P.off_lq;
         sa = ws + P.off_ls;
     }
     if (e == cudaSuccess && !P.rcanon) {
-        e = permute_operand(rhs, rhs_dims, rhs_rank, P.rperm, P.rc, 1, ws + P.off_rq, s);
+        e = permute_operand(rhs, rhs_dims, rhs_rank, P.rperm, P.rc, code_div, ws + P.off_rq, s);
         if (e == cudaSuccess) e = permute_operand(rhs_scale, rhs_dims, rhs_rank, P.rperm, P.rc, 32, ws + P.off_rs, s);
         bt = ws + P.off_rq;
         sb = ws + P.off_rs;
@@ -587,12 +602,12 @@ mx_status mx_block_scaled_dot(const void* lhs, const int64_t* lhs_dims, int lhs_
     g.K = P.K;
     g.c = out;
     g.ldc = P.N;
-    g.elem_fmt = elem_dtype == MX_E4M3FN ? kE4M3 : kE5M2;
+    g.elem_fmt = gemm_fmt(elem_dtype);
     g.out_bf16 = out_dtype == MX_BF16;
     g.vec_store = aligned16(out) && (P.N * static_cast<int64_t>(esize)) % 16 == 0;
     g.batch = P.batch;
-    g.a_batch_stride = P.M * P.K;
-    g.b_batch_stride = P.N * P.K;
+    g.a_batch_stride = P.M * elem_bytes(elem_dtype, P.K);
+    g.b_batch_stride = P.N * elem_bytes(elem_dtype, P.K);
     g.c_batch_stride = P.M * P.N;
     return from_cuda(launch_scaled_matmul(g, s));
 }

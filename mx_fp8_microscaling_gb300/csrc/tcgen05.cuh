@@ -152,6 +152,20 @@ __device__ __forceinline__ void tc_mma_mxf8(uint32_t d_taddr, uint64_t adesc, ui
         : "memory");
 }
 
+// Block-scaled MXFP4: A and B packed e2m1 (two elements a byte, K = 64 per
+// instruction), one UE8M0 scale per 32 elements (scale_vec::2X: the scale
+// data ID selects bytes {0,1} or {2,3} of each scale column).
+__device__ __forceinline__ void tc_mma_mxf4(uint32_t d_taddr, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t sfa_taddr, uint32_t sfb_taddr, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(
+            d_taddr),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa_taddr), "r"(sfb_taddr)
+        : "memory");
+}
+
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // 32 lanes x 32 consecutive 32-bit columns: thread i of the warp receives
@@ -254,6 +268,17 @@ __device__ __forceinline__ void tc_mma_mxf8_pair(uint32_t d_taddr, uint64_t ades
         : "memory");
 }
 
+__device__ __forceinline__ void tc_mma_mxf4_pair(uint32_t d_taddr, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                                 uint32_t sfa_taddr, uint32_t sfb_taddr, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(
+            d_taddr),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa_taddr), "r"(sfb_taddr)
+        : "memory");
+}
+
 // 32 lanes x 128 consecutive 32-bit columns in one instruction: thread i of
 // the warp receives lane (quarter base + i), columns [col, col + 128) as
 // r[j][k] = column col + 32 j + k.
@@ -297,6 +322,13 @@ __device__ __forceinline__ uint64_t sdesc_sf_tile(uint32_t saddr) {
 __host__ __device__ constexpr uint32_t make_idesc_mxf8(int a_fmt, int b_fmt, int m, int n) {
     return (static_cast<uint32_t>(a_fmt) << 7) | (static_cast<uint32_t>(b_fmt) << 10) |
            (static_cast<uint32_t>(n >> 3) << 17) | (1u << 23) | (static_cast<uint32_t>(m >> 4) << 24);
+}
+
+// Instruction descriptor for kind::mxf4: A and B E2M1 (format code 1 in this
+// kind), UE8M0 scales, M x N tile; scale data IDs are or-ed in per MMA.
+__host__ __device__ constexpr uint32_t make_idesc_mxf4(int m, int n) {
+    return (1u << 7) | (1u << 10) | (static_cast<uint32_t>(n >> 3) << 17) | (1u << 23) |
+           (static_cast<uint32_t>(m >> 4) << 24);
 }
 
 }  // namespace mx

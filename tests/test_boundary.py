@@ -121,7 +121,7 @@ def _matmul_status(lib, elem=4, M=128, N=128, K=128, out=3, ldc=128, a=FAKE, bt=
 
 
 @pytest.mark.parametrize("kwargs,status", [
-    (dict(elem=6), 2),          # e2m1 operands: not a ScaledMatmul target
+    (dict(elem=7), 2),          # e8m0 is a scale type, not an operand type
     (dict(elem=1), 2),
     (dict(out=4), 2),           # output only f32 / bf16
     (dict(K=48), 5),
@@ -220,7 +220,7 @@ def test_dot_argument_errors(lib, mx):
         kw.get("lhs", FAKE), shape, 3, FAKE, kw.get("rhs", FAKE), shape, 3, FAKE, ct.byref(dims),
         kw.get("elem", 4), kw.get("out_dtype", 3), kw.get("out", FAKE), kw.get("ws", FAKE),
         kw.get("ws_bytes", 1 << 30), None)
-    assert call(elem=6) == 2
+    assert call(elem=7) == 2
     assert call(out_dtype=4) == 2
     assert call(lhs=None) == 1
     assert call(lhs=FAKE_MISALIGNED) == 6   # read in place by TMA
@@ -229,3 +229,14 @@ def test_dot_argument_errors(lib, mx):
     assert call(ws=None) == 7
     assert lib.mx_block_scaled_dot(FAKE, shape, 3, FAKE, FAKE, shape, 3, FAKE, None, 4, 3, FAKE, FAKE, 1 << 30,
                                    None) == 1
+
+
+def test_fp4_dot_needs_contracting_axis_innermost(lib, mx):
+    import ctypes as ct
+    # rhs [B, K, N]: packed e2m1 pairs would run along N, not K
+    dims = mx.make_dot_dims((0,), (0,), (2,), (1,))
+    ls = (ct.c_int64 * 3)(2, 128, 128)
+    rs = (ct.c_int64 * 3)(2, 128, 64)
+    st = lib.mx_block_scaled_dot(FAKE, ls, 3, FAKE, FAKE, rs, 3, FAKE, ct.byref(dims), 6, 3, FAKE, FAKE, 1 << 30,
+                                 None)
+    assert st == 2
