@@ -102,6 +102,24 @@ def test_matmul_strided_output(mx, variant):
     assert torch.all(big[:, N:] == -7.0)
 
 
+@pytest.mark.parametrize("out_dtype,pad,offset", [("bf16", 8, 8), ("f32", 4, 4), ("bf16", 8, 0)])
+def test_matmul_rows_16_byte_not_32_byte_aligned(mx, variant, out_dtype, pad, offset):
+    # rows 16-byte aligned but alternately 32-byte aligned (and a base 16
+    # bytes past a 32-byte boundary): both vector store widths run
+    import torch
+    M, N, K = 256, 384, 256
+    a, bt, sa, sb = _random_operands(M, N, K, "e5m2", seed=12)
+    dt = torch.float32 if out_dtype == "f32" else torch.bfloat16
+    big = torch.full((M, N + pad + offset), -3.0, dtype=dt, device="cuda")
+    out = big[:, offset:offset + N]
+    mx.mx_scaled_matmul(to_device_u8(a), to_device_u8(bt), to_device_u8(sa), to_device_u8(sb), "e5m2", out_dtype,
+                        out=out)
+    torch.cuda.synchronize()
+    c_ref, s_ref = orc.scaled_matmul(a, bt, sa, sb, "e5m2")
+    check_gemm(out.float().cpu().numpy(), c_ref, s_ref, out_dtype, TOL)
+    assert torch.all(big[:, :offset] == -3.0) and torch.all(big[:, offset + N:] == -3.0)
+
+
 def test_pipeline_256(mx):
     """MX-FP8 pipeline at M=N=K=256, seed 0: A and Bt (bf16, N(0,1) * 2^U(-20,20)
     per 32-block) quantized along K to e4m3fn on the GPU, then ScaledMatmul to
