@@ -161,6 +161,33 @@ mx_status mx_quantize(const void* in, mx_dtype in_dtype, int64_t rows, int64_t c
                       mx_stream stream);
 
 /*
+ * QuantizeMX from HOST memory to HOST memory (no page counterpart: the
+ * pipelined runtime around mx_quantize).  The rows are processed in chunks
+ * through three device slots in `workspace`: chunk i+1 is copied in and
+ * chunk i-1 copied out while chunk i is quantized on `stream` (the copies run
+ * on two internal per-device streams; events order all three).  Results are
+ * bit-identical to mx_quantize on the same data.
+ *   in_host        host [rows, ld_in] bf16/f16; pinned (cudaHostAlloc /
+ *                  cudaHostRegister) for the copies to overlap, pageable works
+ *                  but serialises
+ *   out_data_host, out_scale_host  host buffers of mx_quantize_sizes; in the
+ *                  interleaved layout rows the layout never addresses are left
+ *                  untouched
+ *   chunk_rows     rows per chunk, a multiple of the block's row extent x 1
+ *                  (plain scales), x 4 (interleaved) or x 128 (SF layout);
+ *                  0 selects about 16 MiB of input per chunk
+ *   workspace      device, 256-byte aligned, mx_quantize_host_workspace bytes
+ * Other arguments and errors as mx_quantize; MX_ERR_SHAPE for a chunk_rows
+ * that is not such a multiple.  Asynchronous: `stream` waits for the last copy
+ * out; the host buffers must stay valid until then.
+ */
+mx_status mx_quantize_host_workspace(mx_dtype in_dtype, int64_t rows, int64_t cols, mx_dtype out_dtype,
+                                     const mx_quant_cfg* cfg, int64_t chunk_rows, size_t* bytes);
+mx_status mx_quantize_host(const void* in_host, mx_dtype in_dtype, int64_t rows, int64_t cols, int64_t ld_in,
+                           mx_dtype out_dtype, const mx_quant_cfg* cfg, void* out_data_host, void* out_scale_host,
+                           int64_t chunk_rows, void* workspace, size_t workspace_bytes, mx_stream stream);
+
+/*
  * MX dequantize (page "MX Microscaling", quantizeDataApplyingMxScales NOTE:
  * the matmul side applies ldexpf(x, E8M0 - 127); "FP4 x4-Pack": the read-back
  * uses the same lane permutation): out[r,c] = decode(code) * 2^(E - 127).

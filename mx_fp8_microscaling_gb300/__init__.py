@@ -72,6 +72,8 @@ def _load():
         "mx_quantize_sizes": [I, I, I64, I64, ctypes.POINTER(QuantCfg), PS, PI64, PI64, PS],
         "mx_quantize": [P, I, I64, I64, I64, I, ctypes.POINTER(QuantCfg), P, P, P],
         "mx_dequantize": [P, P, I, I64, I64, ctypes.POINTER(QuantCfg), I, P, I64, P],
+        "mx_quantize_host_workspace": [I, I64, I64, I, ctypes.POINTER(QuantCfg), I64, PS],
+        "mx_quantize_host": [P, I, I64, I64, I64, I, ctypes.POINTER(QuantCfg), P, P, I64, P, SZ, P],
         "mx_sf_layout_bytes": [I64, I64, PS],
         "mx_repack_scales": [P, I64, I64, I64, P, P],
         "mx_scaled_matmul_workspace": [I64, I64, I64, I, PS],
@@ -191,6 +193,40 @@ def mx_quantize(x: torch.Tensor, out_dtype: str = "e4m3fn", *, geometry="8x4", d
                             ctypes.byref(cfg), _dev_ptr(out_data), _dev_ptr(out_scale), _stream(stream)),
            "mx_quantize")
     return out_data, out_scale
+
+
+def mx_quantize_host_workspace(rows: int, cols: int, in_dtype: str = "bf16", out_dtype: str = "e4m3fn",
+                               cfg: QuantCfg | None = None, chunk_rows: int = 0) -> int:
+    n = ctypes.c_size_t()
+    _check(_lib.mx_quantize_host_workspace(DTYPES[in_dtype], rows, cols, DTYPES[out_dtype],
+                                           ctypes.byref(cfg) if cfg is not None else None, chunk_rows,
+                                           ctypes.byref(n)), "mx_quantize_host_workspace")
+    return n.value
+
+
+def mx_quantize_host(x: torch.Tensor, out_dtype: str = "e4m3fn", *, out_data: torch.Tensor,
+                     out_scale: torch.Tensor, geometry="8x4", dim=-2, scale_layout="plain", fp4_lane_stride=2,
+                     fp4_nibble_parity=0, emax_alt=False, chunk_rows: int = 0,
+                     workspace: torch.Tensor | None = None, stream=None) -> None:
+    """QuantizeMX of a HOST tensor x (bf16/f16, 2-D, rows may be strided)
+    into HOST tensors out_data / out_scale (sizes of mx_quantize_sizes),
+    pipelined through device slots.  Pinned host tensors overlap the copies.
+    Asynchronous on `stream`."""
+    if x.is_cuda or out_data.is_cuda or out_scale.is_cuda:
+        raise ValueError("mx_quantize_host takes host tensors")
+    if x.dim() != 2 or x.stride(1) != 1:
+        raise ValueError("mx_quantize_host takes a 2-D tensor with unit column stride")
+    rows, cols = x.shape
+    cfg = make_cfg(geometry, dim, scale_layout, fp4_lane_stride, fp4_nibble_parity, emax_alt)
+    in_dtype = _in_dtype(x)
+    need = mx_quantize_host_workspace(rows, cols, in_dtype, out_dtype, cfg, chunk_rows)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device="cuda")
+    _check(_lib.mx_quantize_host(ctypes.c_void_p(x.data_ptr()), DTYPES[in_dtype], rows, cols, x.stride(0),
+                                 DTYPES[out_dtype], ctypes.byref(cfg), ctypes.c_void_p(out_data.data_ptr()),
+                                 ctypes.c_void_p(out_scale.data_ptr()), chunk_rows, _dev_ptr(workspace),
+                                 workspace.numel(), _stream(stream)),
+           "mx_quantize_host")
 
 
 def mx_dequantize(data: torch.Tensor, scale: torch.Tensor, rows: int, cols: int, in_dtype: str = "e4m3fn",

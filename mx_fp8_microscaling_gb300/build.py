@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT_DIR, "libmx.so")
 
-SOURCES = ["mx_api.cu", "quantize.cu", "dequantize.cu", "repack.cu", "permute.cu", "gemm.cu", "noalloc.cu"]
+SOURCES = ["mx_api.cu", "quantize.cu", "dequantize.cu", "repack.cu", "permute.cu", "gemm.cu", "noalloc.cu", "host_pipeline.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",
                      "-I", INCLUDE, "-I", CSRC]

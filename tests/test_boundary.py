@@ -240,3 +240,25 @@ def test_fp4_dot_needs_contracting_axis_innermost(lib, mx):
     st = lib.mx_block_scaled_dot(FAKE, ls, 3, FAKE, FAKE, rs, 3, FAKE, ct.byref(dims), 6, 3, FAKE, FAKE, 1 << 30,
                                  None)
     assert st == 2
+
+
+def test_host_quantize_workspace_and_errors(mx, lib):
+    import ctypes as ct
+    cfg = mx.make_cfg("1x32", -1, "plain")
+    # three slots of (input chunk + codes + scales), each 256-byte rounded
+    slot = 128 * 512 * 2 + 128 * 512 + 128 * 16
+    assert mx.mx_quantize_host_workspace(1000, 512, "bf16", "e4m3fn", cfg, 128) == 3 * slot
+    cfg_sf = mx.make_cfg("1x32", -1, "sf")
+    with pytest.raises(mx.MxError) as e:
+        mx.mx_quantize_host_workspace(1000, 512, "bf16", "e4m3fn", cfg_sf, 100)   # SF: multiples of 128 rows
+    assert e.value.status == 5
+    cfg84 = mx.make_cfg("8x4", -2, "interleave")
+    with pytest.raises(mx.MxError) as e:
+        mx.mx_quantize_host_workspace(1024, 512, "bf16", "e4m3fn", cfg84, 24)  # 4 scale rows of 8x4 = 32
+    assert e.value.status == 5
+    assert mx.mx_quantize_host_workspace(1024, 512, "bf16", "e4m3fn", cfg84, 32) > 0
+    st = lib.mx_quantize_host(FAKE, 1, 256, 512, 512, 4, ct.byref(cfg), FAKE, FAKE, 128, FAKE, 16, None)
+    assert st == 7
+    st = lib.mx_quantize_host(FAKE, 1, 256, 512, 512, 4, ct.byref(cfg), FAKE, FAKE, 128, FAKE_MISALIGNED,
+                              1 << 30, None)
+    assert st == 6
