@@ -452,6 +452,42 @@ class Dot:
             timer.run(label, fn)
 
 
+def vendor_gemm_reference(torch, g, steps):
+    """cuBLASLt's block-scaled FP8 GEMM (torch._scaled_mm with E8M0 scales in
+    the same tensor-core layout) on the same e4m3fn operands and scales as
+    this library's 8192^3 GEMM, timed after the main loop in the same
+    pattern (operand quantize + repack, then the GEMM): a comparison point,
+    not part of this library's path or of the timed step."""
+    try:
+        qa, qb, sfa, sfb = g.keep[2], g.keep[3], g.keep[6], g.keep[7]
+        a8 = qa.view(torch.float8_e4m3fn)
+        b8 = qb.view(torch.float8_e4m3fn)
+        sa8 = sfa.view(torch.float8_e8m0fnu)
+        sb8 = sfb.view(torch.float8_e8m0fnu)
+        quant = [fn for label, fn in g.ops[:4]]            # e4m3fn case: quantize A, B, repack A, B
+        ours = g.ops[4][1]
+        times = {"ours": [], "cublaslt": []}
+        for it in range(3 + steps):
+            for which in ("ours", "cublaslt"):
+                for fn in quant:
+                    fn()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                if which == "ours":
+                    ours()
+                else:
+                    torch._scaled_mm(a8, b8.t(), sa8, sb8, out_dtype=torch.bfloat16)
+                e1.record()
+                torch.cuda.synchronize()
+                if it >= 3:
+                    times[which].append(e0.elapsed_time(e1))
+        out = {k: round(GEMM_FLOP / (statistics.median(v) * 1e-3) / 1e12, 1) for k, v in times.items()}
+        return {"tflops": out, "what": "e4m3fn -> bf16 8192^3, same operands and SF-layout scales, median of "
+                                      f"{steps}; cuBLASLt via torch._scaled_mm"}
+    except Exception as e:  # a torch build without block-scaled _scaled_mm
+        return {"unavailable": f"{type(e).__name__}: {str(e)[:160]}"}
+
+
 # ------------------------------------------------------------- CPU oracle
 
 def oracle_sweep_sample(rows=2048, repeats=1):
@@ -665,6 +701,8 @@ def main():
                          "peak": round(peak_fp8, 1), "unit": "TFLOP/s", "frac": round(avg / peak_fp8, 4),
                          "peak_source": f"{peaks['src']} bf16 burst x {FP8_OVER_BF16} (nominal MXFP8/bf16)",
                          "traffic": profiled_traffic("mx_gemm_2sm_kernel", source_hash("gemm.cu"))}}
+    if "gemm" in parts:
+        line["scaled_matmul"]["vendor_reference"] = vendor_gemm_reference(torch, parts["gemm"], args.steps)
     if "fp4" in parts:
         ms = timer.avg_ms("fp4")
         gbs = FP4_BYTES / (ms * 1e-3) / 1e9

@@ -456,31 +456,44 @@ constexpr uint32_t B_STAGE = 128 * BK;   // 16 KB
 constexpr uint32_t OFF_A = 0;
 constexpr uint32_t OFF_B = OFF_A + STAGES * A_STAGE;
 constexpr uint32_t OFF_SFA = OFF_B + STAGES * B_STAGE;
-// this CTA's 128 rows of A; all 256 rows of B (both CTAs need them)
+// Scale tiles travel in groups of sf_group() stages.  FP8: one TMA load per
+// scale tensor per 8 stages, on a group barrier of its own, 2 groups in
+// flight (per-stage loads of 512-byte tiles measured 2.6 % slower at 8192^3,
+// and counting a group's bytes on its first stage's barrier 1.3 % slower).
+// FP4: one stage per group, the scales riding with each stage's operands in
+// the stage's own slot (grouping measured 6 % slower there).  A group holds
+// this CTA's 128 rows of A and all 256 rows of B (both CTAs need them).
+__host__ __device__ constexpr int sf_group(bool fp4) { return fp4 ? 1 : 8; }
+__host__ __device__ constexpr int sf_slots(bool fp4) { return fp4 ? STAGES : 2; }
 __host__ __device__ constexpr uint32_t sfa_stage(bool fp4) { return fp4 ? 1024u : 512u; }
-__host__ __device__ constexpr uint32_t sfb_stage(bool fp4) { return 2 * sfa_stage(fp4); }
-__host__ __device__ constexpr uint32_t off_sfb(bool fp4) { return OFF_SFA + STAGES * sfa_stage(fp4); }
-__host__ __device__ constexpr uint32_t off_bar(bool fp4) { return off_sfb(fp4) + STAGES * sfb_stage(fp4); }
-constexpr int NUM_BARS = 3 * STAGES + 4;  // full, empty, sf_full [S]; tmem_full, tmem_empty, mma_done, sf_done
-__host__ __device__ constexpr uint32_t off_misc(bool fp4) { return off_bar(fp4) + NUM_BARS * 8; }
+__host__ __device__ constexpr uint32_t sfa_group(bool fp4) { return sf_group(fp4) * sfa_stage(fp4); }
+__host__ __device__ constexpr uint32_t off_sfb(bool fp4) { return OFF_SFA + sf_slots(fp4) * sfa_group(fp4); }
+__host__ __device__ constexpr uint32_t off_bar(bool fp4) { return off_sfb(fp4) + sf_slots(fp4) * 2 * sfa_group(fp4); }
+// full, empty, sf_full [S]; tmem_full, tmem_empty, mma_done, sf_done; group full, empty [slots]
+__host__ __device__ constexpr int num_bars(bool fp4) { return 3 * STAGES + 4 + 2 * sf_slots(fp4); }
+__host__ __device__ constexpr uint32_t off_misc(bool fp4) { return off_bar(fp4) + num_bars(fp4) * 8; }
 __host__ __device__ constexpr uint32_t smem_alloc(bool fp4) { return off_misc(fp4) + 16 + 1024; }
-__host__ __device__ constexpr uint32_t pair_tx(bool fp4) { return 2 * (A_STAGE + B_STAGE + sfa_stage(fp4) + sfb_stage(fp4)); }
+constexpr uint32_t PAIR_TX = 2 * (A_STAGE + B_STAGE);  // both CTAs' operand tiles of a stage
+__host__ __device__ constexpr uint32_t pair_sf_tx(bool fp4) { return 2 * 3 * sfa_group(fp4); }
 constexpr int SF_WARP = 10;              // warp that copies scale factors to tensor memory
 constexpr int THREADS = NUM_THREADS + 32;
 }  // namespace sm2
 
 // Scale-factor buffers are read by TMA as [2 * tiles, 256] bytes: a 512-byte
-// tile t is rows 2t and 2t+1 (box 256 x 2); tiles past the end read as zeros.
+// tile t is rows 2t and 2t+1; one box is a scale group's consecutive tiles;
+// tiles past the end read as zeros.
 template <bool FP4>
 __global__ void __launch_bounds__(sm2::THREADS, 1)
     mx_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                        const __grid_constant__ CUtensorMap tmap_sfa, const __grid_constant__ CUtensorMap tmap_sfb,
                        const KParams p) {
     using namespace sm2;
-    constexpr uint32_t SFA_STAGE = sfa_stage(FP4), SFB_STAGE = sfb_stage(FP4);
+    constexpr uint32_t SFA_STAGE = sfa_stage(FP4), SFA_GROUP = sfa_group(FP4);
     constexpr uint32_t OFF_SFB = off_sfb(FP4), OFF_BAR = off_bar(FP4), OFF_MISC = off_misc(FP4);
     constexpr uint32_t SF_COLS = sf_cols(FP4);
-    constexpr uint32_t PAIR_TX = pair_tx(FP4);
+    constexpr uint32_t PAIR_SF_TX = pair_sf_tx(FP4);
+    constexpr int SF_TILES_PER_STAGE = FP4 ? 2 : 1;
+    constexpr int SF_GROUP = sf_group(FP4), SF_SLOTS = sf_slots(FP4);
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sb = smem_u32(smem);
@@ -495,6 +508,8 @@ __global__ void __launch_bounds__(sm2::THREADS, 1)
     const uint32_t tmem_empty = tmem_full + 8;
     const uint32_t mma_done = tmem_full + 16;
     const uint32_t sf_done = tmem_full + 24;
+    auto sfg_full_bar = [&](int g) { return sb + OFF_BAR + 8u * (3 * STAGES + 4 + g); };
+    auto sfg_empty_bar = [&](int g) { return sb + OFF_BAR + 8u * (3 * STAGES + 4 + SF_SLOTS + g); };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
 
@@ -503,6 +518,10 @@ __global__ void __launch_bounds__(sm2::THREADS, 1)
             mbar_init(full_bar(s), 1);     // rank 0's: its arrive + both CTAs' bytes
             mbar_init(empty_bar(s), 1);    // one multicast commit per use
             mbar_init(sf_full_bar(s), 1);  // rank 0's: the scale copies of the stage are done
+        }
+        for (int g = 0; g < SF_SLOTS; ++g) {
+            mbar_init(sfg_full_bar(g), 1);   // rank 0's: its arrive + both CTAs' scale bytes
+            mbar_init(sfg_empty_bar(g), 1);  // one multicast commit per use
         }
         mbar_init(tmem_full, 1);
         mbar_init(tmem_empty, 2 * NUM_EPI_WARPS);  // rank 0's: both CTAs' epilogue warps
@@ -528,8 +547,8 @@ __global__ void __launch_bounds__(sm2::THREADS, 1)
 
     if (warp == 0) {
         if (lane == 0 && !p.skip_producer) {
-            int stage = 0;
-            uint32_t phase = 0;
+            int stage = 0, gslot = 0;
+            uint32_t phase = 0, gphase = 0;
             bool ok = true;
             for (int t = cluster; t < num_tiles && ok; t += num_clusters) {
                 int b, mt, nt;
@@ -543,23 +562,44 @@ __global__ void __launch_bounds__(sm2::THREADS, 1)
                 const int64_t sfb_tile0 = b * p.sfb_batch_tiles + (2 * nt) * p.sf_ntk;
                 const int64_t sfb_tile1 = sfb_tile0 + p.sf_ntk;
                 for (int kb = 0; kb < p.num_kb; ++kb) {
+                    const bool group_start = kb % SF_GROUP == 0;
+                    // a scale slot is free once its last group's copies into
+                    // tensor memory have completed (for one-stage groups the
+                    // stage's empty barrier already says so)
+                    if (group_start && SF_GROUP > 1 &&
+                        !mbar_wait_bounded(sfg_empty_bar(gslot), gphase ^ 1u, abort_flag, p.timeout_ns,
+                                           &g_mx_status)) {
+                        ok = false;
+                        break;
+                    }
                     if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, p.timeout_ns, &g_mx_status)) {
                         ok = false;
                         break;
                     }
                     const uint32_t fb = mapa_shared(full_bar(stage), 0);
-                    if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), PAIR_TX);
+                    constexpr bool own_bar = SF_GROUP > 1;  // group bytes on a barrier of their own
+                    if (rank == 0) {
+                        mbar_arrive_expect_tx(full_bar(stage), PAIR_TX + (group_start && !own_bar ? PAIR_SF_TX : 0u));
+                        if (group_start && own_bar) mbar_arrive_expect_tx(sfg_full_bar(gslot), PAIR_SF_TX);
+                    }
+                    if (group_start) {
+                        // the scale tiles of stages kb .. kb + SF_GROUP - 1, one
+                        // load per scale tensor; tiles past K (or past the
+                        // buffer) feed no MMA
+                        const uint32_t gb = own_bar ? mapa_shared(sfg_full_bar(gslot), 0) : fb;
+                        const int64_t t0 = static_cast<int64_t>(SF_TILES_PER_STAGE) * kb;
+                        const uint32_t sa_g = sb + OFF_SFA + gslot * SFA_GROUP;
+                        const uint32_t sb_g = sb + OFF_SFB + gslot * 2 * SFA_GROUP;
+                        tma_load_2d_pair(sa_g, &tmap_sfa, gb, 0, static_cast<int>(2 * (sfa_tile + t0)));
+                        tma_load_2d_pair(sb_g, &tmap_sfb, gb, 0, static_cast<int>(2 * (sfb_tile0 + t0)));
+                        tma_load_2d_pair(sb_g + SFA_GROUP, &tmap_sfb, gb, 0, static_cast<int>(2 * (sfb_tile1 + t0)));
+                        if (++gslot == SF_SLOTS) {
+                            gslot = 0;
+                            gphase ^= 1u;
+                        }
+                    }
                     tma_load_3d_pair(sb + OFF_A + stage * A_STAGE, &tmap_a, fb, kb * BK, a_row, b);
                     tma_load_3d_pair(sb + OFF_B + stage * B_STAGE, &tmap_b, fb, kb * BK, b_row, b);
-                    // an FP4 stage's box covers two scale tiles along K; a
-                    // tile past K (or past the buffer) feeds no MMA
-                    const int t0 = FP4 ? 2 * kb : kb;
-                    tma_load_2d_pair(sb + OFF_SFA + stage * SFA_STAGE, &tmap_sfa, fb, 0,
-                                     static_cast<int>(2 * (sfa_tile + t0)));
-                    tma_load_2d_pair(sb + OFF_SFB + stage * SFB_STAGE, &tmap_sfb, fb, 0,
-                                     static_cast<int>(2 * (sfb_tile0 + t0)));
-                    tma_load_2d_pair(sb + OFF_SFB + stage * SFB_STAGE + SFB_STAGE / 2, &tmap_sfb, fb, 0,
-                                     static_cast<int>(2 * (sfb_tile1 + t0)));
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
@@ -567,8 +607,9 @@ __global__ void __launch_bounds__(sm2::THREADS, 1)
                 }
             }
             if (rank == 0) {
-                // rank 0's full barriers count both CTAs' bytes: once the last
-                // STAGES fills have completed, no copy of the pair is in flight
+                // rank 0's full and group barriers count both CTAs' bytes: once
+                // the last STAGES fills and SF_SLOTS groups have completed, no
+                // copy of the pair is in flight
                 for (int i = 0; i < STAGES; ++i) {
                     if (--stage < 0) {
                         stage = STAGES - 1;
@@ -576,6 +617,14 @@ __global__ void __launch_bounds__(sm2::THREADS, 1)
                     }
                     volatile int no_abort = 0;
                     (void)mbar_wait_bounded(full_bar(stage), phase, &no_abort, 100000000ull, &g_mx_status);
+                }
+                for (int i = 0; SF_GROUP > 1 && i < SF_SLOTS; ++i) {
+                    if (--gslot < 0) {
+                        gslot = SF_SLOTS - 1;
+                        gphase ^= 1u;
+                    }
+                    volatile int no_abort = 0;
+                    (void)mbar_wait_bounded(sfg_full_bar(gslot), gphase, &no_abort, 100000000ull, &g_mx_status);
                 }
             }
         }
@@ -635,34 +684,54 @@ __global__ void __launch_bounds__(sm2::THREADS, 1)
     } else if (warp == SF_WARP) {
         // Scale-factor copies, one K block at a time, off the MMA thread: a
         // tcgen05.cp costs the issuing thread as much as the four MMAs of a
-        // K block, so the MMA thread only waits for this warp's commit.
+        // K block, so the MMA thread only waits for this warp's commit.  A
+        // scale group is released (multicast commit) after its last stage.
         if (lane == 0 && rank == 0) {
-            int stage = 0;
-            uint32_t phase = 0;
+            int stage = 0, gslot = 0;
+            uint32_t phase = 0, gphase = 0;
             bool ok = true;
             for (int t = cluster; t < num_tiles && ok; t += num_clusters) {
                 for (int kb = 0; kb < p.num_kb; ++kb) {
+                    const int j = kb % SF_GROUP;
+                    // a group's scales: on their own barrier, or (one-stage
+                    // groups) with the stage's operands
+                    if (SF_GROUP > 1 && j == 0 &&
+                        !mbar_wait_bounded(sfg_full_bar(gslot), gphase, abort_flag, p.timeout_ns, &g_mx_status)) {
+                        ok = false;
+                        break;
+                    }
                     if (!mbar_wait_bounded(full_bar(stage), phase, abort_flag, p.timeout_ns, &g_mx_status)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     const uint32_t sf_t = tmem_base + TMEM_SF + SF_COLS * stage;
-                    const uint32_t s_sfa = sb + OFF_SFA + stage * SFA_STAGE;
-                    const uint32_t s_sfb = sb + OFF_SFB + stage * SFB_STAGE;
+                    // stage j of the group: A at j * SFA_STAGE; B rows 0-127 and
+                    // 128-255 in the group's two B row tiles
+                    const uint32_t s_sfa = sb + OFF_SFA + gslot * SFA_GROUP + j * SFA_STAGE;
+                    const uint32_t s_sfb0 = sb + OFF_SFB + gslot * 2 * SFA_GROUP + j * SFA_STAGE;
+                    const uint32_t s_sfb1 = s_sfb0 + SFA_GROUP;
                     if constexpr (FP4) {
+                        // K group g of the stage is scale tile g of each
                         tc_cp_pair_32x128b_warpx4(sf_t, sdesc_sf_tile(s_sfa));
                         tc_cp_pair_32x128b_warpx4(sf_t + 4u, sdesc_sf_tile(s_sfa + 512u));
-                        tc_cp_pair_32x128b_warpx4(sf_t + 8u, sdesc_sf_tile(s_sfb));
-                        tc_cp_pair_32x128b_warpx4(sf_t + 12u, sdesc_sf_tile(s_sfb + 1024u));
-                        tc_cp_pair_32x128b_warpx4(sf_t + 16u, sdesc_sf_tile(s_sfb + 512u));
-                        tc_cp_pair_32x128b_warpx4(sf_t + 20u, sdesc_sf_tile(s_sfb + 1536u));
+                        tc_cp_pair_32x128b_warpx4(sf_t + 8u, sdesc_sf_tile(s_sfb0));
+                        tc_cp_pair_32x128b_warpx4(sf_t + 12u, sdesc_sf_tile(s_sfb1));
+                        tc_cp_pair_32x128b_warpx4(sf_t + 16u, sdesc_sf_tile(s_sfb0 + 512u));
+                        tc_cp_pair_32x128b_warpx4(sf_t + 20u, sdesc_sf_tile(s_sfb1 + 512u));
                     } else {
                         tc_cp_pair_32x128b_warpx4(sf_t, sdesc_sf_tile(s_sfa));
-                        tc_cp_pair_32x128b_warpx4(sf_t + 4u, sdesc_sf_tile(s_sfb));
-                        tc_cp_pair_32x128b_warpx4(sf_t + 8u, sdesc_sf_tile(s_sfb + 512u));
+                        tc_cp_pair_32x128b_warpx4(sf_t + 4u, sdesc_sf_tile(s_sfb0));
+                        tc_cp_pair_32x128b_warpx4(sf_t + 8u, sdesc_sf_tile(s_sfb1));
                     }
                     tc_commit_pair_mc(sf_full_bar(stage), 1);
+                    if (j == SF_GROUP - 1 || kb == p.num_kb - 1) {
+                        if (SF_GROUP > 1) tc_commit_pair_mc(sfg_empty_bar(gslot), 3);  // both CTAs' producers
+                        if (++gslot == SF_SLOTS) {
+                            gslot = 0;
+                            gphase ^= 1u;
+                        }
+                    }
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
@@ -739,9 +808,9 @@ bool make_operand_map(CUtensorMap* map, const void* base, int64_t rows, int64_t 
     return r == CUDA_SUCCESS;
 }
 
-// A scale-factor buffer of `tiles` 512-byte tiles as [2 * tiles, 256] bytes, box 256 x 2.
+// A scale-factor buffer of `tiles` 512-byte tiles as [2 * tiles, 256] bytes.
 // Tiles past the end read as zeros.  A box is `box_tiles` consecutive tiles
-// (1 for FP8 stages, 2 for FP4 stages).
+// (one scale group: SF_GROUP stages of 1 (FP8) or 2 (FP4) tiles).
 bool make_sf_map(CUtensorMap* map, const void* base, int64_t tiles, uint32_t box_tiles) {
     auto enc = tensor_map_encoder();
     if (!enc) return false;
@@ -863,7 +932,8 @@ cudaError_t launch_2sm(const GemmArgs& g, cudaStream_t stream) {
     const int64_t sfb_tiles = g.batch * ((g.N + 127) / 128) * ((g.K + 127) / 128);
     if (!make_operand_map(&ma, g.a, g.M, row_bytes(g), 128, g.batch, g.a_batch_stride) ||
         !make_operand_map(&mb, g.bt, g.N, row_bytes(g), 128, g.batch, g.b_batch_stride) ||
-        !make_sf_map(&msa, g.sfa, sfa_tiles, FP4 ? 2 : 1) || !make_sf_map(&msb, g.sfb, sfb_tiles, FP4 ? 2 : 1))
+        !make_sf_map(&msa, g.sfa, sfa_tiles, sm2::sf_group(FP4) * (FP4 ? 2 : 1)) ||
+        !make_sf_map(&msb, g.sfb, sfb_tiles, sm2::sf_group(FP4) * (FP4 ? 2 : 1)))
         return cudaErrorInvalidValue;
     KParams p = base_params(g, sm2::BM, sm2::BN);
     const int tiles = p.batch * p.num_m_tiles * p.num_n_tiles;
