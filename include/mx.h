@@ -188,6 +188,29 @@ mx_status mx_quantize_host(const void* in_host, mx_dtype in_dtype, int64_t rows,
                            int64_t chunk_rows, void* workspace, size_t workspace_bytes, mx_stream stream);
 
 /*
+ * Several host-to-host QuantizeMX jobs in one pipeline: their chunks share the
+ * slot ring, so one tensor's copies overlap the next one's (no drain between
+ * tensors).  Each job is what mx_quantize_host takes (cfg by value).  All
+ * jobs are checked before anything is enqueued; the workspace is
+ * mx_quantize_host_batch_workspace bytes (the largest job's slots).
+ * njobs <= 4096.  Results equal njobs separate mx_quantize_host calls.
+ */
+typedef struct mx_host_quant_job {
+    const void* in_host;
+    mx_dtype in_dtype;
+    int64_t rows, cols, ld_in;
+    mx_dtype out_dtype;
+    mx_quant_cfg cfg;
+    void* out_data_host;
+    void* out_scale_host;
+} mx_host_quant_job;
+
+mx_status mx_quantize_host_batch_workspace(const mx_host_quant_job* jobs, int njobs, int64_t chunk_rows,
+                                           size_t* bytes);
+mx_status mx_quantize_host_batch(const mx_host_quant_job* jobs, int njobs, int64_t chunk_rows, void* workspace,
+                                 size_t workspace_bytes, mx_stream stream);
+
+/*
  * MX dequantize (page "MX Microscaling", quantizeDataApplyingMxScales NOTE:
  * the matmul side applies ldexpf(x, E8M0 - 127); "FP4 x4-Pack": the read-back
  * uses the same lane permutation): out[r,c] = decode(code) * 2^(E - 127).

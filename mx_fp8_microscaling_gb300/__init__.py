@@ -59,6 +59,12 @@ class QuantCfg(ctypes.Structure):
                 ("fp4_nibble_parity", ctypes.c_int32), ("emax_alt", ctypes.c_int32)]
 
 
+class HostJob(ctypes.Structure):
+    _fields_ = [("in_host", ctypes.c_void_p), ("in_dtype", ctypes.c_int32), ("rows", ctypes.c_int64),
+                ("cols", ctypes.c_int64), ("ld_in", ctypes.c_int64), ("out_dtype", ctypes.c_int32),
+                ("cfg", QuantCfg), ("out_data_host", ctypes.c_void_p), ("out_scale_host", ctypes.c_void_p)]
+
+
 def _load():
     if not os.path.exists(LIB_PATH):
         raise ImportError(f"libmx is not built ({LIB_PATH} missing); run "
@@ -74,6 +80,8 @@ def _load():
         "mx_dequantize": [P, P, I, I64, I64, ctypes.POINTER(QuantCfg), I, P, I64, P],
         "mx_quantize_host_workspace": [I, I64, I64, I, ctypes.POINTER(QuantCfg), I64, PS],
         "mx_quantize_host": [P, I, I64, I64, I64, I, ctypes.POINTER(QuantCfg), P, P, I64, P, SZ, P],
+        "mx_quantize_host_batch_workspace": [ctypes.POINTER(HostJob), I, I64, PS],
+        "mx_quantize_host_batch": [ctypes.POINTER(HostJob), I, I64, P, SZ, P],
         "mx_sf_layout_bytes": [I64, I64, PS],
         "mx_repack_scales": [P, I64, I64, I64, P, P],
         "mx_scaled_matmul_workspace": [I64, I64, I64, I, PS],
@@ -227,6 +235,47 @@ def mx_quantize_host(x: torch.Tensor, out_dtype: str = "e4m3fn", *, out_data: to
                                  ctypes.c_void_p(out_scale.data_ptr()), chunk_rows, _dev_ptr(workspace),
                                  workspace.numel(), _stream(stream)),
            "mx_quantize_host")
+
+
+def make_host_jobs(specs) -> ctypes.Array:
+    """specs: sequence of dicts with x (host bf16/f16 2-D tensor), out_dtype,
+    out_data, out_scale (host uint8 tensors) and the mx_quantize keyword
+    arguments geometry / dim / scale_layout / fp4_lane_stride /
+    fp4_nibble_parity / emax_alt.  The tensors must stay alive while the
+    jobs run."""
+    jobs = (HostJob * max(1, len(specs)))()
+    for j, sp in zip(jobs, specs):
+        x = sp["x"]
+        if x.is_cuda or x.dim() != 2 or x.stride(1) != 1:
+            raise ValueError("host jobs take 2-D host tensors with unit column stride")
+        j.in_host = x.data_ptr()
+        j.in_dtype = DTYPES[_in_dtype(x)]
+        j.rows, j.cols = x.shape
+        j.ld_in = x.stride(0)
+        j.out_dtype = DTYPES[sp.get("out_dtype", "e4m3fn")]
+        j.cfg = make_cfg(sp.get("geometry", "8x4"), sp.get("dim", -2), sp.get("scale_layout", "plain"),
+                         sp.get("fp4_lane_stride", 2), sp.get("fp4_nibble_parity", 0), sp.get("emax_alt", False))
+        j.out_data_host = sp["out_data"].data_ptr()
+        j.out_scale_host = sp["out_scale"].data_ptr()
+    return jobs
+
+
+def mx_quantize_host_batch_workspace(jobs, njobs: int, chunk_rows: int = 0) -> int:
+    n = ctypes.c_size_t()
+    _check(_lib.mx_quantize_host_batch_workspace(jobs, njobs, chunk_rows, ctypes.byref(n)),
+           "mx_quantize_host_batch_workspace")
+    return n.value
+
+
+def mx_quantize_host_batch(specs, *, chunk_rows: int = 0, workspace: torch.Tensor | None = None, stream=None):
+    """Several host-to-host QuantizeMX jobs (see make_host_jobs) in one
+    pipelined call.  Asynchronous on `stream`."""
+    jobs = make_host_jobs(specs)
+    if workspace is None:
+        workspace = torch.empty(mx_quantize_host_batch_workspace(jobs, len(specs), chunk_rows), dtype=torch.uint8,
+                                device="cuda")
+    _check(_lib.mx_quantize_host_batch(jobs, len(specs), chunk_rows, _dev_ptr(workspace), workspace.numel(),
+                                       _stream(stream)), "mx_quantize_host_batch")
 
 
 def mx_dequantize(data: torch.Tensor, scale: torch.Tensor, rows: int, cols: int, in_dtype: str = "e4m3fn",

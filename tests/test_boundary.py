@@ -262,3 +262,24 @@ def test_host_quantize_workspace_and_errors(mx, lib):
     st = lib.mx_quantize_host(FAKE, 1, 256, 512, 512, 4, ct.byref(cfg), FAKE, FAKE, 128, FAKE_MISALIGNED,
                               1 << 30, None)
     assert st == 6
+
+
+def test_host_quantize_batch_workspace_and_checks(mx, lib):
+    import ctypes as ct
+    import torch
+    small = torch.zeros(256, 512, dtype=torch.bfloat16)
+    big = torch.zeros(2048, 512, dtype=torch.bfloat16)
+    d = torch.empty(2048 * 512, dtype=torch.uint8)
+    s = torch.empty(2048 * 16, dtype=torch.uint8)
+    spec = lambda x: dict(x=x, out_data=d, out_scale=s, geometry="1x32", dim=-1)  # noqa: E731
+    jobs = mx.make_host_jobs([spec(small), spec(big)])
+    # the slot is the larger job's (chunks of 1024 rows here)
+    one_big = mx.make_host_jobs([spec(big)])
+    assert mx.mx_quantize_host_batch_workspace(jobs, 2, 1024) == mx.mx_quantize_host_batch_workspace(one_big, 1, 1024)
+    assert mx.mx_quantize_host_batch_workspace(jobs, 2, 1024) > mx.mx_quantize_host_batch_workspace(
+        mx.make_host_jobs([spec(small)]), 1, 1024)
+    # a bad job anywhere fails the whole call before anything runs
+    bad = mx.make_host_jobs([spec(small), spec(big)])
+    bad[1].cols = 500   # not a multiple of 32 along the block
+    assert lib.mx_quantize_host_batch(bad, 2, 0, FAKE, 1 << 30, None) == 5
+    assert lib.mx_quantize_host_batch(jobs, 2, 0, FAKE, 16, None) == 7

@@ -89,3 +89,43 @@ def test_host_quantize_repeated_calls_share_the_pipeline(mx):
         want_d, want_s = orc.quantize(bits, "bf16", "e4m3fn", geometry="1x32", dim=-1)
         assert np.array_equal(d.numpy(), want_d.reshape(-1))
         assert np.array_equal(s.numpy(), want_s.reshape(-1))
+
+
+def test_host_quantize_batch_equals_separate_calls(mx):
+    # mixed geometries, layouts, formats and input types in one pipeline,
+    # including an empty job; each result equals the device quantizer's
+    import torch
+    specs, want = [], []
+    shapes = [("8x4", -2, "interleave", "e4m3fn", "bf16", 1000, 256), ("1x32", -1, "sf", "e5m2", "f16", 300, 384),
+              ("8x4", -2, "plain", "e2m1", "bf16", 0, 64), ("1x32", -1, "plain", "e2m1", "bf16", 520, 128),
+              ("8x4", -1, "plain", "e4m3fn", "f16", 1040, 192)]
+    for i, (geometry, dim, layout, fmt, in_dtype, rows, cols) in enumerate(shapes):
+        bits = syn.random_bits(max(rows, 1), cols, in_dtype, seed=50 + i, block_exp=(-12, 12), block=(1, 4))[:rows]
+        x = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(
+            torch.bfloat16 if in_dtype == "bf16" else torch.float16).pin_memory()
+        db, sr, sc = mx.mx_quantize_sizes(rows, cols, in_dtype, fmt, mx.make_cfg(geometry, dim, layout))
+        d = torch.full((max(db, 1),), 0x5A, dtype=torch.uint8).pin_memory()
+        s = torch.full((max(sr * sc, 1),), 0x5A, dtype=torch.uint8).pin_memory()
+        specs.append(dict(x=x, out_dtype=fmt, out_data=d, out_scale=s, geometry=geometry, dim=dim,
+                          scale_layout=layout))
+        if rows:
+            dd, ds = mx.mx_quantize(x.cuda(), fmt, geometry=geometry, dim=dim, scale_layout=layout)
+            want.append((dd, ds, layout, sr, sc, rows // BLOCK_ROWS[(geometry, dim)]))
+        else:
+            want.append(None)
+    mx.mx_quantize_host_batch(specs, chunk_rows=0)
+    torch.cuda.synchronize()
+    for sp, w in zip(specs, want):
+        if w is None:
+            assert torch.all(sp["out_data"] == 0x5A)   # an empty job writes nothing
+            continue
+        dd, ds, layout, sr, sc, nscale = w
+        assert np.array_equal(sp["out_data"].numpy()[:dd.numel()], dd.cpu().numpy().reshape(-1))
+        got = sp["out_scale"].numpy()[:sr * sc].reshape(sr, sc)
+        ref = ds.cpu().numpy().reshape(sr, sc)
+        if layout == "interleave":
+            live = np.zeros(sr, bool)
+            live[[(i & 3) + 32 * (i >> 2) for i in range(nscale)]] = True
+            assert np.all(got[~live] == 0x5A)
+            got, ref = got[live], ref[live]
+        assert np.array_equal(got, ref)
