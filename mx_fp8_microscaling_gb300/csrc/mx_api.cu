@@ -340,6 +340,8 @@ mx_status mx_quantize(const void* in, mx_dtype in_dtype, int64_t rows, int64_t c
     q.fp4_perm = fp4_pair_perm(plan.stride);
     q.vec_ok = aligned16(in) && (ld_in * 2) % 16 == 0 && (reinterpret_cast<uintptr_t>(out_data) & 7u) == 0 &&
                (reinterpret_cast<uintptr_t>(out_scale) & 1u) == 0;
+    q.vec32_ok = q.vec_ok && (reinterpret_cast<uintptr_t>(in) & 31u) == 0 && (ld_in * 2) % 32 == 0 &&
+                 (reinterpret_cast<uintptr_t>(out_data) & 15u) == 0 && cols % 32 == 0;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (plan.scale_mode == MX_SCALE_TC_SF && (rows % 128 != 0 || (cols / 32) % 4 != 0)) {
         // the kernel writes live scales only; padding of the SF tiles is 0

@@ -13,6 +13,13 @@ namespace dev {
 // ---------------------------------------------------------------- memory
 
 // 16-byte streaming load that does not allocate in L1 (inputs are read once).
+// 32 bytes, read once: 256-bit load that skips L1.
+__device__ __forceinline__ void ld_stream_v8(const void* p, uint32_t (&r)[8]) {
+    asm("ld.global.nc.L1::no_allocate.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+        : "l"(p));
+}
+
 __device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
     uint4 v;
     asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"

@@ -31,6 +31,7 @@ struct QuantArgs {
     int32_t fp4_parity;     // nibble parity
     uint32_t fp4_perm;      // __byte_perm selector placing the 4 pair-bytes of an 8-element chunk
     int32_t vec_ok;         // 16-byte input rows and 8-byte output rows: vectorised kernels allowed
+    int32_t vec32_ok;       // 32-byte input rows and 16-byte output rows (FP8; 8-byte e2m1)
 };
 
 cudaError_t launch_quantize(const QuantArgs& q, bool in_f16, int fmt, cudaStream_t stream);

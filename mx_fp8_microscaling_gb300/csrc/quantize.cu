@@ -304,6 +304,87 @@ __device__ __forceinline__ int64_t remap_index(int64_t n, int stride) {
 
 // One thread per tile of br rows x tc columns (tc = max(bc, 8), the last
 // tile of a row may hold only 4 columns).  Every block of the tile is whole.
+// ----------------------------------------- 1x32 blocks along rows, 32-byte rows
+
+// Thread unit: row group g (TR rows) x column chunk c (16 columns): half a
+// block per row, one 32-byte load per row, so a block spans 2 lanes and one
+// xor shuffle finishes its max; a warp reads 1 KiB contiguous per row.  Per
+// element this does about half the work of the 8-column kernel (the per-row
+// exponent / scale arithmetic is shared by 16 elements instead of 8).
+template <bool F16, int FMT>
+__global__ void __launch_bounds__(kThreads) quant_g1x32w(QuantArgs q) {
+    constexpr int TR = 4;
+    const int lane = threadIdx.x & 31;
+    const int64_t nchunk = q.cols >> 4;
+    const int64_t ngroups = (q.rows + TR - 1) / TR;
+    const int64_t total = ngroups * nchunk;  // even: nchunk % 2 == 0
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    const int64_t in_pitch = q.ld_in * 2;
+    for (int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x + (threadIdx.x & ~31);
+         base < total; base += stride) {
+        const int64_t u = base + lane;
+        const bool active = u < total;
+        const int64_t g = active ? u / nchunk : 0;
+        const int64_t c = active ? u - g * nchunk : 0;
+        const int64_t r0 = g * TR;
+        uint32_t v[TR][8];
+#pragma unroll
+        for (int r = 0; r < TR; ++r) {
+            if (active && r0 + r < q.rows) {
+                ld_stream_v8(q.in + (r0 + r) * in_pitch + c * 32, v[r]);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) v[r][j] = 0;
+            }
+        }
+        uint32_t e[TR];
+        float s[TR];
+        bool special = false;
+#pragma unroll
+        for (int r = 0; r < TR; ++r) {
+            uint32_t m = vmax_u16x2(vmax_u16x2(vmax_u16x2(mag2(v[r][0]), mag2(v[r][1])),
+                                               vmax_u16x2(mag2(v[r][2]), mag2(v[r][3]))),
+                                    vmax_u16x2(vmax_u16x2(mag2(v[r][4]), mag2(v[r][5])),
+                                               vmax_u16x2(mag2(v[r][6]), mag2(v[r][7]))));
+            m = hmax(m);
+            m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
+            const uint32_t x = exp_byte_of_mag<F16>(m);
+            special |= (x == 255u);
+            e[r] = e8m0_of(x, q.emax_bias);
+            s[r] = prescale_mul(e[r]);
+        }
+        if (active) {
+#pragma unroll
+            for (int r = 0; r < TR; ++r) {
+                if (r0 + r >= q.rows) break;
+                uint32_t w[4];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    float y[8];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        y[2 * j] = mul_rn(widen_lo<F16>(v[r][4 * h + j]), s[r]);
+                        y[2 * j + 1] = mul_rn(widen_hi<F16>(v[r][4 * h + j]), s[r]);
+                    }
+                    pack8<FMT>(y, special, q.fp4_parity, q.fp4_perm, w[2 * h], w[2 * h + 1]);
+                }
+                if constexpr (FMT == kE2M1) {
+                    *reinterpret_cast<uint2*>(q.data + (r0 + r) * q.ld_data + c * 8) = make_uint2(w[0], w[2]);
+                } else {
+                    *reinterpret_cast<uint4*>(q.data + (r0 + r) * q.ld_data + c * 16) =
+                        make_uint4(w[0], w[1], w[2], w[3]);
+                }
+            }
+            // the even lane of each pair writes the block's scales
+            if ((lane & 1) == 0) {
+#pragma unroll
+                for (int r = 0; r < TR; ++r)
+                    if (r0 + r < q.rows) q.scale[scale_offset(q, r0 + r, c >> 1)] = static_cast<uint8_t>(e[r]);
+            }
+        }
+    }
+}
+
 template <bool F16, int FMT>
 __global__ void __launch_bounds__(kThreads) quant_generic(QuantArgs q) {
     const int br = q.block_rows, bc = q.block_cols;
@@ -374,6 +455,9 @@ cudaError_t launch_typed(const QuantArgs& q, cudaStream_t stream) {
     if (wide && q.block_rows == 8 && q.block_cols == 4) {
         const int64_t units = (q.rows / 8) * (q.cols / 8);
         quant_g84<F16, FMT><<<grid_for(units), kThreads, 0, stream>>>(q);
+    } else if (wide && q.vec32_ok && q.block_rows == 1 && q.block_cols == 32) {
+        const int64_t units = ((q.rows + 3) / 4) * (q.cols / 16);
+        quant_g1x32w<F16, FMT><<<grid_for(units), kThreads, 0, stream>>>(q);
     } else if (wide && q.block_rows == 1 && q.block_cols == 32) {
         const int64_t units = ((q.rows + 7) / 8) * (q.cols / 8);
         // round the grid so each warp's 32 units stay inside one launch slot
