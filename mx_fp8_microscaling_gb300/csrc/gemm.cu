@@ -95,6 +95,9 @@ struct KParams {
     int64_t sfb_batch_tiles;
     int group_m;
     uint32_t idesc;
+    uint32_t idesc_half;  // the same MMA with N = 128 (split tail tiles of the pair kernel)
+    int full_rounds;      // pair kernel: rounds of whole tiles before a split tail round
+    int split_tail;       // 1: the last round's tiles run as two 256 x 128 halves each
     uint64_t timeout_ns;
     int skip_producer;   // fault injection: never issue loads (waits must time out)
 };
@@ -113,6 +116,29 @@ __device__ __forceinline__ void tile_coords(int t, const KParams& p, int& b, int
     const int idx = t - g * group;
     mt = first_m + idx % gm;
     nt = idx / gm;
+}
+
+// Work units of the pair kernel's cluster `c` (of `nc`).  Whole 256 x 256
+// tiles round-robin over the clusters; when the last round would leave most
+// clusters idle (its tiles fit in half of them), each of its tiles runs as
+// two 256 x 128 halves on two clusters instead, halving the tail.
+__device__ __forceinline__ int pair_units(const KParams& p, int c, int nc) {
+    if (p.split_tail) return p.full_rounds + (c < 2 * (p.batch * p.num_m_tiles * p.num_n_tiles - p.full_rounds * nc));
+    const int tiles = p.batch * p.num_m_tiles * p.num_n_tiles;
+    return c < tiles ? (tiles - c + nc - 1) / nc : 0;
+}
+// half: -1 for a whole tile, else which 128-column half
+__device__ __forceinline__ void pair_unit_coords(int u, const KParams& p, int c, int nc, int& b, int& mt, int& nt,
+                                                 int& half) {
+    int t;
+    if (!p.split_tail || u < p.full_rounds) {
+        t = c + u * nc;
+        half = -1;
+    } else {
+        t = p.full_rounds * nc + (c >> 1);
+        half = c & 1;
+    }
+    tile_coords(t, p, b, mt, nt);
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -543,24 +569,27 @@ __global__ void __launch_bounds__(sm2::THREADS, 1)
     cluster_sync_all();  // the peer's barriers are initialised before any remote use
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    const int num_tiles = p.batch * p.num_m_tiles * p.num_n_tiles;  // pair tiles
+    const int num_units = pair_units(p, cluster, num_clusters);
 
     if (warp == 0) {
         if (lane == 0 && !p.skip_producer) {
             int stage = 0, gslot = 0;
             uint32_t phase = 0, gphase = 0;
             bool ok = true;
-            for (int t = cluster; t < num_tiles && ok; t += num_clusters) {
-                int b, mt, nt;
-                tile_coords(t, p, b, mt, nt);
+            for (int u = 0; u < num_units && ok; ++u) {
+                int b, mt, nt, hf;
+                pair_unit_coords(u, p, cluster, num_clusters, b, mt, nt, hf);
                 const int a_row = mt * BM + static_cast<int>(rank) * 128;
-                const int b_row = nt * BN + static_cast<int>(rank) * 128;
+                // a half tile's 128 B rows split 64 / 64 over the pair (the
+                // 128-row box brings 64 rows more, which no MMA reads)
+                const int b_row = hf < 0 ? nt * BN + static_cast<int>(rank) * 128
+                                         : nt * BN + hf * 128 + static_cast<int>(rank) * 64;
                 // scale tiles past this problem's last one belong to rows past
                 // M / N (the next problem's tiles, or zeros past the buffer):
                 // their products land in rows the epilogue never stores
                 const int64_t sfa_tile = b * p.sfa_batch_tiles + (2 * mt + static_cast<int>(rank)) * p.sf_ntk;
-                const int64_t sfb_tile0 = b * p.sfb_batch_tiles + (2 * nt) * p.sf_ntk;
-                const int64_t sfb_tile1 = sfb_tile0 + p.sf_ntk;
+                const int64_t sfb_tile0 = b * p.sfb_batch_tiles + (2 * nt + (hf < 0 ? 0 : hf)) * p.sf_ntk;
+                const int64_t sfb_tile1 = hf < 0 ? sfb_tile0 + p.sf_ntk : sfb_tile0;
                 for (int kb = 0; kb < p.num_kb; ++kb) {
                     const bool group_start = kb % SF_GROUP == 0;
                     // a scale slot is free once its last group's copies into
@@ -633,7 +662,9 @@ __global__ void __launch_bounds__(sm2::THREADS, 1)
             int stage = 0;
             uint32_t phase = 0, acc_phase = 0;
             bool ok = true;
-            for (int t = cluster; t < num_tiles && ok; t += num_clusters) {
+            for (int u = 0; u < num_units && ok; ++u) {
+                const bool half_tile = p.split_tail && u >= p.full_rounds;
+                const uint32_t unit_idesc = half_tile ? p.idesc_half : p.idesc;
                 if (!mbar_wait_bounded(tmem_empty, acc_phase ^ 1u, abort_flag, p.timeout_ns, &g_mx_status)) break;
                 tc_fence_after();
                 for (int kb = 0; kb < p.num_kb; ++kb) {
@@ -654,13 +685,13 @@ __global__ void __launch_bounds__(sm2::THREADS, 1)
                             if (kk >= kk_end) break;
                             const uint32_t id = 2u * static_cast<uint32_t>(kk & 1);
                             tc_mma_mxf4_pair(tmem_base, sdesc_kmajor_sw128(sa + kk * 32),
-                                             sdesc_kmajor_sw128(sbb + kk * 32), p.idesc | (id << 4) | (id << 29),
+                                             sdesc_kmajor_sw128(sbb + kk * 32), unit_idesc | (id << 4) | (id << 29),
                                              sf_t + 4u * (kk >> 1), sf_t + 8u + 8u * (kk >> 1), (kb | kk) != 0);
                         }
                     } else {
 #pragma unroll
                         for (int kk = 0; kk < BK / 32; ++kk) {
-                            const uint32_t idesc = p.idesc | (static_cast<uint32_t>(kk) << 4) |
+                            const uint32_t idesc = unit_idesc | (static_cast<uint32_t>(kk) << 4) |
                                                    (static_cast<uint32_t>(kk) << 29);
                             tc_mma_mxf8_pair(tmem_base, sdesc_kmajor_sw128(sa + kk * 32),
                                              sdesc_kmajor_sw128(sbb + kk * 32), idesc, sf_t, sf_t + 4u,
@@ -690,7 +721,7 @@ __global__ void __launch_bounds__(sm2::THREADS, 1)
             int stage = 0, gslot = 0;
             uint32_t phase = 0, gphase = 0;
             bool ok = true;
-            for (int t = cluster; t < num_tiles && ok; t += num_clusters) {
+            for (int u = 0; u < num_units && ok; ++u) {
                 for (int kb = 0; kb < p.num_kb; ++kb) {
                     const int j = kb % SF_GROUP;
                     // a group's scales: on their own barrier, or (one-stage
@@ -747,24 +778,30 @@ __global__ void __launch_bounds__(sm2::THREADS, 1)
         const int half = (warp - 2) >> 2;
         const uint32_t tmem_empty_rank0 = mapa_shared(tmem_empty, 0);
         uint32_t acc_phase = 0;
-        for (int t = cluster; t < num_tiles; t += num_clusters) {
-            int b, mt, nt;
-            tile_coords(t, p, b, mt, nt);
+        for (int u = 0; u < num_units; ++u) {
+            int b, mt, nt, hf;
+            pair_unit_coords(u, p, cluster, num_clusters, b, mt, nt, hf);
             bool ok = true;
             if (lane == 0) ok = mbar_wait_bounded(tmem_full, acc_phase, abort_flag, p.timeout_ns, &g_mx_status);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             tc_fence_after();
+            // a half tile's accumulator is columns 0..127: the second half's
+            // warps only release
+            const bool live = hf < 0 || half == 0;
             uint32_t v[4][32];
-            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + half * 128;
-            tmem_ld_32x32b_x128(taddr, v);
-            tmem_wait_ld();
+            if (live) {
+                const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + half * 128;
+                tmem_ld_32x32b_x128(taddr, v);
+                tmem_wait_ld();
+            }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(tmem_empty_rank0);
             acc_phase ^= 1u;
-            store_row128(p, b, static_cast<int64_t>(mt) * BM + rank * 128 + quarter * 32 + lane,
-                         static_cast<int64_t>(nt) * BN + half * 128, v);
+            if (live)
+                store_row128(p, b, static_cast<int64_t>(mt) * BM + rank * 128 + quarter * 32 + lane,
+                             static_cast<int64_t>(nt) * BN + (hf < 0 ? half : hf) * 128, v);
         }
     }
 
@@ -938,7 +975,14 @@ cudaError_t launch_2sm(const GemmArgs& g, cudaStream_t stream) {
     KParams p = base_params(g, sm2::BM, sm2::BN);
     const int tiles = p.batch * p.num_m_tiles * p.num_n_tiles;
     const int cap = max_pair_clusters<FP4>();
-    const int clusters = tiles < cap ? tiles : cap;
+    // split the last round's tiles into 128-column halves when they fit in
+    // half the clusters (a tail of R < cap / 2 tiles then takes half as long)
+    const int full_rounds = tiles / cap, tail = tiles - full_rounds * cap;
+    p.split_tail = (tail > 0 && 2 * tail <= cap) ? 1 : 0;
+    p.full_rounds = full_rounds;
+    p.idesc_half = make_idesc_mxf8(g.elem_fmt, g.elem_fmt, sm2::BM, sm2::BN / 2);
+    if (is_fp4(g)) p.idesc_half = make_idesc_mxf4(sm2::BM, sm2::BN / 2);
+    const int clusters = p.split_tail ? (full_rounds > 0 ? cap : 2 * tail) : (tiles < cap ? tiles : cap);
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[1];
     pair_launch_config(&cfg, attr, clusters, FP4, stream);

@@ -65,6 +65,22 @@ def test_matmul_matches_oracle(mx, variant, fmt, out_dtype, M, N, K):
     check_gemm(c, c_ref, s_ref, out_dtype, TOL)
 
 
+@pytest.mark.parametrize("out_dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("M,N,K", [(2560, 2048, 256), (512, 1024, 256), (256, 200, 64), (768, 640, 384)])
+def test_matmul_split_tail_round(mx, out_dtype, M, N, K):
+    # the pair kernel runs a last round that fits in half the clusters as
+    # 256 x 128 half tiles (80 tiles on 74-76 clusters; few-tile problems run
+    # entirely as halves): every element against the oracle
+    mx.mx_debug_set_gemm_variant(2)
+    try:
+        a, bt, sa, sb = _random_operands(M, N, K, "e4m3fn", seed=M + N + K)
+        c = _gpu_matmul(mx, a, bt, sa, sb, "e4m3fn", out_dtype)
+    finally:
+        mx.mx_debug_set_gemm_variant(0)
+    c_ref, s_ref = orc.scaled_matmul(a, bt, sa, sb, "e4m3fn")
+    check_gemm(c, c_ref, s_ref, out_dtype, TOL)
+
+
 @pytest.mark.parametrize("fmt", ["e4m3fn", "e5m2"])
 def test_matmul_sf_layout_scales(mx, variant, fmt):
     M, N, K = 256, 512, 384
