@@ -488,6 +488,38 @@ def vendor_gemm_reference(torch, g, steps):
         return {"unavailable": f"{type(e).__name__}: {str(e)[:160]}"}
 
 
+def vendor_fp4_reference(torch, g, steps):
+    """cuBLASLt's FP4 GEMM at the same size for context.  torch._scaled_mm
+    offers block-scaled FP4 only as NVFP4 (16-element blocks, e4m3 scales),
+    so this times that format on the same packed e2m1 operands with unit
+    scales, alternating with this library's MXFP4 GEMM: a comparison of the
+    FP4 tensor-core rate, not of the same arithmetic."""
+    try:
+        n = GEMM_N
+        a4 = g.qa.view(n, n // 2).view(torch.float4_e2m1fn_x2)
+        b4 = g.qb.view(n, n // 2).view(torch.float4_e2m1fn_x2)
+        s4 = torch.full((n * n // 16,), 0x38, dtype=torch.uint8, device="cuda").view(torch.float8_e4m3fn)
+        ours = g.ops[4][1]
+        times = {"ours_mxfp4": [], "cublaslt_nvfp4": []}
+        for it in range(3 + steps):
+            for which in times:
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                if which == "ours_mxfp4":
+                    ours()
+                else:
+                    torch._scaled_mm(a4, b4.t(), s4, s4, out_dtype=torch.bfloat16)
+                e1.record()
+                torch.cuda.synchronize()
+                if it >= 3:
+                    times[which].append(e0.elapsed_time(e1))
+        out = {k: round(GEMM_FLOP / (statistics.median(v) * 1e-3) / 1e12, 1) for k, v in times.items()}
+        return {"tflops": out, "what": "8192^3 -> bf16 on the same packed e2m1 operands; cuBLASLt runs NVFP4 "
+                                      "(1x16 blocks, e4m3 scales: the only block-scaled FP4 form torch exposes)"}
+    except Exception as e:
+        return {"unavailable": f"{type(e).__name__}: {str(e)[:160]}"}
+
+
 # ------------------------------------------------------------- CPU oracle
 
 def oracle_sweep_sample(rows=2048, repeats=1):
@@ -744,6 +776,7 @@ def main():
             "roofline": {"bound": "tensor", "kernel": "mx_gemm_2sm_kernel<true>", "achieved": round(tf, 1),
                          "peak": round(peak_fp4, 1), "unit": "TFLOP/s", "frac": round(tf / peak_fp4, 4),
                          "peak_source": f"{peaks['src']} bf16 burst x {FP4_OVER_BF16} (nominal FP4/bf16)"}}
+        line["scaled_matmul_fp4"]["vendor_reference"] = vendor_fp4_reference(torch, parts["gemm_fp4"], args.steps)
     if "dot" in parts:
         peak_fp8 = peaks["bf16"] * FP8_OVER_BF16
         cases = {}
