@@ -58,6 +58,8 @@ GEMM_FLOP = 2 * GEMM_N ** 3
 FUSED = (16384, 28672, 8192)
 FUSED_FLOP = 2 * FUSED[0] * FUSED[1] * FUSED[2]
 DOT = (16, 2048, 2048, 2048)  # batch, M, N, K
+SMALL_M = (16, 64, 128)       # M of M x 8192 x 8192 ScaledMatmuls (HBM-bound: one pass over B)
+SMALL_M_COPIES = 4            # B copies rotated so every call reads B from HBM (4 x 64 MiB > L2)
 DOT_FLOP = 2 * DOT[0] * DOT[1] * DOT[2] * DOT[3]
 # nominal dense MXFP8 : bf16 and FP4 : bf16 tensor ratios (4.5 and 13.5 : 2.25 PFLOP/s)
 FP8_OVER_BF16 = 2.0
@@ -452,6 +454,109 @@ class Dot:
             timer.run(label, fn)
 
 
+class GemmSmallM:
+    """ScaledMatmul with few rows: M in SMALL_M, N = K = 8192, e4m3fn ->
+    bf16 with SF-layout scales.  The kernel streams B once, so HBM bounds
+    it.  B rotates over SMALL_M_COPIES copies (256 MiB, larger than L2); each
+    shape's 4 calls (one per copy) run as one CUDA graph, since host launch
+    cost is comparable to these ~17-20 us kernels.  A holds the first M rows
+    of one quantized [128, 8192] operand."""
+
+    def __init__(self, torch, mx, api):
+        n = GEMM_N
+        a_bits, b_bits = syn.gemm_operands(max(SMALL_M), n, n, seed=0)
+        a = dev_bits(torch, a_bits, "bf16")
+        b = dev_bits(torch, b_bits, "bf16")
+        del a_bits, b_bits
+        qa, sa = mx.mx_quantize(a, "e4m3fn", geometry="1x32", dim=-1)
+        qb, sfb = mx.mx_quantize(b, "e4m3fn", geometry="1x32", dim=-1, scale_layout="sf")
+        del a, b
+        self.qb = [qb] + [qb.clone() for _ in range(SMALL_M_COPIES - 1)]
+        self.sfb = sfb
+        self.a = {}
+        for m in SMALL_M:
+            sfa = torch.empty(mx.mx_sf_layout_bytes(m, n), dtype=torch.uint8, device="cuda")
+            mx.mx_repack_scales(sa.view(max(SMALL_M), n // 32)[:m], n, out=sfa)
+            self.a[m] = (qa.view(max(SMALL_M), n)[:m], sfa, torch.empty((m, n), dtype=torch.bfloat16,
+                                                                         device="cuda"))
+        torch.cuda.synchronize()
+        self.split = {}
+        self.graphs = {}
+        for m in SMALL_M:
+            qa_m, sfa, c = self.a[m]
+
+            def calls(qa_m=qa_m, sfa=sfa, c=c):
+                for qb_i in self.qb:
+                    mx.mx_scaled_matmul(qa_m, qb_i, sfa, self.sfb, "e4m3fn", "bf16", scales_are_sf_layout=True,
+                                        out=c)
+            self.graphs[m] = capture_graph(torch, calls)
+            self.split[m] = mx.mx_debug_last_gemm_launch()[1]
+        self.launches = SMALL_M_COPIES * len(SMALL_M)
+
+    def bytes_per_call(self, m):
+        n = GEMM_N
+        return n * n + m * n + sf_layout_bytes(n, n) + sf_layout_bytes(m, n) + 2 * m * n
+
+    def step(self, timer):
+        for m in SMALL_M:
+            timer.run(f"small_m_{m}", self.graphs[m].replay)
+
+
+def sf_layout_bytes(rows, k):
+    """Bytes of an SF-layout scale tensor: 512-byte tiles of 128 rows x 4
+    scale columns (four 32-element blocks)."""
+    return -(-rows // 128) * -(-(k // 32) // 4) * 512
+
+
+def capture_graph(torch, fn):
+    """fn() once on a side stream (warm-up: attributes, cached queries), then
+    captured into a CUDA graph."""
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        fn()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        fn()
+    torch.cuda.synchronize()
+    return graph
+
+
+def vendor_small_m_reference(torch, g, steps):
+    """cuBLASLt's block-scaled FP8 GEMM (torch._scaled_mm) on the same
+    operands, scales and B rotation, also as one CUDA graph per shape, timed
+    after the main loop: a comparison point, not part of the timed step."""
+    try:
+        out = {}
+        for m in SMALL_M:
+            qa_m, sfa, _ = g.a[m]
+            a8 = qa_m.view(torch.float8_e4m3fn)
+            sa8 = sfa.view(torch.float8_e8m0fnu)
+            sb8 = g.sfb.view(torch.float8_e8m0fnu)
+
+            def calls(a8=a8, sa8=sa8):
+                for qb_i in g.qb:
+                    torch._scaled_mm(a8, qb_i.view(torch.float8_e4m3fn).t(), sa8, sb8, out_dtype=torch.bfloat16)
+            graph = capture_graph(torch, calls)
+            ts = {"ours": [], "cublaslt": []}
+            for it in range(3 + steps):
+                for which, gr in (("ours", g.graphs[m]), ("cublaslt", graph)):
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record()
+                    gr.replay()
+                    e1.record()
+                    torch.cuda.synchronize()
+                    if it >= 3:
+                        ts[which].append(e0.elapsed_time(e1) * 1e3 / SMALL_M_COPIES)
+            out[str(m)] = {k: round(statistics.median(v), 2) for k, v in ts.items()}
+        return {"us_per_call": out, "what": f"M x 8192 x 8192 e4m3fn -> bf16, B rotated over {SMALL_M_COPIES} "
+                                            f"copies, CUDA graphs, median of {steps}; cuBLASLt via torch._scaled_mm"}
+    except Exception as e:
+        return {"unavailable": f"{type(e).__name__}: {str(e)[:160]}"}
+
+
 def vendor_gemm_reference(torch, g, steps):
     """cuBLASLt's block-scaled FP8 GEMM (torch._scaled_mm with E8M0 scales in
     the same tensor-core layout) on the same e4m3fn operands and scales as
@@ -631,7 +736,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="mx", choices=["mx", "reference"])
     ap.add_argument("--workload", default="all",
-                    choices=["all", "sweep", "gemm", "fp4", "fused", "dequant", "dot", "gemm_fp4"])
+                    choices=["all", "sweep", "gemm", "fp4", "fused", "dequant", "dot", "gemm_fp4", "gemm_small_m"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--reference-rows", type=int, default=1024,
                     help="rows of each [rows, 8192] sweep slice the reference arm quantizes per step")
@@ -649,10 +754,10 @@ def main():
 
     peaks = load_peaks()
     parts = {}
-    want = (["sweep", "gemm", "fp4", "dequant", "fused", "dot", "gemm_fp4"] if args.workload == "all"
+    want = (["sweep", "gemm", "fp4", "dequant", "fused", "dot", "gemm_fp4", "gemm_small_m"] if args.workload == "all"
             else [args.workload])
     builders = {"sweep": Sweep, "gemm": Gemm, "fp4": Fp4, "dequant": Dequant, "fused": Fused, "dot": Dot,
-                "gemm_fp4": GemmFp4}
+                "gemm_fp4": GemmFp4, "gemm_small_m": GemmSmallM}
     api = Api(torch, mx)
     for name in want:
         parts[name] = builders[name](torch, mx, api)
@@ -777,6 +882,23 @@ def main():
                          "peak": round(peak_fp4, 1), "unit": "TFLOP/s", "frac": round(tf / peak_fp4, 4),
                          "peak_source": f"{peaks['src']} bf16 burst x {FP4_OVER_BF16} (nominal FP4/bf16)"}}
         line["scaled_matmul_fp4"]["vendor_reference"] = vendor_fp4_reference(torch, parts["gemm_fp4"], args.steps)
+    if "gemm_small_m" in parts:
+        sm = parts["gemm_small_m"]
+        cases = {}
+        for m in SMALL_M:
+            us = timer.avg_ms(f"small_m_{m}") * 1e3 / SMALL_M_COPIES
+            gbs = sm.bytes_per_call(m) / (us * 1e-6) / 1e9
+            cases[str(m)] = {"us": round(us, 2), "gbs": round(gbs, 1), "frac": round(gbs / peaks["hbm"], 4),
+                             "split_k": sm.split[m]}
+        top = cases[str(max(SMALL_M))]
+        line["scaled_matmul_small_m"] = {
+            "unit": "GB/s", "config": f"M x 8192 x 8192, M in {list(SMALL_M)}, e4m3fn -> bf16, SF-layout scales; "
+                                      f"B rotated over {SMALL_M_COPIES} copies (256 MiB > L2); CUDA graphs",
+            "cases": cases,
+            "roofline": {"bound": "hbm", "kernel": "mx_gemm_kernel (split-K)", "achieved": top["gbs"],
+                         "peak": peaks["hbm"], "unit": "GB/s", "frac": top["frac"], "peak_source": peaks["src"],
+                         "traffic": None, "note": f"M = {max(SMALL_M)}; bytes = B + A + both scale tensors + C"}}
+        line["scaled_matmul_small_m"]["vendor_reference"] = vendor_small_m_reference(torch, sm, args.steps)
     if "dot" in parts:
         peak_fp8 = peaks["bf16"] * FP8_OVER_BF16
         cases = {}

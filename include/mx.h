@@ -436,10 +436,23 @@ mx_status mx_debug_gemm_fault_injection(int skip_producer, uint64_t timeout_ns);
 /*
  * Testing hook (no counterpart on the pages): which ScaledMatmul kernel later
  * calls use.  0 = automatic (the 2-SM pair kernel when M > 128, else the
- * 1-SM kernel), 1 = always the 1-SM kernel, 2 = always the pair kernel.
- * Both give results within the same tolerance.  Not thread-safe; host only.
+ * 1-SM kernel), 1 = always the 1-SM kernel, 2 = always the pair kernel,
+ * 3 = always the 1-SM kernel and never split K.  The 1-SM kernel splits K
+ * over a cluster of up to 8 CTAs per tile when the problem has too few
+ * tiles to fill the GPU (small M); the slices' f32 partial sums are added in
+ * slice order, so a given shape always gives the same bits.  All variants
+ * give results within the same tolerance.  Returns MX_ERR_INVALID_ARG for
+ * other values.  Not thread-safe; host only.
  */
 mx_status mx_debug_set_gemm_variant(int variant);
+
+/*
+ * Testing hook (no counterpart on the pages): the kernel of the last
+ * ScaledMatmul launch made by this process (*kernel: 1 = 1-SM, 2 = pair,
+ * 0 = none yet) and its split-K factor (*split_k: CTAs per tile along K, 1 =
+ * no split).  MX_ERR_INVALID_ARG if a pointer is NULL.  Host only.
+ */
+mx_status mx_debug_last_gemm_launch(int* kernel, int* split_k);
 
 #ifdef __cplusplus
 }

@@ -27,6 +27,7 @@ LIB_PATH = os.path.join(_PKG, "_build", "libmx.so")
 
 # enum values of include/mx.h
 MX_OK = 0
+MX_ERR_INVALID_ARG = 1
 MX_ERR_TIMEOUT = 9
 DTYPES = {"bf16": 1, "f16": 2, "f32": 3, "e4m3fn": 4, "e5m2": 5, "e2m1": 6, "e8m0": 7}
 GEOMETRIES = {"8x4": 0, "1x32": 1}
@@ -97,6 +98,7 @@ def _load():
         "mx_version": [],
         "mx_debug_gemm_fault_injection": [I, ctypes.c_uint64],
         "mx_debug_set_gemm_variant": [I],
+        "mx_debug_last_gemm_launch": [P, P],
     }
     for name, args in sigs.items():
         fn = getattr(lib, name)
@@ -462,8 +464,17 @@ def mx_debug_gemm_fault_injection(skip_producer: bool, timeout_ns: int = 0):
 
 
 def mx_debug_set_gemm_variant(variant: int):
-    """0 automatic, 1 force the 1-SM ScaledMatmul kernel, 2 force the 2-SM pair kernel."""
+    """0 automatic, 1 force the 1-SM ScaledMatmul kernel, 2 force the 2-SM pair
+    kernel, 3 force the 1-SM kernel without split-K."""
     _check(_lib.mx_debug_set_gemm_variant(int(variant)), "mx_debug_set_gemm_variant")
+
+
+def mx_debug_last_gemm_launch():
+    """(kernel, split_k) of the last ScaledMatmul launch: kernel 1 = 1-SM,
+    2 = pair, 0 = none yet; split_k = CTAs per tile along K."""
+    kernel, split = ctypes.c_int(0), ctypes.c_int(0)
+    _check(_lib.mx_debug_last_gemm_launch(ctypes.byref(kernel), ctypes.byref(split)), "mx_debug_last_gemm_launch")
+    return kernel.value, split.value
 
 
 def raw_library() -> ctypes.CDLL:

@@ -34,6 +34,13 @@
 //
 //   mx_gemm_kernel      1 SM per 128 x 256 tile (M = 128 MMA), 4 stages of
 //                       A 16 KB + B 32 KB + scales 1.5 KB.  Used for M <= 128.
+//                       When the tiles are too few to fill the GPU it splits K:
+//                       a cluster of S <= 8 CTAs per tile, CTA s accumulating
+//                       the s-th slice of the K stages; each slice's f32 tile
+//                       goes to its CTA's drained stage buffers, and the
+//                       cluster sums the S partials chunk by chunk in slice
+//                       order through distributed shared memory (the same
+//                       bits on every run) and stores C.
 //   mx_gemm_2sm_kernel  a cluster of 2 CTAs per 256 x 256 tile with the pair
 //                       MMA (cta_group::2, M = 256): each CTA loads its own
 //                       128 rows of A and 128 rows of B, so each SM takes in
@@ -98,6 +105,7 @@ struct KParams {
     uint32_t idesc_half;  // the same MMA with N = 128 (split tail tiles of the pair kernel)
     int full_rounds;      // pair kernel: rounds of whole tiles before a split tail round
     int split_tail;       // 1: the last round's tiles run as two 256 x 128 halves each
+    int split_k;          // 1-SM kernel: CTAs (one cluster) per tile, each a slice of K; 1 = none
     uint64_t timeout_ns;
     int skip_producer;   // fault injection: never issue loads (waits must time out)
 };
@@ -140,6 +148,31 @@ __device__ __forceinline__ void pair_unit_coords(int u, const KParams& p, int c,
     }
     tile_coords(t, p, b, mt, nt);
 }
+
+// Work of one 1-SM CTA.  Without split-K: tiles blockIdx.x, + gridDim.x, ...
+// over all of K.  With split-K (p.split_k = S > 1, clusters of S CTAs, grid
+// = tiles x S): the one tile blockIdx.x / S, K stages [s num_kb / S,
+// (s + 1) num_kb / S) for cluster rank s.
+struct Sm1Work {
+    int first, step, kb0, kb1;
+};
+__device__ __forceinline__ Sm1Work sm1_work(const KParams& p, int num_tiles) {
+    if (p.split_k > 1) {
+        const int s = static_cast<int>(blockIdx.x) % p.split_k;
+        return {static_cast<int>(blockIdx.x) / p.split_k, num_tiles, s * p.num_kb / p.split_k,
+                (s + 1) * p.num_kb / p.split_k};
+    }
+    return {static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x), 0, p.num_kb};
+}
+
+// Split-K partial tile in shared memory: 128 rows of 1024 bytes (256 f32);
+// the 16-byte chunk j of row r sits in slot j ^ (r & 7), so 8 consecutive
+// rows writing the same chunk, or one row's 8 consecutive chunks, hit 8
+// different 16-byte bank groups.
+__device__ __forceinline__ uint32_t partial_off(int r, int j) {
+    return static_cast<uint32_t>(r) * 1024u + (static_cast<uint32_t>(j ^ (r & 7)) << 4);
+}
+constexpr int kMaxSplitK = 8;  // CTAs per split-K cluster (the portable cluster size)
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     uint32_t r;
@@ -226,6 +259,31 @@ __device__ __forceinline__ void store_row128(const KParams& p, int b, int64_t m,
     }
 }
 
+// Store C[m, n .. n + 3] of problem b (columns past N skipped).
+__device__ __forceinline__ void store_chunk4(const KParams& p, int b, int64_t m, int64_t n, float4 x) {
+    const int64_t row = static_cast<int64_t>(b) * p.c_batch_stride + m * p.ldc + n;
+    const float e[4] = {x.x, x.y, x.z, x.w};
+    if (p.out_bf16) {
+        uint16_t* c = reinterpret_cast<uint16_t*>(p.c) + row;
+        if (p.vec_store && n + 4 <= p.N) {
+            *reinterpret_cast<uint2*>(c) = make_uint2(pack_bf16x2(e[0], e[1]), pack_bf16x2(e[2], e[3]));
+        } else {
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                if (n + i < p.N) c[i] = static_cast<uint16_t>(pack_bf16x2(e[i], 0.0f) & 0xFFFFu);
+        }
+    } else {
+        float* c = reinterpret_cast<float*>(p.c) + row;
+        if (p.vec_store && n + 4 <= p.N) {
+            *reinterpret_cast<float4*>(c) = x;
+        } else {
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                if (n + i < p.N) c[i] = e[i];
+        }
+    }
+}
+
 // ====================================================== 1-SM, 128 x 256 tiles
 
 namespace sm1 {
@@ -296,20 +354,21 @@ __global__ void __launch_bounds__(sm1::THREADS, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     const int num_tiles = p.batch * p.num_m_tiles * p.num_n_tiles;
+    const Sm1Work work = sm1_work(p, num_tiles);
 
     if (warp == 0) {
         if (lane == 0 && !p.skip_producer) {
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+            for (int t = work.first; t < num_tiles && ok; t += work.step) {
                 int b, mt, nt;
                 tile_coords(t, p, b, mt, nt);
                 const int nsf0 = 2 * nt;
                 const int nsf1 = (2 * nt + 1 < p.num_sf_n_tiles) ? 2 * nt + 1 : 2 * nt;
                 const uint8_t* sfa = p.sfa + static_cast<size_t>(b) * p.sfa_batch_tiles * 512u;
                 const uint8_t* sfb = p.sfb + static_cast<size_t>(b) * p.sfb_batch_tiles * 512u;
-                for (int kb = 0; kb < p.num_kb; ++kb) {
+                for (int kb = work.kb0; kb < work.kb1; ++kb) {
                     if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, p.timeout_ns, &g_mx_status)) {
                         ok = false;
                         break;
@@ -351,10 +410,11 @@ __global__ void __launch_bounds__(sm1::THREADS, 1)
             int stage = 0;
             uint32_t phase = 0, acc_phase = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+            for (int t = work.first; t < num_tiles && ok; t += work.step) {
                 if (!mbar_wait_bounded(tmem_empty, acc_phase ^ 1u, abort_flag, p.timeout_ns, &g_mx_status)) break;
                 tc_fence_after();
-                for (int kb = 0; kb < p.num_kb; ++kb) {
+                for (int kb = work.kb0; kb < work.kb1; ++kb) {
+                    const bool first_kb = kb == work.kb0;
                     if (!mbar_wait_bounded(sf_full_bar(stage), phase, abort_flag, p.timeout_ns, &g_mx_status)) {
                         ok = false;
                         break;
@@ -373,7 +433,7 @@ __global__ void __launch_bounds__(sm1::THREADS, 1)
                             const uint32_t id = 2u * static_cast<uint32_t>(kk & 1);
                             tc_mma_mxf4(tmem_base, sdesc_kmajor_sw128(sa + kk * 32),
                                         sdesc_kmajor_sw128(sbb + kk * 32), p.idesc | (id << 4) | (id << 29),
-                                        sf_t + 4u * (kk >> 1), sf_t + 8u + 8u * (kk >> 1), (kb | kk) != 0);
+                                        sf_t + 4u * (kk >> 1), sf_t + 8u + 8u * (kk >> 1), !first_kb || kk != 0);
                         }
                     } else {
 #pragma unroll
@@ -381,7 +441,8 @@ __global__ void __launch_bounds__(sm1::THREADS, 1)
                             const uint32_t idesc = p.idesc | (static_cast<uint32_t>(kk) << 4) |
                                                    (static_cast<uint32_t>(kk) << 29);
                             tc_mma_mxf8(tmem_base, sdesc_kmajor_sw128(sa + kk * 32),
-                                        sdesc_kmajor_sw128(sbb + kk * 32), idesc, sf_t, sf_t + 4u, (kb | kk) != 0);
+                                        sdesc_kmajor_sw128(sbb + kk * 32), idesc, sf_t, sf_t + 4u,
+                                        !first_kb || kk != 0);
                         }
                     }
                     tc_commit(empty_bar(stage));
@@ -405,8 +466,8 @@ __global__ void __launch_bounds__(sm1::THREADS, 1)
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-                for (int kb = 0; kb < p.num_kb; ++kb) {
+            for (int t = work.first; t < num_tiles && ok; t += work.step) {
+                for (int kb = work.kb0; kb < work.kb1; ++kb) {
                     if (!mbar_wait_bounded(full_bar(stage), phase, abort_flag, p.timeout_ns, &g_mx_status)) {
                         ok = false;
                         break;
@@ -444,7 +505,7 @@ __global__ void __launch_bounds__(sm1::THREADS, 1)
         const int quarter = warp & 3;          // TMEM lanes this warp may access
         const int half = (warp - 2) >> 2;      // accumulator columns [128*half, +128)
         uint32_t acc_phase = 0;
-        for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+        for (int t = work.first; t < num_tiles; t += work.step) {
             int b, mt, nt;
             tile_coords(t, p, b, mt, nt);
             // one lane waits; the warp follows its verdict so it never diverges
@@ -453,21 +514,80 @@ __global__ void __launch_bounds__(sm1::THREADS, 1)
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             tc_fence_after();
+            const int row = quarter * 32 + lane;
+            const int64_t m = static_cast<int64_t>(mt) * BM + row;
+            const int64_t n0 = static_cast<int64_t>(nt) * BN + half * 128;
+            // a warp whose 32 rows or 128 columns all lie outside C stores nothing
+            // (it still loads: skipping the load costs registers)
+            const bool live = static_cast<int64_t>(mt) * BM + quarter * 32 < p.M && n0 < p.N;
             uint32_t v[4][32];
-            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + half * 128;
-            tmem_ld_32x32b_x128(taddr, v);
-            tmem_wait_ld();
+            {
+                const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + half * 128;
+                tmem_ld_32x32b_x128(taddr, v);
+                tmem_wait_ld();
+            }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(tmem_empty);
             acc_phase ^= 1u;
-            store_row128(p, b, static_cast<int64_t>(mt) * BM + quarter * 32 + lane,
-                         static_cast<int64_t>(nt) * BN + half * 128, v);
+            if (!live) continue;
+            if (p.split_k > 1) {
+                // this slice's partial sums go into the drained operand stages
+                // for the cluster to reduce
+                fence_proxy_async_smem();
+                if (m < p.M) {
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) {
+                        const uint32_t* x = &v[c >> 3][4 * (c & 7)];
+                        st_shared_v4(sb + OFF_A + partial_off(row, half * 32 + c), x[0], x[1], x[2], x[3]);
+                    }
+                }
+            } else {
+                store_row128(p, b, m, n0, v);
+            }
         }
     }
 
     tc_fence_before();
     __syncthreads();
+    if (p.split_k > 1) {
+        // Split-K reduction: each CTA of the cluster takes a share of the
+        // tile's 4-column chunks, sums the S partials in slice order (so the
+        // result does not depend on timing) and stores C.
+        cluster_sync_all();  // all partials written and visible cluster-wide
+        const int S = p.split_k;
+        const int s = static_cast<int>(cluster_ctarank());
+        int b, mt, nt;
+        tile_coords(work.first, p, b, mt, nt);
+        const int rows = min(BM, p.M - mt * BM);
+        const int chunks = (min(BN, p.N - nt * BN) + 3) / 4;  // per row
+        const int total = rows * chunks;
+        const int e_end = (s + 1) * total / S;
+        for (int e = s * total / S + static_cast<int>(threadIdx.x); e < e_end; e += blockDim.x) {
+            const int r = e / chunks, j = e - r * chunks;
+            const float4* own = reinterpret_cast<const float4*>(generic_shared(sb + OFF_A + partial_off(r, j)));
+            float4 acc = *map_cluster(own, 0);
+            // CTA q's partial, through the cluster window, 4 loads in flight
+#pragma unroll
+            for (int q0 = 1; q0 < kMaxSplitK; q0 += 4) {
+                float4 x[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    if (q0 + i < S) x[i] = *map_cluster(own, q0 + i);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    if (q0 + i < S) {
+                        acc.x += x[i].x;
+                        acc.y += x[i].y;
+                        acc.z += x[i].z;
+                        acc.w += x[i].w;
+                    }
+                }
+            }
+            store_chunk4(p, b, static_cast<int64_t>(mt) * BM + r, static_cast<int64_t>(nt) * BN + 4 * j, acc);
+        }
+        cluster_sync_all();  // no CTA leaves while another may still read its partial
+    }
     tc_fence_after();
     if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
 }
@@ -790,7 +910,7 @@ __global__ void __launch_bounds__(sm2::THREADS, 1)
             // warps only release
             const bool live = hf < 0 || half == 0;
             uint32_t v[4][32];
-            if (live) {
+            {
                 const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + half * 128;
                 tmem_ld_32x32b_x128(taddr, v);
                 tmem_wait_ld();
@@ -863,7 +983,10 @@ bool make_sf_map(CUtensorMap* map, const void* base, int64_t tiles, uint32_t box
 
 uint64_t g_timeout_ns = 2000000000ull;
 int g_fault_skip_producer = 0;
-int g_variant = 0;  // 0 automatic, 1 force the 1-SM kernel, 2 force the 2-SM kernel
+// 0 automatic, 1 force the 1-SM kernel, 2 force the 2-SM kernel, 3 force the
+// 1-SM kernel without split-K
+int g_variant = 0;
+GemmLaunchInfo g_last_launch{};
 
 bool is_fp4(const GemmArgs& g) { return g.elem_fmt == kE2M1; }
 
@@ -899,8 +1022,58 @@ KParams base_params(const GemmArgs& g, int bm, int bn) {
     return p;
 }
 
+constexpr int kMinStagesPerSlice = 4;  // K stages each split-K slice accumulates at least
+
+void split_launch_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, int tiles, int split, bool fp4,
+                         cudaStream_t stream) {
+    *cfg = cudaLaunchConfig_t{};
+    cfg->gridDim = dim3(static_cast<unsigned>(tiles * split), 1, 1);
+    cfg->blockDim = dim3(sm1::THREADS, 1, 1);
+    cfg->dynamicSmemBytes = sm1::smem_alloc(fp4);
+    cfg->stream = stream;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(split);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg->attrs = attr;
+    cfg->numAttrs = 1;
+}
+
+// Co-resident clusters of `split` 1-SM GEMM CTAs on the current device (cached).
 template <bool FP4>
-cudaError_t launch_1sm(const GemmArgs& g, cudaStream_t stream) {
+int max_split_clusters(int split) {
+    static std::mutex mu;
+    static int cached[64][kMaxSplitK + 1] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    std::lock_guard<std::mutex> lock(mu);
+    if (cached[dev][split] == 0) {
+        cudaLaunchConfig_t cfg;
+        cudaLaunchAttribute attr[1];
+        split_launch_config(&cfg, attr, device_sm_count() / split, split, FP4, nullptr);
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, mx_gemm_kernel<FP4>, &cfg) != cudaSuccess) n = 0;
+        cached[dev][split] = n > 0 ? n : -1;
+    }
+    return cached[dev][split] > 0 ? cached[dev][split] : 0;
+}
+
+// Split-K factor for `tiles` 128 x 256 tiles of `num_kb` K stages: the
+// largest S <= 8 whose tiles x S CTAs run in one wave (all clusters resident
+// at once) while every slice keeps at least kMinStagesPerSlice stages.
+// Few-tile problems (small M) otherwise leave most SMs idle.
+template <bool FP4>
+int choose_split_k(int tiles, int num_kb) {
+    const int sms = device_sm_count();
+    for (int s = kMaxSplitK; s > 1; --s) {
+        if (static_cast<int64_t>(tiles) * s > sms || num_kb < kMinStagesPerSlice * s) continue;
+        if (max_split_clusters<FP4>(s) >= tiles) return s;
+    }
+    return 1;
+}
+
+template <bool FP4>
+cudaError_t launch_1sm(const GemmArgs& g, cudaStream_t stream, bool allow_split) {
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once, [] {
@@ -914,6 +1087,14 @@ cudaError_t launch_1sm(const GemmArgs& g, cudaStream_t stream) {
         return cudaErrorInvalidValue;
     KParams p = base_params(g, sm1::BM, sm1::BN);
     const int tiles = p.batch * p.num_m_tiles * p.num_n_tiles;
+    p.split_k = allow_split ? choose_split_k<FP4>(tiles, p.num_kb) : 1;
+    g_last_launch = GemmLaunchInfo{1, p.split_k};
+    if (p.split_k > 1) {
+        cudaLaunchConfig_t cfg;
+        cudaLaunchAttribute attr[1];
+        split_launch_config(&cfg, attr, tiles, p.split_k, FP4, stream);
+        return cudaLaunchKernelEx(&cfg, mx_gemm_kernel<FP4>, ma, mb, p);
+    }
     const int sms = device_sm_count();
     const int grid = tiles < sms ? tiles : sms;
     mx_gemm_kernel<FP4><<<grid, sm1::THREADS, sm1::smem_alloc(FP4), stream>>>(ma, mb, p);
@@ -983,6 +1164,8 @@ cudaError_t launch_2sm(const GemmArgs& g, cudaStream_t stream) {
     p.idesc_half = make_idesc_mxf8(g.elem_fmt, g.elem_fmt, sm2::BM, sm2::BN / 2);
     if (is_fp4(g)) p.idesc_half = make_idesc_mxf4(sm2::BM, sm2::BN / 2);
     const int clusters = p.split_tail ? (full_rounds > 0 ? cap : 2 * tail) : (tiles < cap ? tiles : cap);
+    p.split_k = 1;
+    g_last_launch = GemmLaunchInfo{2, 1};
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[1];
     pair_launch_config(&cfg, attr, clusters, FP4, stream);
@@ -998,10 +1181,13 @@ void set_gemm_fault_injection(int skip_producer, uint64_t timeout_ns) {
 
 void set_gemm_variant(int variant) { g_variant = variant; }
 
+GemmLaunchInfo last_gemm_launch() { return g_last_launch; }
+
 cudaError_t launch_scaled_matmul(const GemmArgs& g, cudaStream_t stream) {
     const bool pair = g_variant == 2 || (g_variant == 0 && g.M > 128);
-    if (is_fp4(g)) return pair ? launch_2sm<true>(g, stream) : launch_1sm<true>(g, stream);
-    return pair ? launch_2sm<false>(g, stream) : launch_1sm<false>(g, stream);
+    const bool split = g_variant != 3;
+    if (is_fp4(g)) return pair ? launch_2sm<true>(g, stream) : launch_1sm<true>(g, stream, split);
+    return pair ? launch_2sm<false>(g, stream) : launch_1sm<false>(g, stream, split);
 }
 
 cudaError_t read_and_clear_device_status(int* status) {

@@ -646,8 +646,16 @@ mx_status mx_debug_gemm_fault_injection(int skip_producer, uint64_t timeout_ns) 
 }
 
 mx_status mx_debug_set_gemm_variant(int variant) {
-    if (variant < 0 || variant > 2) return MX_ERR_INVALID_ARG;
+    if (variant < 0 || variant > 3) return MX_ERR_INVALID_ARG;
     set_gemm_variant(variant);
+    return MX_OK;
+}
+
+mx_status mx_debug_last_gemm_launch(int* kernel, int* split_k) {
+    if (!kernel || !split_k) return MX_ERR_INVALID_ARG;
+    const GemmLaunchInfo info = last_gemm_launch();
+    *kernel = info.kernel;
+    *split_k = info.split_k;
     return MX_OK;
 }
 

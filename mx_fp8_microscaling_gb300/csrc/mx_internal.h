@@ -96,6 +96,13 @@ struct GemmArgs {
 };
 cudaError_t launch_scaled_matmul(const GemmArgs& g, cudaStream_t stream);
 
+// Which kernel the last ScaledMatmul launch on this host used (testing aid).
+struct GemmLaunchInfo {
+    int kernel;   // 1: 1-SM kernel, 2: 2-SM pair kernel, 0: none yet
+    int split_k;  // CTAs per tile along K (1-SM kernel), else 1
+};
+GemmLaunchInfo last_gemm_launch();
+
 // Per-device properties, cached.
 int device_sm_count();
 bool device_is_sm103();

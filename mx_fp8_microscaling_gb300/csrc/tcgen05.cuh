@@ -210,6 +210,33 @@ __device__ __forceinline__ void cluster_sync_all() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// Generic address of a shared-memory address of this CTA.
+__device__ __forceinline__ const void* generic_shared(uint32_t saddr) {
+    uint64_t r;
+    asm volatile("cvta.shared.u64 %0, %1;" : "=l"(r) : "l"(static_cast<uint64_t>(saddr)));
+    return reinterpret_cast<const void*>(r);
+}
+
+// Generic address of the same shared-memory object in cluster CTA `rank`
+// (plain loads through it reach that CTA's shared memory).
+template <typename T>
+__device__ __forceinline__ const T* map_cluster(const T* p, uint32_t rank) {
+    uint64_t r;
+    asm("mapa.u64 %0, %1, %2;" : "=l"(r) : "l"(reinterpret_cast<uint64_t>(p)), "r"(rank));
+    return reinterpret_cast<const T*>(r);
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t saddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(saddr), "r"(a), "r"(b), "r"(c), "r"(d)
+                 : "memory");
+}
+
+// Orders this thread's earlier async-proxy (TMA, tensor core) accesses of
+// shared memory before its later generic ones.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // Arrive on an mbarrier of any CTA of the cluster (release at cluster scope).
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");

@@ -283,3 +283,16 @@ def test_host_quantize_batch_workspace_and_checks(mx, lib):
     bad[1].cols = 500   # not a multiple of 32 along the block
     assert lib.mx_quantize_host_batch(bad, 2, 0, FAKE, 1 << 30, None) == 5
     assert lib.mx_quantize_host_batch(jobs, 2, 0, FAKE, 16, None) == 7
+
+
+def test_debug_hooks_check_arguments(mx, lib):
+    # the kernel-choice hook takes 0..3; the last-launch query wants both pointers
+    assert lib.mx_debug_set_gemm_variant(4) == mx.MX_ERR_INVALID_ARG
+    assert lib.mx_debug_set_gemm_variant(-1) == mx.MX_ERR_INVALID_ARG
+    for v in (3, 0):
+        assert lib.mx_debug_set_gemm_variant(v) == mx.MX_OK
+    one = ctypes.c_int()
+    assert lib.mx_debug_last_gemm_launch(None, ctypes.byref(one)) == mx.MX_ERR_INVALID_ARG
+    assert lib.mx_debug_last_gemm_launch(ctypes.byref(one), None) == mx.MX_ERR_INVALID_ARG
+    kernel, split = mx.mx_debug_last_gemm_launch()
+    assert kernel in (0, 1, 2) and split >= (1 if kernel else 0)

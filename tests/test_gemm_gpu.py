@@ -23,9 +23,10 @@ def mx():
     return mx
 
 
-@pytest.fixture(params=[1, 2], ids=["1sm", "2sm"])
+@pytest.fixture(params=[1, 2, 3], ids=["1sm", "2sm", "1sm_nosplit"])
 def variant(request, mx):
-    """Run a test on the 1-SM kernel and on the 2-SM pair kernel."""
+    """Run a test on the 1-SM kernel (split-K where the shape calls for it),
+    on the 2-SM pair kernel and on the 1-SM kernel with split-K disabled."""
     mx.mx_debug_set_gemm_variant(request.param)
     yield request.param
     mx.mx_debug_set_gemm_variant(0)
