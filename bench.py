@@ -897,7 +897,8 @@ def main():
             "cases": cases,
             "roofline": {"bound": "hbm", "kernel": "mx_gemm_kernel (split-K)", "achieved": top["gbs"],
                          "peak": peaks["hbm"], "unit": "GB/s", "frac": top["frac"], "peak_source": peaks["src"],
-                         "traffic": None, "note": f"M = {max(SMALL_M)}; bytes = B + A + both scale tensors + C"}}
+                         "traffic": profiled_traffic("mx_gemm_kernel_small_m", source_hash("gemm.cu")),
+                         "note": f"M = {max(SMALL_M)}; bytes = B + A + both scale tensors + C"}}
         line["scaled_matmul_small_m"]["vendor_reference"] = vendor_small_m_reference(torch, sm, args.steps)
     if "dot" in parts:
         peak_fp8 = peaks["bf16"] * FP8_OVER_BF16
