@@ -379,10 +379,19 @@ class Fused:
         self.c = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
         self.work = torch.empty(mx.mx_fused_quantize_matmul_workspace(M, N, K), dtype=torch.uint8, device="cuda")
         self.op = api.fused(self.x, self.wq, self.ws, "e4m3fn", "bf16", self.c, self.work)
-        self.launches = 2
+        # the same product unfused: QuantizeMX of X into SF-layout scales,
+        # then ScaledMatmul, as two calls (reported as the fused call's split)
+        self.xq = torch.empty((M, K), dtype=torch.uint8, device="cuda")
+        self.xs = torch.empty(mx.mx_sf_layout_bytes(M, K), dtype=torch.uint8, device="cuda")
+        self.unfused = [("fused_split_quantize", api.quantize(self.x, "e4m3fn", "1x32", -1, "sf", self.xq, self.xs)),
+                        ("fused_split_gemm", api.matmul_sf(self.xq, self.wq, self.xs, self.ws, "e4m3fn", "bf16",
+                                                           self.c, K))]
+        self.launches = 2 + 2
 
     def step(self, timer):
         timer.run("fused", self.op)
+        for label, fn in self.unfused:
+            timer.run(label, fn)
 
 
 class GemmFp4:
@@ -452,6 +461,66 @@ class Dot:
     def step(self, timer):
         for label, fn in self.ops:
             timer.run(label, fn)
+
+
+class Pipeline256:
+    """The MX-FP8 pipeline at M = N = K = 256, seed 0: QuantizeMX of A and
+    Bt (bf16, N(0,1) x 2^U(-20,20) per 32-block) along K to e4m3fn with
+    plain scales, repack of both scale tensors, ScaledMatmul to f32.  Five
+    launches, a few microseconds each: latency-bound, reported in us."""
+
+    def __init__(self, torch, mx, api):
+        self.torch = torch
+        a_bits, b_bits = syn.pipeline_operands(256, 256, 256, seed=0)
+        self.a, self.b = dev_bits(torch, a_bits, "bf16"), dev_bits(torch, b_bits, "bf16")
+        self.qa = torch.empty((256, 256), dtype=torch.uint8, device="cuda")
+        self.qb = torch.empty((256, 256), dtype=torch.uint8, device="cuda")
+        self.sa = torch.empty((256, 8), dtype=torch.uint8, device="cuda")
+        self.sb = torch.empty((256, 8), dtype=torch.uint8, device="cuda")
+        self.sfa = torch.empty(mx.mx_sf_layout_bytes(256, 256), dtype=torch.uint8, device="cuda")
+        self.sfb = torch.empty(mx.mx_sf_layout_bytes(256, 256), dtype=torch.uint8, device="cuda")
+        self.c = torch.empty((256, 256), dtype=torch.float32, device="cuda")
+        self.ops = [api.quantize(self.a, "e4m3fn", "1x32", -1, "plain", self.qa, self.sa),
+                    api.quantize(self.b, "e4m3fn", "1x32", -1, "plain", self.qb, self.sb),
+                    api.repack(self.sa, 256, self.sfa), api.repack(self.sb, 256, self.sfb),
+                    api.matmul_sf(self.qa, self.qb, self.sfa, self.sfb, "e4m3fn", "f32", self.c, 256)]
+        self.launches = 5
+        # the same five calls captured once as a CUDA graph (bound to the
+        # capturing stream), timed after the main loop: the device time
+        # without host dispatch
+        self.side = torch.cuda.Stream()
+        with torch.cuda.stream(self.side):
+            ops = [api.quantize(self.a, "e4m3fn", "1x32", -1, "plain", self.qa, self.sa),
+                   api.quantize(self.b, "e4m3fn", "1x32", -1, "plain", self.qb, self.sb),
+                   api.repack(self.sa, 256, self.sfa), api.repack(self.sb, 256, self.sfb),
+                   api.matmul_sf(self.qa, self.qb, self.sfa, self.sfb, "e4m3fn", "f32", self.c, 256)]
+            for fn in ops:
+                fn()
+        self.side.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph, stream=self.side):
+            for fn in ops:
+                fn()
+        torch.cuda.synchronize()
+
+    def graph_us(self, reps=200):
+        torch = self.torch
+        for _ in range(10):
+            self.graph.replay()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            self.graph.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) * 1e3 / reps
+
+    def run_all(self):
+        for fn in self.ops:
+            fn()
+
+    def step(self, timer):
+        timer.run("pipeline_256", self.run_all)
 
 
 class GemmSmallM:
@@ -662,6 +731,21 @@ def oracle_gemm_sample(rows=2):
     return 2.0 * rows * GEMM_N * K / dt / 1e12, dt
 
 
+def oracle_pipeline_256(repeats=5):
+    """The oracle's 256^3 MX-FP8 pipeline (quantize both operands along K,
+    then the binary64 ScaledMatmul); median microseconds over `repeats`."""
+    import oracle as orc
+    a_bits, b_bits = syn.pipeline_operands(256, 256, 256, seed=0)
+    times = []
+    for _ in range(repeats):
+        t0 = time.perf_counter()
+        qa, sa = orc.quantize(a_bits, "bf16", "e4m3fn", geometry="1x32", dim=-1)
+        qb, sb = orc.quantize(b_bits, "bf16", "e4m3fn", geometry="1x32", dim=-1)
+        orc.scaled_matmul(qa, qb, sa, sb, "e4m3fn")
+        times.append(time.perf_counter() - t0)
+    return statistics.median(times) * 1e6
+
+
 # ------------------------------------------------------------------- main
 
 def dist_setup():
@@ -736,7 +820,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="mx", choices=["mx", "reference"])
     ap.add_argument("--workload", default="all",
-                    choices=["all", "sweep", "gemm", "fp4", "fused", "dequant", "dot", "gemm_fp4", "gemm_small_m"])
+                    choices=["all", "sweep", "gemm", "fp4", "fused", "dequant", "dot", "gemm_fp4", "gemm_small_m",
+                             "pipeline_256"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--reference-rows", type=int, default=1024,
                     help="rows of each [rows, 8192] sweep slice the reference arm quantizes per step")
@@ -754,10 +839,11 @@ def main():
 
     peaks = load_peaks()
     parts = {}
-    want = (["sweep", "gemm", "fp4", "dequant", "fused", "dot", "gemm_fp4", "gemm_small_m"] if args.workload == "all"
+    want = (["sweep", "gemm", "fp4", "dequant", "fused", "dot", "gemm_fp4", "gemm_small_m", "pipeline_256"]
+            if args.workload == "all"
             else [args.workload])
     builders = {"sweep": Sweep, "gemm": Gemm, "fp4": Fp4, "dequant": Dequant, "fused": Fused, "dot": Dot,
-                "gemm_fp4": GemmFp4, "gemm_small_m": GemmSmallM}
+                "gemm_fp4": GemmFp4, "gemm_small_m": GemmSmallM, "pipeline_256": Pipeline256}
     api = Api(torch, mx)
     for name in want:
         parts[name] = builders[name](torch, mx, api)
@@ -862,7 +948,12 @@ def main():
         ms = timer.avg_ms("fused")
         tf = FUSED_FLOP / (ms * 1e-3) / 1e12
         peak_fp8 = peaks["bf16"] * FP8_OVER_BF16
+        q_ms, g_ms = timer.avg_ms("fused_split_quantize"), timer.avg_ms("fused_split_gemm")
         line["fused"] = {"value": round(tf, 1), "unit": "TFLOP/s", "ms": round(ms, 4),
+                         "unfused": {"quantize_x_ms": round(q_ms, 4), "gemm_ms": round(g_ms, 4),
+                                     "total_ms": round(q_ms + g_ms, 4),
+                                     "tflops": round(FUSED_FLOP / ((q_ms + g_ms) * 1e-3) / 1e12, 1),
+                                     "what": "QuantizeMX of X to SF-layout scales, then ScaledMatmul, as two calls"},
                          "config": "X[16384,8192] bf16 -> e4m3fn (1x32 along K) x W[8192,28672] e4m3fn -> bf16",
                          "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": round(peak_fp8, 1),
                                       "unit": "TFLOP/s", "frac": round(tf / peak_fp8, 4),
@@ -882,6 +973,12 @@ def main():
                          "peak": round(peak_fp4, 1), "unit": "TFLOP/s", "frac": round(tf / peak_fp4, 4),
                          "peak_source": f"{peaks['src']} bf16 burst x {FP4_OVER_BF16} (nominal FP4/bf16)"}}
         line["scaled_matmul_fp4"]["vendor_reference"] = vendor_fp4_reference(torch, parts["gemm_fp4"], args.steps)
+    if "pipeline_256" in parts:
+        us = timer.avg_ms("pipeline_256") * 1e3
+        line["pipeline_256"] = {"us": round(us, 2), "tflops": round(2 * 256 ** 3 / (us * 1e-6) / 1e12, 3),
+                                "us_cuda_graph": round(parts["pipeline_256"].graph_us(), 2),
+                                "config": "M=N=K=256 bf16 -> quantize A, Bt (1x32 along K, e4m3fn) -> repack x2 -> "
+                                          "ScaledMatmul -> f32; 5 launches, latency-bound (no roofline claimed)"}
     if "gemm_small_m" in parts:
         sm = parts["gemm_small_m"]
         cases = {}
@@ -978,6 +1075,11 @@ def main():
                                                      "sample": "2 full output rows of the 8192^3 product, "
                                                                "binary64 k-ordered sums",
                                                      "seconds": round(dtg, 2)}
+        if "pipeline_256" in parts:
+            us = oracle_pipeline_256()
+            line["cpu_baseline"]["pipeline_256"] = {"us": round(us, 1), "cores": 1,
+                                                    "sample": "the whole 256^3 pipeline: oracle QuantizeMX of A "
+                                                              "and Bt, binary64 dequantize-then-matmul"}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if ws > 1:
