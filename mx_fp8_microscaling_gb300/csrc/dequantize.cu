@@ -25,6 +25,7 @@
 
 #include "mx_device.cuh"
 #include "mx_internal.h"
+#include "pdl.cuh"
 
 namespace mx {
 namespace {
@@ -250,6 +251,8 @@ __device__ __forceinline__ void store_chunk(const DequantArgs& q, const uint32_t
 // t, t + blockDim.x, ...  BR / BC: the block's extent along rows / columns.
 template <int FMT, bool BF16, int BR, int BC>
 __global__ void __launch_bounds__(kThreads, BF16 ? kMinBlocksBf16 : kMinBlocksF32) dequant_kernel(DequantArgs q) {
+    dev::pdl_allow_next();
+    dev::pdl_wait_prior();
     const int64_t nchunk = (q.cols + kChunk - 1) / kChunk;
     for (int64_t r = blockIdx.x; r < q.rows; r += gridDim.x) {
         const int64_t srow = r / BR;
@@ -270,8 +273,7 @@ template <int FMT, bool BF16, int BR, int BC>
 cudaError_t launch_shape(const DequantArgs& q, cudaStream_t stream) {
     const int64_t cap = static_cast<int64_t>(device_sm_count()) * kGridPerSm;
     const int64_t blocks = q.rows < cap ? q.rows : cap;
-    dequant_kernel<FMT, BF16, BR, BC><<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(q);
-    return cudaGetLastError();
+    return launch_pdl(dequant_kernel<FMT, BF16, BR, BC>, static_cast<unsigned>(blocks), kThreads, 0, stream, q);
 }
 
 template <int FMT, bool BF16>

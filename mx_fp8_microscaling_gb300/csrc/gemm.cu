@@ -66,6 +66,7 @@
 
 #include "mx_device.cuh"
 #include "mx_internal.h"
+#include "pdl.cuh"
 #include "tcgen05.cuh"
 
 namespace mx {
@@ -330,6 +331,7 @@ __global__ void __launch_bounds__(sm1::THREADS, 1)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
 
+    pdl_allow_next();
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full_bar(s), 1);
@@ -355,6 +357,7 @@ __global__ void __launch_bounds__(sm1::THREADS, 1)
     const uint32_t tmem_base = *tmem_slot;
     const int num_tiles = p.batch * p.num_m_tiles * p.num_n_tiles;
     const Sm1Work work = sm1_work(p, num_tiles);
+    pdl_wait_prior();  // set-up done; operands, scales and C belong to earlier kernels until here
 
     if (warp == 0) {
         if (lane == 0 && !p.skip_producer) {
@@ -659,6 +662,7 @@ __global__ void __launch_bounds__(sm2::THREADS, 1)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
 
+    pdl_allow_next();
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full_bar(s), 1);     // rank 0's: its arrive + both CTAs' bytes
@@ -690,6 +694,7 @@ __global__ void __launch_bounds__(sm2::THREADS, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     const int num_units = pair_units(p, cluster, num_clusters);
+    pdl_wait_prior();  // set-up done; operands, scales and C belong to earlier kernels until here
 
     if (warp == 0) {
         if (lane == 0 && !p.skip_producer) {
@@ -1024,6 +1029,7 @@ KParams base_params(const GemmArgs& g, int bm, int bn) {
 
 constexpr int kMinStagesPerSlice = 4;  // K stages each split-K slice accumulates at least
 
+// attr: room for 2 (cluster shape, programmatic serialization)
 void split_launch_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, int tiles, int split, bool fp4,
                          cudaStream_t stream) {
     *cfg = cudaLaunchConfig_t{};
@@ -1035,8 +1041,9 @@ void split_launch_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, int
     attr[0].val.clusterDim.x = static_cast<unsigned>(split);
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1] = pdl_attribute();
     cfg->attrs = attr;
-    cfg->numAttrs = 1;
+    cfg->numAttrs = 2;
 }
 
 // Co-resident clusters of `split` 1-SM GEMM CTAs on the current device (cached).
@@ -1049,7 +1056,7 @@ int max_split_clusters(int split) {
     std::lock_guard<std::mutex> lock(mu);
     if (cached[dev][split] == 0) {
         cudaLaunchConfig_t cfg;
-        cudaLaunchAttribute attr[1];
+        cudaLaunchAttribute attr[2];
         split_launch_config(&cfg, attr, device_sm_count() / split, split, FP4, nullptr);
         int n = 0;
         if (cudaOccupancyMaxActiveClusters(&n, mx_gemm_kernel<FP4>, &cfg) != cudaSuccess) n = 0;
@@ -1091,16 +1098,17 @@ cudaError_t launch_1sm(const GemmArgs& g, cudaStream_t stream, bool allow_split)
     g_last_launch = GemmLaunchInfo{1, p.split_k};
     if (p.split_k > 1) {
         cudaLaunchConfig_t cfg;
-        cudaLaunchAttribute attr[1];
+        cudaLaunchAttribute attr[2];
         split_launch_config(&cfg, attr, tiles, p.split_k, FP4, stream);
         return cudaLaunchKernelEx(&cfg, mx_gemm_kernel<FP4>, ma, mb, p);
     }
     const int sms = device_sm_count();
     const int grid = tiles < sms ? tiles : sms;
-    mx_gemm_kernel<FP4><<<grid, sm1::THREADS, sm1::smem_alloc(FP4), stream>>>(ma, mb, p);
-    return cudaGetLastError();
+    return launch_pdl(mx_gemm_kernel<FP4>, static_cast<unsigned>(grid), sm1::THREADS, sm1::smem_alloc(FP4), stream,
+                      ma, mb, p);
 }
 
+// attr: room for 2 (cluster shape, programmatic serialization)
 void pair_launch_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, int clusters, bool fp4,
                         cudaStream_t stream) {
     *cfg = cudaLaunchConfig_t{};
@@ -1112,8 +1120,9 @@ void pair_launch_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, int 
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1] = pdl_attribute();
     cfg->attrs = attr;
-    cfg->numAttrs = 1;
+    cfg->numAttrs = 2;
 }
 
 // Co-resident 2-CTA clusters of the pair kernel on the current device (cached).
@@ -1126,7 +1135,7 @@ int max_pair_clusters() {
     std::lock_guard<std::mutex> lock(mu);
     if (cached[dev] == 0) {
         cudaLaunchConfig_t cfg;
-        cudaLaunchAttribute attr[1];
+        cudaLaunchAttribute attr[2];
         pair_launch_config(&cfg, attr, device_sm_count() / 2, FP4, nullptr);
         int n = 0;
         if (cudaOccupancyMaxActiveClusters(&n, mx_gemm_2sm_kernel<FP4>, &cfg) != cudaSuccess || n <= 0)
@@ -1167,7 +1176,7 @@ cudaError_t launch_2sm(const GemmArgs& g, cudaStream_t stream) {
     p.split_k = 1;
     g_last_launch = GemmLaunchInfo{2, 1};
     cudaLaunchConfig_t cfg;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     pair_launch_config(&cfg, attr, clusters, FP4, stream);
     return cudaLaunchKernelEx(&cfg, mx_gemm_2sm_kernel<FP4>, ma, mb, msa, msb, p);
 }

@@ -18,6 +18,7 @@
 #include <cstdint>
 
 #include "mx_internal.h"
+#include "pdl.cuh"
 
 namespace mx {
 namespace {
@@ -45,6 +46,8 @@ __device__ __forceinline__ int64_t row_offset(const Dims& d, int64_t row) {
 
 __global__ void __launch_bounds__(kThreads) permute_rows(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst,
                                                          Dims d, int64_t rows) {
+    dev::pdl_allow_next();
+    dev::pdl_wait_prior();
     const int64_t len = d.dst_dims[d.rank - 1];
     for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
         const uint8_t* s = src + row_offset(d, r);
@@ -80,6 +83,8 @@ __global__ void __launch_bounds__(kThreads) permute_transpose(const uint8_t* __r
                                                               uint8_t* __restrict__ dst, Dims d, int ai,
                                                               int64_t tiles_i, int64_t tiles_j, int64_t units,
                                                               int aligned) {
+    dev::pdl_allow_next();
+    dev::pdl_wait_prior();
     const int aj = d.rank - 1;
     const int64_t ni = d.dst_dims[ai], nj = d.dst_dims[aj];
     const int64_t sj = d.src_stride[aj], di = d.dst_stride[ai];
@@ -162,8 +167,7 @@ cudaError_t launch_permute_bytes(const PermuteArgs& a, cudaStream_t stream) {
     if (d.src_stride[d.rank - 1] == 1) {
         const int64_t rows = total / d.dst_dims[d.rank - 1];
         const int64_t grid = rows < cap ? rows : cap;
-        permute_rows<<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(a.src, a.dst, d, rows);
-        return cudaGetLastError();
+        return launch_pdl(permute_rows, static_cast<unsigned>(grid), kThreads, 0, stream, a.src, a.dst, d, rows);
     }
     int ai = -1;
     for (int i = 0; i < d.rank - 1; ++i)
@@ -179,9 +183,8 @@ cudaError_t launch_permute_bytes(const PermuteArgs& a, cudaStream_t stream) {
         if (i != ai) aligned = aligned && d.src_stride[i] % 4 == 0 && d.dst_stride[i] % 16 == 0;
     const int64_t warps = (units + 7) / 8;
     const int64_t grid = warps < cap ? warps : cap;
-    permute_transpose<<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(a.src, a.dst, d, ai, tiles_i, tiles_j,
-                                                                            units, aligned ? 1 : 0);
-    return cudaGetLastError();
+    return launch_pdl(permute_transpose, static_cast<unsigned>(grid), kThreads, 0, stream, a.src, a.dst, d, ai,
+                      tiles_i, tiles_j, units, aligned ? 1 : 0);
 }
 
 }  // namespace mx

@@ -32,6 +32,7 @@
 
 #include "mx_device.cuh"
 #include "mx_internal.h"
+#include "pdl.cuh"
 
 namespace mx {
 namespace {
@@ -172,6 +173,8 @@ __device__ __forceinline__ void store8(uint8_t* dst, uint32_t w0, uint32_t w1) {
 // Consecutive threads take consecutive chunks of the same rows.
 template <bool F16, int FMT>
 __global__ void __launch_bounds__(kThreads) quant_g84(QuantArgs q) {
+    dev::pdl_allow_next();
+    dev::pdl_wait_prior();
     const int64_t nchunk = q.cols >> 3;
     const int64_t total = (q.rows >> 3) * nchunk;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -224,6 +227,8 @@ __global__ void __launch_bounds__(kThreads) quant_g84(QuantArgs q) {
 // row.  The loop is warp-uniform so every lane takes part in the shuffles.
 template <bool F16, int FMT>
 __global__ void __launch_bounds__(kThreads) quant_g1x32(QuantArgs q) {
+    dev::pdl_allow_next();
+    dev::pdl_wait_prior();
     constexpr int TR = 8;
     const int lane = threadIdx.x & 31;
     const int64_t nchunk = q.cols >> 3;
@@ -313,6 +318,8 @@ __device__ __forceinline__ int64_t remap_index(int64_t n, int stride) {
 // exponent / scale arithmetic is shared by 16 elements instead of 8).
 template <bool F16, int FMT>
 __global__ void __launch_bounds__(kThreads) quant_g1x32w(QuantArgs q) {
+    dev::pdl_allow_next();
+    dev::pdl_wait_prior();
     constexpr int TR = 4;
     const int lane = threadIdx.x & 31;
     const int64_t nchunk = q.cols >> 4;
@@ -387,6 +394,8 @@ __global__ void __launch_bounds__(kThreads) quant_g1x32w(QuantArgs q) {
 
 template <bool F16, int FMT>
 __global__ void __launch_bounds__(kThreads) quant_generic(QuantArgs q) {
+    dev::pdl_allow_next();
+    dev::pdl_wait_prior();
     const int br = q.block_rows, bc = q.block_cols;
     const int tc = bc > 8 ? bc : 8;
     const int64_t ntc = (q.cols + tc - 1) / tc;
@@ -454,20 +463,19 @@ cudaError_t launch_typed(const QuantArgs& q, cudaStream_t stream) {
     const bool wide = (q.cols % 8) == 0 && q.vec_ok;
     if (wide && q.block_rows == 8 && q.block_cols == 4) {
         const int64_t units = (q.rows / 8) * (q.cols / 8);
-        quant_g84<F16, FMT><<<grid_for(units), kThreads, 0, stream>>>(q);
+        return launch_pdl(quant_g84<F16, FMT>, grid_for(units), kThreads, 0, stream, q);
     } else if (wide && q.vec32_ok && q.block_rows == 1 && q.block_cols == 32) {
         const int64_t units = ((q.rows + 3) / 4) * (q.cols / 16);
-        quant_g1x32w<F16, FMT><<<grid_for(units), kThreads, 0, stream>>>(q);
+        return launch_pdl(quant_g1x32w<F16, FMT>, grid_for(units), kThreads, 0, stream, q);
     } else if (wide && q.block_rows == 1 && q.block_cols == 32) {
         const int64_t units = ((q.rows + 7) / 8) * (q.cols / 8);
         // round the grid so each warp's 32 units stay inside one launch slot
-        quant_g1x32<F16, FMT><<<grid_for(units), kThreads, 0, stream>>>(q);
+        return launch_pdl(quant_g1x32<F16, FMT>, grid_for(units), kThreads, 0, stream, q);
     } else {
         const int tc = q.block_cols > 8 ? q.block_cols : 8;
         const int64_t units = (q.rows / q.block_rows) * ((q.cols + tc - 1) / tc);
-        quant_generic<F16, FMT><<<grid_for(units), kThreads, 0, stream>>>(q);
+        return launch_pdl(quant_generic<F16, FMT>, grid_for(units), kThreads, 0, stream, q);
     }
-    return cudaGetLastError();
 }
 
 }  // namespace

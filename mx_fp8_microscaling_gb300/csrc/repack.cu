@@ -18,6 +18,7 @@
 #include <cstdint>
 
 #include "mx_internal.h"
+#include "pdl.cuh"
 
 namespace mx {
 namespace {
@@ -30,6 +31,8 @@ __global__ void __launch_bounds__(kRepackThreads) repack_sf_kernel(const uint8_t
                                                                   int64_t kb, int64_t ld, int64_t ntm, int64_t ntk,
                                                                   int64_t plain_batch_stride, int64_t batch,
                                                                   uint8_t* __restrict__ sf, int vec_ok) {
+    dev::pdl_allow_next();
+    dev::pdl_wait_prior();
     __shared__ __align__(16) uint8_t rows[128][kCols + 16];
     const int64_t nchunk = (ntk + kTilesPerBlock - 1) / kTilesPerBlock;
     const int64_t units = batch * ntm * nchunk;
@@ -90,9 +93,8 @@ cudaError_t launch_repack_scales_batched(const uint8_t* plain, int64_t mn, int64
     const int64_t blocks = units < cap ? units : cap;
     const int vec_ok = (reinterpret_cast<uintptr_t>(plain) & 15u) == 0 && ld_plain % 16 == 0 &&
                        plain_batch_stride % 16 == 0;
-    repack_sf_kernel<<<static_cast<unsigned>(blocks), kRepackThreads, 0, stream>>>(
-        plain, mn, kb, ld_plain, ntm, ntk, plain_batch_stride, batch, sf, vec_ok);
-    return cudaGetLastError();
+    return launch_pdl(repack_sf_kernel, static_cast<unsigned>(blocks), kRepackThreads, 0, stream, plain, mn, kb,
+                      ld_plain, ntm, ntk, plain_batch_stride, batch, sf, vec_ok);
 }
 
 cudaError_t launch_repack_scales(const uint8_t* plain, int64_t mn, int64_t k, int64_t ld_plain,
