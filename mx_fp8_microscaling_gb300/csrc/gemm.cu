@@ -1042,6 +1042,29 @@ KParams base_params(const GemmArgs& g, int bm, int bn) {
 
 constexpr int kMinStagesPerSlice = 4;  // K stages each split-K slice accumulates at least
 
+// The kernels' dynamic shared memory exceeds the default limit: set the
+// attribute once, before any launch or occupancy query.
+template <bool FP4>
+cudaError_t ensure_1sm_attr() {
+    static std::once_flag once;
+    static cudaError_t err = cudaSuccess;
+    std::call_once(once, [] {
+        err = cudaFuncSetAttribute(mx_gemm_kernel<FP4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   sm1::smem_alloc(FP4));
+    });
+    return err;
+}
+template <bool FP4>
+cudaError_t ensure_2sm_attr() {
+    static std::once_flag once;
+    static cudaError_t err = cudaSuccess;
+    std::call_once(once, [] {
+        err = cudaFuncSetAttribute(mx_gemm_2sm_kernel<FP4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   sm2::smem_alloc(FP4));
+    });
+    return err;
+}
+
 // attr: room for 2 (cluster shape, programmatic serialization)
 void split_launch_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, int tiles, int split, bool fp4,
                          cudaStream_t stream) {
@@ -1066,6 +1089,7 @@ int max_split_clusters(int split) {
     static int cached[64][kMaxSplitK + 1] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (ensure_1sm_attr<FP4>() != cudaSuccess) return 0;
     std::lock_guard<std::mutex> lock(mu);
     if (cached[dev][split] == 0) {
         cudaLaunchConfig_t cfg;
@@ -1094,12 +1118,7 @@ int choose_split_k(int tiles, int num_kb) {
 
 template <bool FP4>
 cudaError_t launch_1sm(const GemmArgs& g, cudaStream_t stream, bool allow_split) {
-    static std::once_flag attr_once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(attr_once, [] {
-        attr_err = cudaFuncSetAttribute(mx_gemm_kernel<FP4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        sm1::smem_alloc(FP4));
-    });
+    const cudaError_t attr_err = ensure_1sm_attr<FP4>();
     if (attr_err != cudaSuccess) return attr_err;
     CUtensorMap ma, mb;
     if (!make_operand_map(&ma, g.a, g.M, row_bytes(g), sm1::BM, g.batch, g.a_batch_stride) ||
@@ -1145,6 +1164,7 @@ int max_pair_clusters() {
     static int cached[64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+    if (ensure_2sm_attr<FP4>() != cudaSuccess) return 1;
     std::lock_guard<std::mutex> lock(mu);
     if (cached[dev] == 0) {
         cudaLaunchConfig_t cfg;
@@ -1160,12 +1180,7 @@ int max_pair_clusters() {
 
 template <bool FP4>
 cudaError_t launch_2sm(const GemmArgs& g, cudaStream_t stream) {
-    static std::once_flag attr_once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(attr_once, [] {
-        attr_err = cudaFuncSetAttribute(mx_gemm_2sm_kernel<FP4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        sm2::smem_alloc(FP4));
-    });
+    const cudaError_t attr_err = ensure_2sm_attr<FP4>();
     if (attr_err != cudaSuccess) return attr_err;
     CUtensorMap ma, mb, msa, msb;
     const int64_t sfa_tiles = g.batch * ((g.M + 127) / 128) * ((g.K + 127) / 128);
@@ -1205,10 +1220,27 @@ void set_gemm_variant(int variant) { g_variant = variant; }
 
 GemmLaunchInfo last_gemm_launch() { return g_last_launch; }
 
+// Automatic kernel choice.  M <= 128: the 1-SM kernel.  Otherwise the pair
+// kernel, unless its 256 x 256 tiles would fill at most a quarter of the
+// clusters and the 1-SM kernel can split K over clusters of at least 2: such
+// few-tile problems ran 1.3-2x faster on the 1-SM kernel with split-K than as
+// the pair kernel's half tiles (e.g. 1024 x 1024 x 8192: 14.4 against 21.0
+// us), while at about half the clusters the pair kernel was ahead again.
+template <bool FP4>
+bool prefer_pair(const GemmArgs& g) {
+    if (g.M <= 128) return false;
+    const int64_t pair_tiles = g.batch * ((g.M + 255) / 256) * ((g.N + 255) / 256);
+    if (pair_tiles * 4 > max_pair_clusters<FP4>()) return true;
+    const int64_t tiles_1sm = g.batch * ((g.M + sm1::BM - 1) / sm1::BM) * ((g.N + sm1::BN - 1) / sm1::BN);
+    const int64_t stage_k = FP4 ? 2 * BK : BK;
+    return choose_split_k<FP4>(static_cast<int>(tiles_1sm), static_cast<int>((g.K + stage_k - 1) / stage_k)) < 2;
+}
+
 cudaError_t launch_scaled_matmul(const GemmArgs& g, cudaStream_t stream) {
-    const bool pair = g_variant == 2 || (g_variant == 0 && g.M > 128);
+    const bool fp4 = is_fp4(g);
+    const bool pair = g_variant == 2 || (g_variant == 0 && (fp4 ? prefer_pair<true>(g) : prefer_pair<false>(g)));
     const bool split = g_variant != 3;
-    if (is_fp4(g)) return pair ? launch_2sm<true>(g, stream) : launch_1sm<true>(g, stream, split);
+    if (fp4) return pair ? launch_2sm<true>(g, stream) : launch_1sm<true>(g, stream, split);
     return pair ? launch_2sm<false>(g, stream) : launch_1sm<false>(g, stream, split);
 }
 

@@ -187,3 +187,18 @@ def test_split_k_bounded_wait_times_out_without_fault(mx):
     c = matmul(mx, a, bt, sa, sb, "e4m3fn", "f32")
     c_ref, s_ref = orc.scaled_matmul(a, bt, sa, sb, "e4m3fn")
     check_gemm(c.cpu().numpy(), c_ref, s_ref, "f32")
+
+
+@pytest.mark.parametrize("M,N,K,kernel", [(1024, 1024, 4096, 1), (2048, 512, 4096, 1), (300, 1000, 4096, 1),
+                                          (512, 4096, 2048, 2), (256, 8192, 1024, 2)])
+def test_auto_choice_for_few_tile_problems(mx, M, N, K, kernel):
+    # M > 128 whose 256 x 256 tiles fill at most a quarter of the pair
+    # clusters runs on the 1-SM kernel with split-K; at half the clusters and
+    # more, on the pair kernel.  Every element against the oracle.
+    a, bt, sa, sb = fp8_operands(M, N, K, "e4m3fn", seed=M + N + 1)
+    c = matmul(mx, a, bt, sa, sb, "e4m3fn", "bf16")
+    got_kernel, split = mx.mx_debug_last_gemm_launch()
+    assert got_kernel == kernel
+    assert split > 1 if kernel == 1 else split == 1
+    c_ref, s_ref = orc.scaled_matmul(a, bt, sa, sb, "e4m3fn")
+    check_gemm(c.float().cpu().numpy(), c_ref, s_ref, "bf16")
