@@ -257,14 +257,24 @@ __global__ void __launch_bounds__(kThreads, BF16 ? kMinBlocksBf16 : kMinBlocksF3
     for (int64_t r = blockIdx.x; r < q.rows; r += gridDim.x) {
         const int64_t srow = r / BR;
         const uint8_t* srow_ptr = q.scale + scale_slot(srow, q.scale_mode) * q.scale_cols;  // unused for SF
-        for (int64_t ch = threadIdx.x; ch < nchunk; ch += blockDim.x) {
-            const int64_t c0 = ch * kChunk;
-            const int n = q.cols - c0 >= kChunk ? kChunk : static_cast<int>(q.cols - c0);
-            uint32_t w[4], h[8], sp[8];
-            load_chunk<FMT>(q, r, c0, n, w);
-            chunk_scales<BC>(q, srow_ptr, srow, c0, n, sp);
-            decode_chunk<FMT>(q, w, h);
-            store_chunk<BF16>(q, h, sp, r, c0, n);
+        // two chunks a step (t and t + blockDim.x), both loads issued first
+        for (int64_t ch = threadIdx.x; ch < nchunk; ch += 2 * blockDim.x) {
+            const int64_t chb = ch + blockDim.x;
+            const bool two = chb < nchunk;
+            const int64_t c0 = ch * kChunk, c1 = chb * kChunk;
+            const int n0 = q.cols - c0 >= kChunk ? kChunk : static_cast<int>(q.cols - c0);
+            const int n1 = !two ? 0 : q.cols - c1 >= kChunk ? kChunk : static_cast<int>(q.cols - c1);
+            uint32_t w0[4], w1[4], h[8], sp[8];
+            load_chunk<FMT>(q, r, c0, n0, w0);
+            if (two) load_chunk<FMT>(q, r, c1, n1, w1);
+            chunk_scales<BC>(q, srow_ptr, srow, c0, n0, sp);
+            decode_chunk<FMT>(q, w0, h);
+            store_chunk<BF16>(q, h, sp, r, c0, n0);
+            if (two) {
+                chunk_scales<BC>(q, srow_ptr, srow, c1, n1, sp);
+                decode_chunk<FMT>(q, w1, h);
+                store_chunk<BF16>(q, h, sp, r, c1, n1);
+            }
         }
     }
 }
