@@ -7,13 +7,12 @@
 //   rows       the innermost destination axis is contiguous in the source:
 //              each block copies whole rows (16-byte accesses when aligned);
 //              the source offset of a row is found once per row.
-//   transpose  otherwise: each warp moves a 64 x 32-byte tile between the
+//   transpose  otherwise: each block moves 128 x 128-byte tiles between the
 //              axis that is contiguous in the source (i) and the
-//              destination's innermost axis (j).  A lane loads 16 words
-//              (4 bytes of i from 16 rows of j), transposes them in registers
-//              with byte permutes and stores 4 rows of 16 bytes: both sides
-//              touch whole 32-byte sectors, and no shared memory is needed.
-//              Tiles at the edges, or unaligned ones, go byte by byte.
+//              destination's innermost axis (j) through shared memory, whole
+//              128-byte lines on both sides; 4 x 4 byte blocks are
+//              transposed in registers with byte permutes.  Tiles at the
+//              edges, or unaligned ones, go byte by byte.
 
 #include <cstdint>
 
@@ -73,26 +72,35 @@ __device__ __forceinline__ void transpose4x4(const uint32_t (&in)[4], uint32_t (
     out[3] = __byte_perm(hi01, hi23, 0x7632);
 }
 
-constexpr int kTileI = 64;  // bytes of the source-contiguous axis per warp tile
-constexpr int kTileJ = 32;  // bytes of the destination-contiguous axis per warp tile
+constexpr int kTile = 128;     // bytes of both tile axes
+constexpr int kPitchWords = 33;  // shared tile row: 128 bytes + one word against bank conflicts
 
-// Warp tiles between destination axis `ai` (contiguous in the source) and
-// the innermost destination axis; every other axis indexes whole tiles.
-// `aligned`: source rows and destination rows allow 4- / 16-byte accesses.
+// Block tiles of 128 x 128 bytes between destination axis `ai` (contiguous
+// in the source) and the innermost destination axis j; every other axis
+// indexes whole tiles.  A full, aligned tile moves in three steps:
+//   1. 128 source rows (one per j) of 128 bytes (i): 16-byte global loads,
+//      8 threads a row, stored as words into a shared tile [j][i];
+//   2. thread (bi, jg) reads the 4 x 16 bytes at i = 4 bi .. 4 bi + 3,
+//      j = 16 jg .. 16 jg + 15 as 16 words and transposes them (4 x 4 byte
+//      blocks, byte permutes) into 4 destination rows of 16 bytes;
+//   3. 16-byte global stores: the 8 threads of a destination row write its
+//      128 bytes, a warp 4 whole rows an instruction.
+// A tile cut by the tensor's edge takes this path too when both of its
+// extents are multiples of 16 bytes (threads past them idle); other edge
+// tiles, or tiles whose rows do not allow 16-byte accesses, go byte by byte.
+// `aligned`: source and destination rows are 16-byte aligned.
 __global__ void __launch_bounds__(kThreads) permute_transpose(const uint8_t* __restrict__ src,
                                                               uint8_t* __restrict__ dst, Dims d, int ai,
                                                               int64_t tiles_i, int64_t tiles_j, int64_t units,
                                                               int aligned) {
+    __shared__ uint32_t tile[kTile * kPitchWords];
     dev::pdl_allow_next();
     dev::pdl_wait_prior();
     const int aj = d.rank - 1;
     const int64_t ni = d.dst_dims[ai], nj = d.dst_dims[aj];
     const int64_t sj = d.src_stride[aj], di = d.dst_stride[ai];
-    const int lane = threadIdx.x & 31;
-    const int bq = lane & 15, half = lane >> 4;
-    const int64_t warps = static_cast<int64_t>(gridDim.x) * (kThreads / 32);
-    for (int64_t u = static_cast<int64_t>(blockIdx.x) * (kThreads / 32) + (threadIdx.x >> 5); u < units;
-         u += warps) {
+    const int t = threadIdx.x;
+    for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
         int64_t rest = u;
         const int64_t tj = rest % tiles_j;
         rest /= tiles_j;
@@ -108,28 +116,48 @@ __global__ void __launch_bounds__(kThreads) permute_transpose(const uint8_t* __r
             dbase += idx * d.dst_stride[a];
             rest = q;
         }
-        const int64_t i = ti * kTileI + 4 * bq;    // this lane's 4 bytes of i
-        const int64_t j = tj * kTileJ + 16 * half; // this lane's 16 rows of j
-        const bool full = (ti + 1) * kTileI <= ni && (tj + 1) * kTileJ <= nj;
-        if (aligned && full) {
-            const uint8_t* s = src + sbase + i + j * sj;
-            uint32_t w[16];
+        const int64_t i0 = ti * kTile, j0 = tj * kTile;
+        const int ei = static_cast<int>(ni - i0 < kTile ? ni - i0 : kTile);  // the tile's extents
+        const int ej = static_cast<int>(nj - j0 < kTile ? nj - j0 : kTile);
+        if (aligned && ei % 16 == 0 && ej % 16 == 0) {
+            const uint8_t* s = src + sbase + i0 + j0 * sj;
+            // 1. rows j = t / 8 + 32 p, 16 bytes c = t % 8 of each
 #pragma unroll
-            for (int r = 0; r < 16; ++r) w[r] = *reinterpret_cast<const uint32_t*>(s + r * sj);
-            uint32_t o[4][4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const uint32_t in[4] = {w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]};
-                transpose4x4(in, o[k]);
+            for (int p = 0; p < 4; ++p) {
+                const int r = t / 8 + 32 * p, c = t % 8;
+                if (r < ej && 16 * c < ei) {
+                    const uint4 v = *reinterpret_cast<const uint4*>(s + r * sj + 16 * c);
+                    uint32_t* w = &tile[r * kPitchWords + 4 * c];
+                    w[0] = v.x;
+                    w[1] = v.y;
+                    w[2] = v.z;
+                    w[3] = v.w;
+                }
             }
-            uint8_t* o_row = dst + dbase + i * di + j;
+            __syncthreads();
+            // 2. thread (bi, jg): words bi of rows 16 jg .. 16 jg + 15
+            const int bi = t / 8, jg = t % 8;
+            if (4 * bi < ei && 16 * jg < ej) {
+                uint32_t o[4][4];
 #pragma unroll
-            for (int m = 0; m < 4; ++m)
-                *reinterpret_cast<uint4*>(o_row + m * di) = make_uint4(o[0][m], o[1][m], o[2][m], o[3][m]);
+                for (int k = 0; k < 4; ++k) {
+                    uint32_t in[4];
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) in[r] = tile[(16 * jg + 4 * k + r) * kPitchWords + bi];
+                    transpose4x4(in, o[k]);  // o[k][m]: row i = 4 bi + m, bytes j = 16 jg + 4 k .. + 3
+                }
+                // 3. destination rows i0 + 4 bi + m, bytes j0 + 16 jg .. + 15
+                uint8_t* o_row = dst + dbase + (i0 + 4 * bi) * di + j0 + 16 * jg;
+#pragma unroll
+                for (int m = 0; m < 4; ++m)
+                    *reinterpret_cast<uint4*>(o_row + m * di) = make_uint4(o[0][m], o[1][m], o[2][m], o[3][m]);
+            }
+            __syncthreads();  // the tile is reused by the next unit
         } else {
-            for (int m = 0; m < 4; ++m)
-                for (int r = 0; r < 16; ++r)
-                    if (i + m < ni && j + r < nj) dst[dbase + (i + m) * di + j + r] = src[sbase + (i + m) + (j + r) * sj];
+            for (int64_t e = t; e < static_cast<int64_t>(ei) * ej; e += blockDim.x) {
+                const int64_t ii = e / ej, jj = e - ii * ej;
+                dst[dbase + (i0 + ii) * di + j0 + jj] = src[sbase + i0 + ii + (j0 + jj) * sj];
+            }
         }
     }
 }
@@ -173,16 +201,15 @@ cudaError_t launch_permute_bytes(const PermuteArgs& a, cudaStream_t stream) {
     for (int i = 0; i < d.rank - 1; ++i)
         if (d.src_stride[i] == 1) ai = i;
     if (ai < 0) return cudaErrorInvalidValue;  // not a permutation of a dense tensor
-    const int64_t tiles_i = (d.dst_dims[ai] + kTileI - 1) / kTileI;
-    const int64_t tiles_j = (d.dst_dims[d.rank - 1] + kTileJ - 1) / kTileJ;
+    const int64_t tiles_i = (d.dst_dims[ai] + kTile - 1) / kTile;
+    const int64_t tiles_j = (d.dst_dims[d.rank - 1] + kTile - 1) / kTile;
     const int64_t units = total / (d.dst_dims[ai] * d.dst_dims[d.rank - 1]) * tiles_i * tiles_j;
-    // 4-byte source loads along i, 16-byte destination stores along j
-    bool aligned = (reinterpret_cast<uintptr_t>(a.src) & 3u) == 0 && (reinterpret_cast<uintptr_t>(a.dst) & 15u) == 0 &&
-                   d.src_stride[d.rank - 1] % 4 == 0 && d.dst_stride[ai] % 16 == 0;
+    // 16-byte accesses along i in the source and along j in the destination
+    bool aligned = (reinterpret_cast<uintptr_t>(a.src) & 15u) == 0 && (reinterpret_cast<uintptr_t>(a.dst) & 15u) == 0 &&
+                   d.src_stride[d.rank - 1] % 16 == 0 && d.dst_stride[ai] % 16 == 0;
     for (int i = 0; i < d.rank - 1; ++i)
-        if (i != ai) aligned = aligned && d.src_stride[i] % 4 == 0 && d.dst_stride[i] % 16 == 0;
-    const int64_t warps = (units + 7) / 8;
-    const int64_t grid = warps < cap ? warps : cap;
+        if (i != ai) aligned = aligned && d.src_stride[i] % 16 == 0 && d.dst_stride[i] % 16 == 0;
+    const int64_t grid = units < cap ? units : cap;
     return launch_pdl(permute_transpose, static_cast<unsigned>(grid), kThreads, 0, stream, a.src, a.dst, d, ai,
                       tiles_i, tiles_j, units, aligned ? 1 : 0);
 }
