@@ -49,6 +49,10 @@ def run(mx, lshape, rshape, lb, rb, lc, rc, fmt, out_dtype, seed):
 CASES = {
     "canonical_pair_kernel": ((3, 200, 256), (3, 300, 256), (0,), (0,), 2, 2),
     "rhs_k_by_n": ((2, 64, 96), (2, 96, 136), (0,), (0,), 2, 1),
+    # 16-byte aligned rows, both tile axes cut by the edge at multiples of 16
+    # bytes (N = 208 = 128 + 80, K = 160 = 128 + 32): the transposing copy's
+    # partial tiles on its shared-memory path
+    "rhs_k_by_n_partial_tiles": ((2, 64, 160), (2, 160, 208), (0,), (0,), 2, 1),
     "batch_in_middle": ((130, 2, 64), (2, 72, 64), (1,), (0,), 2, 2),
     "two_batch_dims_reordered": ((2, 3, 40, 64), (3, 2, 64, 48), (0, 1), (1, 0), 3, 2),
     "several_free_dims": ((2, 5, 7, 64), (64, 3, 40), (), (), 3, 0),
