@@ -189,16 +189,22 @@ def test_split_k_bounded_wait_times_out_without_fault(mx):
     check_gemm(c.cpu().numpy(), c_ref, s_ref, "f32")
 
 
+@pytest.mark.parametrize("fmt", ["e4m3fn", "e2m1"])
 @pytest.mark.parametrize("M,N,K,kernel", [(1024, 1024, 4096, 1), (2048, 512, 4096, 1), (300, 1000, 4096, 1),
                                           (512, 4096, 2048, 2), (256, 8192, 1024, 2)])
-def test_auto_choice_for_few_tile_problems(mx, M, N, K, kernel):
+def test_auto_choice_for_few_tile_problems(mx, fmt, M, N, K, kernel):
     # M > 128 whose 256 x 256 tiles fill at most a quarter of the pair
     # clusters runs on the 1-SM kernel with split-K; at half the clusters and
-    # more, on the pair kernel.  Every element against the oracle.
-    a, bt, sa, sb = fp8_operands(M, N, K, "e4m3fn", seed=M + N + 1)
-    c = matmul(mx, a, bt, sa, sb, "e4m3fn", "bf16")
+    # more, on the pair kernel.  Every element against the oracle.  FP4
+    # stages hold 256 K elements, so FP4 runs at twice the K.
+    if fmt == "e2m1":
+        K *= 2
+        a, bt, sa, sb = fp4_operands(M, N, K, seed=M + N + 1)
+    else:
+        a, bt, sa, sb = fp8_operands(M, N, K, fmt, seed=M + N + 1)
+    c = matmul(mx, a, bt, sa, sb, fmt, "bf16")
     got_kernel, split = mx.mx_debug_last_gemm_launch()
     assert got_kernel == kernel
     assert split > 1 if kernel == 1 else split == 1
-    c_ref, s_ref = orc.scaled_matmul(a, bt, sa, sb, "e4m3fn")
+    c_ref, s_ref = orc.scaled_matmul(a, bt, sa, sb, fmt)
     check_gemm(c.float().cpu().numpy(), c_ref, s_ref, "bf16")
