@@ -435,8 +435,10 @@ mx_status mx_debug_gemm_fault_injection(int skip_producer, uint64_t timeout_ns);
 
 /*
  * Testing hook (no counterpart on the pages): which ScaledMatmul kernel later
- * calls use.  0 = automatic (the 2-SM pair kernel when M > 128, else the
- * 1-SM kernel), 1 = always the 1-SM kernel, 2 = always the pair kernel,
+ * calls use.  0 = automatic (the 1-SM kernel when M <= 128, and when M > 128
+ * but the pair kernel's 256 x 256 tiles would fill at most a quarter of its
+ * clusters while the 1-SM kernel can split K at least two ways; otherwise
+ * the 2-SM pair kernel), 1 = always the 1-SM kernel, 2 = always the pair kernel,
  * 3 = always the 1-SM kernel and never split K.  The 1-SM kernel splits K
  * over a cluster of up to 8 CTAs per tile when the problem has too few
  * tiles to fill the GPU (small M); the slices' f32 partial sums are added in
