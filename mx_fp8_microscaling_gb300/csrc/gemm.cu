@@ -33,7 +33,9 @@
 // elements and two scale tiles along K.
 //
 //   mx_gemm_kernel      1 SM per 128 x 256 tile (M = 128 MMA), 4 stages of
-//                       A 16 KB + B 32 KB + scales 1.5 KB.  Used for M <= 128.
+//                       A 16 KB + B 32 KB + scales 1.5 KB.  Used for M <= 128
+//                       and for problems with too few tiles for the pair
+//                       kernel (see prefer_pair).
 //                       When the tiles are too few to fill the GPU it splits K:
 //                       a cluster of S <= 8 CTAs per tile, CTA s accumulating
 //                       the s-th slice of the K stages; each slice's f32 tile
