@@ -26,7 +26,9 @@
 //               convert (f32, or bf16 round-to-nearest-even) and store rows to
 //               global memory while the next tile's main loop runs.  Stores are
 //               256-bit (a whole 32-byte sector each) where the rows allow:
-//               4 % faster than 128-bit ones at 8192^3.
+//               4 % faster than 128-bit ones at 8192^3.  In the pair kernel
+//               the CTA that issues the MMAs paces its stores by the MMA
+//               thread's progress through the next tile (see the epilogue).
 //
 // Both kernels also run MXFP4 (packed e2m1 operands, kind::mxf4 with
 // scale_vec::2X, K = 64 per MMA): a 128-byte stage row then holds 256 K
@@ -265,6 +267,46 @@ __device__ __forceinline__ void store_row128(const KParams& p, int b, int64_t m,
                 for (int i = 0; i < 32; ++i)
                     if (n0 + 32 * j + i < p.N) crow[32 * j + i] = __uint_as_float(v[j][i]);
         }
+    }
+}
+
+// Columns [n, n + 8 x 32-bit words) of row m of problem b: 16 bf16 columns
+// (w = packed pairs) or 8 f32 columns; columns past N are skipped.
+__device__ __forceinline__ void store_row_chunk(const KParams& p, int b, int64_t m, int64_t n, const uint32_t (&w)[8]) {
+    if (m >= p.M || n >= p.N) return;
+    const int64_t row = static_cast<int64_t>(b) * p.c_batch_stride + m * p.ldc + n;
+    const int cols = p.out_bf16 ? 16 : 8;
+    void* dst = p.out_bf16 ? static_cast<void*>(reinterpret_cast<uint16_t*>(p.c) + row)
+                           : static_cast<void*>(reinterpret_cast<float*>(p.c) + row);
+    if (p.vec_store && n + cols <= p.N) {
+        if ((reinterpret_cast<uintptr_t>(dst) & 31u) == 0) {
+            st_v8(dst, w[0], w[1], w[2], w[3], w[4], w[5], w[6], w[7]);
+        } else {
+            reinterpret_cast<uint4*>(dst)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+            reinterpret_cast<uint4*>(dst)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        }
+    } else if (p.out_bf16) {
+        uint16_t* c = static_cast<uint16_t*>(dst);
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            if (n + i < p.N) c[i] = static_cast<uint16_t>(w[i >> 1] >> (16 * (i & 1)));
+    } else {
+        float* c = static_cast<float*>(dst);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            if (n + i < p.N) c[i] = __uint_as_float(w[i]);
+    }
+}
+
+// Wait (lane 0, bounded) until the MMA thread has issued `target` K stages in
+// all, counting from the kernel's start (a 32-bit count that may wrap).
+__device__ __forceinline__ void wait_mma_progress(const volatile uint32_t* issued, uint32_t target,
+                                                  volatile int* abort_flag, uint64_t limit_ns) {
+    if (static_cast<int32_t>(*issued - target) >= 0) return;
+    const uint64_t t0 = globaltimer_ns();
+    while (static_cast<int32_t>(*issued - target) < 0) {
+        if (*abort_flag || globaltimer_ns() - t0 > limit_ns) return;
+        __nanosleep(128);
     }
 }
 
@@ -634,6 +676,12 @@ constexpr uint32_t PAIR_TX = 2 * (A_STAGE + B_STAGE);  // both CTAs' operand til
 __host__ __device__ constexpr uint32_t pair_sf_tx(bool fp4) { return 2 * 3 * sfa_group(fp4); }
 constexpr int SF_WARP = 10;              // warp that copies scale factors to tensor memory
 constexpr int THREADS = NUM_THREADS + 32;
+// Rank 0's C stores are paced over the first kPaceNum / kPaceDen of the next
+// tile's K stages, when a tile has at least kPaceMinStages of them (A/B at
+// 8192 x 8192, CUDA events: FP8 K = 8192 / 2048 +0.9 / +4.5 %, MXFP4 +2 %;
+// spreading over the whole next tile was slower at K = 1024, where unpaced
+// stores are kept).
+constexpr int kPaceNum = 1, kPaceDen = 2, kPaceMinStages = 16;
 }  // namespace sm2
 
 // Scale-factor buffers are read by TMA as [2 * tiles, 256] bytes: a 512-byte
@@ -669,6 +717,7 @@ __global__ void __launch_bounds__(sm2::THREADS, 1)
     auto sfg_empty_bar = [&](int g) { return sb + OFF_BAR + 8u * (3 * STAGES + 4 + SF_SLOTS + g); };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
+    volatile uint32_t* mma_issued = reinterpret_cast<volatile uint32_t*>(smem + OFF_MISC + 8);  // K stages so far
 
     pdl_allow_next();
     if (threadIdx.x == 0) {
@@ -686,6 +735,7 @@ __global__ void __launch_bounds__(sm2::THREADS, 1)
         mbar_init(mma_done, 1);
         mbar_init(sf_done, 1);
         *abort_flag = 0;
+        *mma_issued = 0;
         fence_mbar_init();
         prefetch_tmap(&tmap_a);
         prefetch_tmap(&tmap_b);
@@ -793,7 +843,7 @@ __global__ void __launch_bounds__(sm2::THREADS, 1)
     } else if (warp == 1) {
         if (lane == 0 && rank == 0) {
             int stage = 0;
-            uint32_t phase = 0, acc_phase = 0;
+            uint32_t phase = 0, acc_phase = 0, issued = 0;
             bool ok = true;
             for (int u = 0; u < num_units && ok; ++u) {
                 const bool half_tile = p.split_tail && u >= p.full_rounds;
@@ -832,6 +882,7 @@ __global__ void __launch_bounds__(sm2::THREADS, 1)
                         }
                     }
                     tc_commit_pair_mc(empty_bar(stage), 3);
+                    *mma_issued = ++issued;
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
@@ -935,18 +986,58 @@ __global__ void __launch_bounds__(sm2::THREADS, 1)
             __syncwarp();
             // Release the accumulator: rank 0's warps arrive locally; rank 1's
             // meet on a named barrier and one thread arrives across the
-            // cluster (eight remote release-arrives cost about 0.4 us more
-            // per tile: 5 % at 8192^3, 15 % at K = 2048).
+            // cluster, relaxed (eight remote release-arrives cost about 0.4 us
+            // more per tile: 5 % at 8192^3, 15 % at K = 2048).
             if (rank == 0) {
                 if (lane == 0) mbar_arrive(tmem_empty);
             } else {
                 named_bar_sync(kEpiBarrier, NUM_EPI_WARPS * 32);
-                if (warp == 2 && lane == 0) mbar_arrive_cluster(tmem_empty_rank0);
+                if (warp == 2 && lane == 0) mbar_arrive_cluster_relaxed(tmem_empty_rank0);
             }
             acc_phase ^= 1u;
-            if (live)
-                store_row128(p, b, static_cast<int64_t>(mt) * BM + rank * 128 + quarter * 32 + lane,
-                             static_cast<int64_t>(nt) * BN + (hf < 0 ? half : hf) * 128, v);
+            if (!live) continue;
+            // Rank 0 (the CTA that issues the MMAs and holds the pipeline's
+            // barriers) stores its rows in 8 KB steps paced by the MMA
+            // thread's progress through the next tile: C leaving that SM in
+            // one 64 KB burst (from registers or through TMA stores alike)
+            // held up the tensor core's completion signals the MMA thread
+            // waits on (the next tile's first scale copies) by about 1.2 us
+            // a tile, where the same bytes written to shared memory cost
+            // nothing.  Rank 1's stores cost nothing measurable and go at once.
+            const int64_t m = static_cast<int64_t>(mt) * BM + rank * 128 + quarter * 32 + lane;
+            const int64_t n0 = static_cast<int64_t>(nt) * BN + (hf < 0 ? half : hf) * 128;
+            const bool paced = rank == 0 && u + 1 < num_units && p.num_kb >= kPaceMinStages;
+            const uint32_t next_tile = static_cast<uint32_t>(u + 1) * static_cast<uint32_t>(p.num_kb);
+            auto pace = [&](int c, int chunks) {
+                if (!paced) return;
+                if (lane == 0)
+                    wait_mma_progress(
+                        mma_issued,
+                        next_tile + static_cast<uint32_t>((c * p.num_kb * kPaceNum) / (chunks * kPaceDen)) + 1u,
+                        abort_flag, p.timeout_ns);
+                __syncwarp();
+            };
+            uint32_t w[8];
+            if (p.out_bf16) {
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {  // 16 columns a step
+                    const uint32_t* x = &v[c >> 1][16 * (c & 1)];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        w[i] = pack_bf16x2(__uint_as_float(x[2 * i]), __uint_as_float(x[2 * i + 1]));
+                    pace(c, 8);
+                    store_row_chunk(p, b, m, n0 + 16 * c, w);
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < 16; ++c) {  // 8 columns a step
+                    const uint32_t* x = &v[c >> 2][8 * (c & 3)];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) w[i] = x[i];
+                    pace(c, 16);
+                    store_row_chunk(p, b, m, n0 + 8 * c, w);
+                }
+            }
         }
     }
 

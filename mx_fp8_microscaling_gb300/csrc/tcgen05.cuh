@@ -254,9 +254,14 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// Arrive on an mbarrier of any CTA of the cluster (release at cluster scope).
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+// Arrive on an mbarrier of any CTA of the cluster, relaxed: the arrive
+// publishes no memory writes, it only signals an event (e.g. "this CTA's
+// tensor-memory loads have completed", which tcgen05.wait::ld already
+// guarantees before the arrive issues).  With release semantics the peer saw
+// the arrive about 1.8 us after it issued while the SM had C stores in
+// flight; relaxed, about 0.1 us once those stores are paced.
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
 // 2-D TMA load into this CTA's shared memory whose completion is counted on
