@@ -1141,26 +1141,33 @@ KParams base_params(const GemmArgs& g, int bm, int bn) {
 constexpr int kMinStagesPerSlice = 4;  // K stages each split-K slice accumulates at least
 
 // The kernels' dynamic shared memory exceeds the default limit: set the
-// attribute once, before any launch or occupancy query.
+// attribute before any launch or occupancy query, once per device (a
+// function attribute belongs to the device it was set on).
+template <typename Kernel>
+cudaError_t ensure_smem_attr(Kernel kernel, uint32_t bytes, std::mutex& mu, bool (&done)[64]) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    std::lock_guard<std::mutex> lock(mu);
+    if (!done[dev]) {
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        if (e != cudaSuccess) return e;
+        done[dev] = true;
+    }
+    return cudaSuccess;
+}
 template <bool FP4>
 cudaError_t ensure_1sm_attr() {
-    static std::once_flag once;
-    static cudaError_t err = cudaSuccess;
-    std::call_once(once, [] {
-        err = cudaFuncSetAttribute(mx_gemm_kernel<FP4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   sm1::smem_alloc(FP4));
-    });
-    return err;
+    static std::mutex mu;
+    static bool done[64] = {};
+    return ensure_smem_attr(mx_gemm_kernel<FP4>, sm1::smem_alloc(FP4), mu, done);
 }
 template <bool FP4>
 cudaError_t ensure_2sm_attr() {
-    static std::once_flag once;
-    static cudaError_t err = cudaSuccess;
-    std::call_once(once, [] {
-        err = cudaFuncSetAttribute(mx_gemm_2sm_kernel<FP4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   sm2::smem_alloc(FP4));
-    });
-    return err;
+    static std::mutex mu;
+    static bool done[64] = {};
+    return ensure_smem_attr(mx_gemm_2sm_kernel<FP4>, sm2::smem_alloc(FP4), mu, done);
 }
 
 // attr: room for 2 (cluster shape, programmatic serialization)
