@@ -310,7 +310,10 @@ mx_status mx_scaled_matmul(const void* a, const void* bt, const uint8_t* a_scale
  *   (M = N = K = 8192 fits); larger problems get MX_ERR_WORKSPACE.
  *   The array takes 4 MiB on every device that loads the library, until
  *   process exit.  The first call on a device looks up the array's device
- *   address (make that first call before any stream capture on the device).
+ *   address (make that first call before any stream capture on the device)
+ *   and keeps it for the life of the process: do not use this call on a
+ *   device after cudaDeviceReset there (the library's device arrays are
+ *   loaded again, possibly at another address).
  *   Every call shares the array: calls whose kernels may overlap on the GPU
  *   (unordered streams) race on it; calls ordered on one stream are safe.
  */

@@ -32,6 +32,12 @@ MUTANTS = {
     "e5m2_max_code_7c": ("57344.0, 0x7Bu", "57344.0, 0x7Cu"),
     "nan_fp4_not_zero": ("if (isnan(y)) return (uint8_t)(s << 3);", "if (isnan(y)) return (uint8_t)((s << 3) | 7);"),
     "matmul_scale_column": ("sb[n * kb + k / 32]", "sb[n * kb + (k / 32 + 1) % kb]"),
+    "nan_e4m3_to_max": ("if (isnan(y)) return (uint8_t)(0x7Fu | (s << 7));\n    return (uint8_t)(nearest_code(fabs((double)y), 3",
+                        "if (isnan(y)) return (uint8_t)(0x7Eu | (s << 7));\n    return (uint8_t)(nearest_code(fabs((double)y), 3"),
+    "nan_e5m2_to_max": ("if (isnan(y)) return (uint8_t)(0x7Fu | (s << 7));\n    return (uint8_t)(nearest_code(fabs((double)y), 2",
+                        "if (isnan(y)) return (uint8_t)(0x7Bu | (s << 7));\n    return (uint8_t)(nearest_code(fabs((double)y), 2"),
+    "nan_fp8_sign_dropped": ("if (isnan(y)) return (uint8_t)(0x7Fu | (s << 7));\n    return (uint8_t)(nearest_code(fabs((double)y), 3",
+                             "if (isnan(y)) return (uint8_t)(0x7Fu);\n    return (uint8_t)(nearest_code(fabs((double)y), 3"),
 }
 
 

@@ -234,10 +234,30 @@ def test_narrow_matches_torch_after_clamp(fmt):
 
 
 def test_fp8_nan_reading():
-    # reading (parity unpinned): NaN -> 0x7F | sign for both FP8 formats
+    # reading (the pages fix no NaN code): NaN -> 0x7F | sign for both FP8 formats
     for fmt in FP8:
         assert orc.narrow(fmt, math.nan) == 0x7F
         assert orc.narrow(fmt, -math.nan) == 0xFF
+
+
+@pytest.mark.parametrize("fmt", FP8)
+def test_fp8_nan_code_is_a_nan_of_the_format(fmt):
+    # What the format definitions do fix, independently of the reading above:
+    # a NaN input must come out as a code that the format decodes as NaN
+    # (torch's float8 decoder, a library routine), carrying the input's sign
+    # bit; no finite input may produce such a code.
+    for sign, x in ((0, math.nan), (1, -math.nan)):
+        c = orc.narrow(fmt, x)
+        v = torch.tensor([c], dtype=torch.uint8).view(TORCH_FP8[fmt]).float().item()
+        assert math.isnan(v), (fmt, hex(c))
+        assert c >> 7 == sign, (fmt, hex(c))
+    # inside a block: the NaN element decodes as NaN, its finite neighbours
+    # stay finite
+    bits = np.array([[0x3F80, 0x7FC0, 0xFFC0, 0xC040] * 8], np.uint16)  # 1, NaN, -NaN, -3
+    q, _ = orc.quantize(bits, "bf16", fmt, geometry="1x32", dim=-1)
+    dec = torch.from_numpy(np.ascontiguousarray(q[0, :4])).view(TORCH_FP8[fmt]).float().numpy()
+    assert np.isnan(dec[1]) and np.isnan(dec[2]) and np.isfinite(dec[0]) and np.isfinite(dec[3])
+    assert int(q[0, 1]) >> 7 == 0 and int(q[0, 2]) >> 7 == 1
 
 
 @pytest.mark.parametrize("fmt", ALL_FMTS)
