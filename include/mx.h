@@ -324,7 +324,10 @@ mx_status mx_scaled_matmul_noalloc(const void* a, const void* bt, const uint8_t*
 
 /*
  * Workspace bytes of mx_fused_quantize_matmul: the quantized activation
- * (M*K bytes) and its SF-layout scales, each 16-byte aligned.
+ * (M*K bytes, at offset 0), its SF-layout scales (at offset
+ * round16(M*K)), then ceil(M/128) * ceil(K/256) 64-bit ready words (at
+ * offset round16(M*K) + round16(ceil(M/128) * ceil(K/128) * 512)), each
+ * part 16-byte aligned; round16(x) rounds x up to a multiple of 16.
  */
 mx_status mx_fused_quantize_matmul_workspace(int64_t M, int64_t N, int64_t K, size_t* bytes);
 
@@ -335,6 +338,22 @@ mx_status mx_fused_quantize_matmul_workspace(int64_t M, int64_t N, int64_t K, si
  * and multiplied by a pre-quantized weight given K-contiguous as
  * Wt [N, K] with SF-layout scales.  The result equals QuantizeMX(X) followed
  * by mx_scaled_matmul bit for bit in the quantized operand.
+ *   Where the pair GEMM kernel takes the product (M > 128 and enough 256 x 256
+ *   tiles; see mx_debug_set_gemm_variant) and x is 32-byte aligned with a
+ *   row pitch of a multiple of 32 bytes, the call is ONE kernel launch: its
+ *   epilogue warps quantize X in items of 128 rows x 256 elements, in the
+ *   order the tiles consume them, while the tensor cores run, and publish
+ *   each item through a ready word in the workspace that the operand loads
+ *   wait on (bounded; a wait that runs out records MX_ERR_TIMEOUT).  Other
+ *   shapes run QuantizeMX, then mx_scaled_matmul, on the stream.  Either way
+ *   the workspace holds QuantizeMX(X) afterwards (codes and SF-layout scales
+ *   at the offsets above; scale bytes of rows past M are unspecified).  The
+ *   ready words need no clearing: a launch only accepts words it wrote itself
+ *   (a per-call tag), and one that completes leaves them all zero, so
+ *   reusing a workspace, and replaying a captured call, are both safe.
+ *   After a call that ended in MX_ERR_TIMEOUT, zero the ready words before
+ *   replaying that captured call.  Calls that share a workspace must not
+ *   overlap on the GPU.
  *   x, x_dtype   device [M, ld_x] MX_BF16 | MX_F16
  *   wt, w_scale_sf  device codes [N, K] and SF-layout scales (mx_repack_scales);
  *                for MX_E2M1 X is packed in the tensor-core nibble order
@@ -429,10 +448,12 @@ int mx_version(void);
 
 /*
  * Testing hook for the bounded-wait path (no counterpart on the pages).
- * skip_producer = 1 makes later mx_scaled_matmul launches issue no loads, so
- * their waits run out after `timeout_ns` (0 = the default of 2 s) and record
- * MX_ERR_TIMEOUT in the device status word, with no fault and no hang.
- * skip_producer = 0 restores normal operation.  Not thread-safe; host only.
+ * skip_producer bit 0 makes later GEMM launches issue no loads; bit 1 makes
+ * the single-launch mx_fused_quantize_matmul never publish its quantize
+ * items (so its loads never start).  Either way the kernels' waits run out
+ * after `timeout_ns` (0 = the default of 2 s) and record MX_ERR_TIMEOUT in
+ * the device status word, with no fault and no hang.  skip_producer = 0
+ * restores normal operation.  Not thread-safe; host only.
  */
 mx_status mx_debug_gemm_fault_injection(int skip_producer, uint64_t timeout_ns);
 
@@ -442,7 +463,10 @@ mx_status mx_debug_gemm_fault_injection(int skip_producer, uint64_t timeout_ns);
  * but the pair kernel's 256 x 256 tiles would fill at most a quarter of its
  * clusters while the 1-SM kernel can split K at least two ways; otherwise
  * the 2-SM pair kernel), 1 = always the 1-SM kernel, 2 = always the pair kernel,
- * 3 = always the 1-SM kernel and never split K.  The 1-SM kernel splits K
+ * 3 = always the 1-SM kernel and never split K, 4 = automatic, but
+ * mx_fused_quantize_matmul always as two launches (QuantizeMX, then
+ * ScaledMatmul).  Under 2 the fused call runs as one launch whenever its
+ * input allows it; under 1 and 3 it runs as two.  The 1-SM kernel splits K
  * over a cluster of up to 8 CTAs per tile when the problem has too few
  * tiles to fill the GPU (small M); the slices' f32 partial sums are added in
  * slice order, so a given shape always gives the same bits.  All variants
@@ -454,7 +478,7 @@ mx_status mx_debug_set_gemm_variant(int variant);
 /*
  * Testing hook (no counterpart on the pages): the kernel of the last
  * ScaledMatmul launch made by this process (*kernel: 1 = 1-SM, 2 = pair,
- * 0 = none yet) and its split-K factor (*split_k: CTAs per tile along K, 1 =
+ * 3 = pair with the fused activation quantize, 0 = none yet) and its split-K factor (*split_k: CTAs per tile along K, 1 =
  * no split).  MX_ERR_INVALID_ARG if a pointer is NULL.  Host only.
  */
 mx_status mx_debug_last_gemm_launch(int* kernel, int* split_k);

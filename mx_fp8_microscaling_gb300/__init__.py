@@ -459,19 +459,25 @@ def mx_version() -> int:
     return _lib.mx_version()
 
 
-def mx_debug_gemm_fault_injection(skip_producer: bool, timeout_ns: int = 0):
+def mx_debug_gemm_fault_injection(skip_producer: int, timeout_ns: int = 0):
+    """Bit 0: the GEMMs issue no loads; bit 1: the fused single launch never
+    publishes its quantize items.  Either makes the kernels' bounded waits run
+    out after ``timeout_ns`` (0 restores the 2 s default)."""
     _check(_lib.mx_debug_gemm_fault_injection(int(skip_producer), timeout_ns), "mx_debug_gemm_fault_injection")
 
 
 def mx_debug_set_gemm_variant(variant: int):
     """0 automatic, 1 force the 1-SM ScaledMatmul kernel, 2 force the 2-SM pair
-    kernel, 3 force the 1-SM kernel without split-K."""
+    kernel (the fused call then runs as one launch whenever its input allows),
+    3 force the 1-SM kernel without split-K, 4 automatic with the fused call
+    as two launches (QuantizeMX, then ScaledMatmul)."""
     _check(_lib.mx_debug_set_gemm_variant(int(variant)), "mx_debug_set_gemm_variant")
 
 
 def mx_debug_last_gemm_launch():
     """(kernel, split_k) of the last ScaledMatmul launch: kernel 1 = 1-SM,
-    2 = pair, 0 = none yet; split_k = CTAs per tile along K."""
+    2 = pair, 3 = pair with the fused activation quantize (one launch for
+    the whole fused call), 0 = none yet; split_k = CTAs per tile along K."""
     kernel, split = ctypes.c_int(0), ctypes.c_int(0)
     _check(_lib.mx_debug_last_gemm_launch(ctypes.byref(kernel), ctypes.byref(split)), "mx_debug_last_gemm_launch")
     return kernel.value, split.value

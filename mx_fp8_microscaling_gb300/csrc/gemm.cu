@@ -62,6 +62,8 @@
 // leave their loops, wait for their own asynchronous work, free tensor memory
 // and return.
 
+#include <atomic>
+#include <chrono>
 #include <cstdint>
 #include <mutex>
 
@@ -71,6 +73,7 @@
 #include "mx_device.cuh"
 #include "mx_internal.h"
 #include "pdl.cuh"
+#include "quant_math.cuh"
 #include "tcgen05.cuh"
 
 namespace mx {
@@ -114,6 +117,22 @@ struct KParams {
     int split_k;          // 1-SM kernel: CTAs (one cluster) per tile, each a slice of K; 1 = none
     uint64_t timeout_ns;
     int skip_producer;   // fault injection: never issue loads (waits must time out)
+    // Fused activation quantize (pair kernel instantiated with QFMT >= 0):
+    // X [M, K] bf16/f16 is quantized along K into the A operand (q_xq) and
+    // its SF-layout scales (q_sf, the buffer sfa points to), in items of 128
+    // rows x kQChunk elements that the epilogue warps take between tiles.
+    const uint8_t* q_x;
+    int64_t q_ld_x;       // bytes between rows of X
+    uint8_t* q_xq;        // codes [M, K] (FP8) or [M, K / 2] (e2m1)
+    uint8_t* q_sf;
+    uint64_t* q_flags;    // one ready word per item, [q_panels, q_nkc]
+    uint64_t q_tag;       // this launch's tag, 40 bits, nonzero (see wait_item_ready)
+    int q_f16;            // X is f16 (else bf16)
+    int q_panels;         // 128-row panels of X
+    int q_nkc;            // items along K per panel
+    int q_lookahead;      // tile groups past the CTA's current one whose items it may quantize
+    int q_emax;           // EMAX of the element format
+    int q_no_publish;     // fault injection: items are never published (the loads' waits time out)
 };
 
 // Tile order: problem by problem; inside one, groups of `group_m` M-tiles,
@@ -333,6 +352,164 @@ __device__ __forceinline__ void store_chunk4(const KParams& p, int b, int64_t m,
                 if (n + i < p.N) c[i] = e[i];
         }
     }
+}
+
+// ============================================ fused activation quantize
+
+// One quantize item: 128 rows (a 128-row panel of A, the rows of one
+// scale-factor tile) x kQChunk elements of X along K, done by the 256 threads
+// of the 8 epilogue warps.  Items are numbered in the order the tiles consume
+// them: tile group by tile group (kQPanelsPerGroup panels each, the group_m
+// pair M-tiles of the tile order), inside a group K chunk by K chunk, panel
+// by panel; CTA c takes items c, c + gridDim.x, ...
+constexpr int kQChunk = 256;            // K elements per item: 2 FP8 stages, 1 FP4 stage
+constexpr int kQPanelsPerGroup = 32;    // 128-row panels in a group of 16 pair M-tiles
+
+struct QItem {
+    int group, panel, kc;
+};
+__device__ __forceinline__ QItem q_item(const KParams& p, int i) {
+    const int per_group = kQPanelsPerGroup * p.q_nkc;
+    QItem it;
+    it.group = i / per_group;
+    const int j = i - it.group * per_group;
+    const int gp = min(kQPanelsPerGroup, p.q_panels - it.group * kQPanelsPerGroup);
+    it.kc = j / gp;
+    it.panel = it.group * kQPanelsPerGroup + (j - it.kc * gp);
+    return it;
+}
+
+// QuantizeMX of one item, 1x32 blocks along K, EMAX (the arithmetic of the
+// standalone quantizer, qdev::): thread t takes 16 consecutive elements of 8
+// rows (rows t/16 + 16 r), so a half-warp reads 512 contiguous bytes of a
+// row and a lane pair holds one block; one xor shuffle finishes the block
+// maximum.  Codes go to q_xq, scales to their SF-layout bytes; scale
+// columns past K inside the last scale tile are written as zero (E8M0 0, so
+// the zero codes the tensor core reads there contribute exactly 0).  All 256
+// threads then fence, meet, and one publishes the item's ready word.
+template <bool F16, int QFMT>
+__device__ __noinline__ void quant_item(const KParams& p, int i, int tid) {
+    using namespace qdev;
+    const QItem it = q_item(p, i);
+    const int col16 = tid & 15;
+    const int64_t k0 = static_cast<int64_t>(it.kc) * kQChunk + col16 * 16;
+    const bool kin = k0 < p.K;
+    const int64_t row0 = static_cast<int64_t>(it.panel) * 128 + (tid >> 4);
+    uint32_t v[8][8];
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+        const int64_t row = row0 + 16 * r;
+        if (kin && row < p.M) {
+            ld_stream_v8(p.q_x + row * p.q_ld_x + k0 * 2, v[r]);
+        } else {
+#pragma unroll
+            for (int w = 0; w < 8; ++w) v[r][w] = 0;
+        }
+    }
+    uint32_t e[8];
+    float sc[8];
+    bool special = false;
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+        uint32_t m = vmax_u16x2(vmax_u16x2(vmax_u16x2(mag2(v[r][0]), mag2(v[r][1])),
+                                           vmax_u16x2(mag2(v[r][2]), mag2(v[r][3]))),
+                                vmax_u16x2(vmax_u16x2(mag2(v[r][4]), mag2(v[r][5])),
+                                           vmax_u16x2(mag2(v[r][6]), mag2(v[r][7]))));
+        m = hmax(m);
+        m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
+        const uint32_t x = exp_byte_of_mag<F16>(m);
+        special |= (x == 255u);
+        e[r] = e8m0_of(x, p.q_emax);
+        sc[r] = prescale_mul(e[r]);
+    }
+    const int64_t kb32 = k0 >> 5;  // this lane pair's scale column
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+        const int64_t row = row0 + 16 * r;
+        if (row >= p.M) break;
+        if (kin) {
+            uint32_t w[4];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const uint32_t hw[4] = {v[r][4 * h], v[r][4 * h + 1], v[r][4 * h + 2], v[r][4 * h + 3]};
+                // e2m1: the tensor cores' order, element 2i in the low nibble
+                quantize8<F16, QFMT>(hw, sc[r], sc[r], special, 1, 0x3210u, w[2 * h], w[2 * h + 1]);
+            }
+            if constexpr (QFMT == kE2M1) {
+                *reinterpret_cast<uint2*>(p.q_xq + row * (p.K / 2) + k0 / 2) = make_uint2(w[0], w[2]);
+            } else {
+                *reinterpret_cast<uint4*>(p.q_xq + row * p.K + k0) = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+        }
+        if ((col16 & 1) == 0 && kb32 < 4 * static_cast<int64_t>(p.sf_ntk)) {
+            const int64_t tile = (row >> 7) * p.sf_ntk + (kb32 >> 2);
+            p.q_sf[tile * 512 + (row & 31) * 16 + ((row >> 5) & 3) * 4 + (kb32 & 3)] =
+                static_cast<uint8_t>(kin ? e[r] : 0u);
+        }
+    }
+    // publish: every writer's stores ordered before the ready word, for the
+    // generic and the async (TMA) proxy alike
+    fence_proxy_async_global();
+    __threadfence();
+    named_bar_sync(kEpiBarrier, NUM_EPI_WARPS * 32);
+    if (tid == 0 && !p.q_no_publish)
+        st_release_gpu_u64(p.q_flags + static_cast<int64_t>(it.panel) * p.q_nkc + it.kc, p.q_tag << 24);
+}
+
+template <int QFMT>
+__device__ __forceinline__ void quant_item_any(const KParams& p, int i, int tid) {
+    if constexpr (QFMT >= 0) {
+        if (p.q_f16) quant_item<true, QFMT>(p, i, tid);
+        else quant_item<false, QFMT>(p, i, tid);
+    }
+}
+
+// Work units (whole tiles, or the two halves of a split tail tile) whose
+// tile has pair M-tile mt: each loads panel 2 mt + rank once per item.
+__device__ __forceinline__ int units_of_m_tile(const KParams& p, int mt, int num_clusters) {
+    const int g = mt / p.group_m;
+    const int first_m = g * p.group_m;
+    const int gm = min(p.num_m_tiles - first_m, p.group_m);
+    if (!p.split_tail) return p.num_n_tiles;
+    // tiles of this mt are t(nt) = g group_m num_n + nt gm + (mt - first_m);
+    // those at or past full_rounds * clusters run as two halves
+    const int64_t base = static_cast<int64_t>(g) * p.group_m * p.num_n_tiles + (mt - first_m);
+    const int64_t tail_start = static_cast<int64_t>(p.full_rounds) * num_clusters;
+    int64_t nt_min = tail_start <= base ? 0 : (tail_start - base + gm - 1) / gm;
+    if (nt_min > p.num_n_tiles) nt_min = p.num_n_tiles;
+    return p.num_n_tiles + static_cast<int>(p.num_n_tiles - nt_min);
+}
+
+// Ready words.  An item's writer stores (tag << 24): the launch's 40-bit tag
+// with a zero count.  Every work unit that loads the item's panel waits
+// (bounded) until the word carries this launch's tag, then adds 1; the unit
+// that makes the count reach the panel's unit count (units_of_m_tile) sets
+// the word back to 0.  So a launch that completes leaves every word 0 (a
+// replay of the same launch, same tag, waits for its own items), a word from
+// an earlier launch never carries this launch's tag, and a word of fresh
+// memory matches it only by a 2^-40 chance.  After the wait the thread's
+// later TMA loads are ordered after the item's stores.  Gives up like
+// mbar_wait_bounded (MX_ERR_TIMEOUT, abort flag).
+__device__ __forceinline__ bool wait_item_ready(const KParams& p, int panel, int kc, int consumers,
+                                                volatile int* abort_flag) {
+    uint64_t* w = p.q_flags + static_cast<int64_t>(panel) * p.q_nkc + kc;
+    if ((ld_acquire_gpu_u64(w) >> 24) != p.q_tag) {
+        const uint64_t t0 = globaltimer_ns();
+        for (;;) {
+            __nanosleep(64);
+            if ((ld_acquire_gpu_u64(w) >> 24) == p.q_tag) break;
+            if (*abort_flag) return false;
+            if (globaltimer_ns() - t0 > p.timeout_ns) {
+                atomicCAS(&g_mx_status, 0, 9);
+                *abort_flag = 1;
+                return false;
+            }
+        }
+    }
+    fence_proxy_async_global();
+    const unsigned long long seen = atomicAdd(reinterpret_cast<unsigned long long*>(w), 1ull);
+    if (static_cast<int>(seen & 0xFFFFFFull) + 1 == consumers) atomicExch(reinterpret_cast<unsigned long long*>(w), 0ull);
+    return true;
 }
 
 // ====================================================== 1-SM, 128 x 256 tiles
@@ -687,7 +864,7 @@ constexpr int kPaceNum = 1, kPaceDen = 2, kPaceMinStages = 16;
 // Scale-factor buffers are read by TMA as [2 * tiles, 256] bytes: a 512-byte
 // tile t is rows 2t and 2t+1; one box is a scale group's consecutive tiles;
 // tiles past the end read as zeros.
-template <bool FP4>
+template <bool FP4, int QFMT>
 __global__ void __launch_bounds__(sm2::THREADS, 1)
     mx_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                        const __grid_constant__ CUtensorMap tmap_sfa, const __grid_constant__ CUtensorMap tmap_sfb,
@@ -699,6 +876,7 @@ __global__ void __launch_bounds__(sm2::THREADS, 1)
     constexpr uint32_t PAIR_SF_TX = pair_sf_tx(FP4);
     constexpr int SF_TILES_PER_STAGE = FP4 ? 2 : 1;
     constexpr int SF_GROUP = sf_group(FP4), SF_SLOTS = sf_slots(FP4);
+    constexpr bool FUSED = QFMT >= 0;  // quantize X into the A operand inside this launch
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sb = smem_u32(smem);
@@ -787,6 +965,20 @@ __global__ void __launch_bounds__(sm2::THREADS, 1)
                     if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, p.timeout_ns, &g_mx_status)) {
                         ok = false;
                         break;
+                    }
+                    if constexpr (FUSED) {
+                        // the A rows and scales of this stage's scale group
+                        // (FP8: 8 stages = 4 items; FP4: 1 stage = 1 item)
+                        // must have been quantized and published
+                        const int panel = 2 * mt + static_cast<int>(rank);
+                        if (group_start && panel < p.q_panels) {
+                            const int kc0 = FP4 ? kb : kb / 2;
+                            const int kc1 = min(kc0 + (FP4 ? 1 : SF_GROUP / 2), p.q_nkc);
+                            const int consumers = units_of_m_tile(p, mt, num_clusters);
+                            for (int kc = kc0; kc < kc1 && ok; ++kc)
+                                ok = wait_item_ready(p, panel, kc, consumers, abort_flag);
+                            if (!ok) break;
+                        }
                     }
                     const uint32_t fb = mapa_shared(full_bar(stage), 0);
                     constexpr bool own_bar = SF_GROUP > 1;  // group bytes on a barrier of their own
@@ -961,16 +1153,37 @@ __global__ void __launch_bounds__(sm2::THREADS, 1)
         const int quarter = warp & 3;
         const int half = (warp - 2) >> 2;
         const uint32_t tmem_empty_rank0 = mapa_shared(tmem_empty, 0);
+        const int epi_tid = threadIdx.x - 64;  // 0 .. 255
+        // fused: this CTA's next quantize item and the item count
+        int q_next = static_cast<int>(blockIdx.x);
+        const int q_total = FUSED ? p.q_panels * p.q_nkc : 0;
         uint32_t acc_phase = 0;
         for (int u = 0; u < num_units; ++u) {
             int b, mt, nt, hf;
             pair_unit_coords(u, p, cluster, num_clusters, b, mt, nt, hf);
+            if constexpr (FUSED) {
+                // Until the accumulator is ready, quantize items of X.  One
+                // thread decides for all eight warps (they meet on named
+                // barriers inside an item), so an accumulator that becomes
+                // ready waits at most one item.  Items more than q_lookahead
+                // tile groups ahead of this tile wait for a later tile.
+                const int cur_group = mt / p.group_m;
+                for (;;) {
+                    bool stop = false;
+                    if (epi_tid == 0)
+                        stop = q_next >= q_total || q_item(p, q_next).group > cur_group + p.q_lookahead ||
+                               *abort_flag || mbar_test(tmem_full, acc_phase);
+                    if (named_bar_or(kEpiBarrier, NUM_EPI_WARPS * 32, stop)) break;
+                    quant_item_any<QFMT>(p, q_next, epi_tid);
+                    q_next += static_cast<int>(gridDim.x);
+                }
+            }
             bool ok = true;
             if (lane == 0) ok = mbar_wait_bounded(tmem_full, acc_phase, abort_flag, p.timeout_ns, &g_mx_status);
             ok = __shfl_sync(0xffffffffu, ok, 0);
-            // rank 1's warps meet on a named barrier below: they leave the
-            // loop together or not at all
-            if (rank == 1) ok = named_bar_and(kEpiBarrier, NUM_EPI_WARPS * 32, ok);
+            // rank 1's warps (and, fused, every CTA's) meet on named
+            // barriers: they leave the loop together or not at all
+            if (rank == 1 || FUSED) ok = named_bar_and(kEpiBarrier, NUM_EPI_WARPS * 32, ok);
             if (!ok) break;
             tc_fence_after();
             // a half tile's accumulator is columns 0..127: the second half's
@@ -1006,7 +1219,10 @@ __global__ void __launch_bounds__(sm2::THREADS, 1)
             // nothing.  Rank 1's stores cost nothing measurable and go at once.
             const int64_t m = static_cast<int64_t>(mt) * BM + rank * 128 + quarter * 32 + lane;
             const int64_t n0 = static_cast<int64_t>(nt) * BN + (hf < 0 ? half : hf) * 128;
-            const bool paced = rank == 0 && u + 1 < num_units && p.num_kb >= kPaceMinStages;
+            // (fused: only once this CTA's items are all written, so the
+            // wait never stands between another CTA's loads and an item)
+            const bool paced = rank == 0 && u + 1 < num_units && p.num_kb >= kPaceMinStages &&
+                               (!FUSED || q_next >= q_total);
             const uint32_t next_tile = static_cast<uint32_t>(u + 1) * static_cast<uint32_t>(p.num_kb);
             auto pace = [&](int c, int chunks) {
                 if (!paced) return;
@@ -1037,6 +1253,16 @@ __global__ void __launch_bounds__(sm2::THREADS, 1)
                     pace(c, 16);
                     store_row_chunk(p, b, m, n0 + 8 * c, w);
                 }
+            }
+        }
+        if constexpr (FUSED) {
+            // items other CTAs' tiles still wait for (a CTA with no tiles
+            // left, or none at all, still owes its share)
+            for (;;) {
+                const bool stop = epi_tid == 0 && (q_next >= q_total || *abort_flag);
+                if (named_bar_or(kEpiBarrier, NUM_EPI_WARPS * 32, stop)) break;
+                quant_item_any<QFMT>(p, q_next, epi_tid);
+                q_next += static_cast<int>(gridDim.x);
             }
         }
     }
@@ -1100,7 +1326,7 @@ bool make_sf_map(CUtensorMap* map, const void* base, int64_t tiles, uint32_t box
 uint64_t g_timeout_ns = 2000000000ull;
 int g_fault_skip_producer = 0;
 // 0 automatic, 1 force the 1-SM kernel, 2 force the 2-SM kernel, 3 force the
-// 1-SM kernel without split-K
+// 1-SM kernel without split-K, 4 automatic but the fused call as two launches
 int g_variant = 0;
 GemmLaunchInfo g_last_launch{};
 
@@ -1134,7 +1360,7 @@ KParams base_params(const GemmArgs& g, int bm, int bn) {
     p.group_m = 16;
     p.idesc = fp4 ? make_idesc_mxf4(bm, bn) : make_idesc_mxf8(g.elem_fmt, g.elem_fmt, bm, bn);
     p.timeout_ns = g_timeout_ns;
-    p.skip_producer = g_fault_skip_producer;
+    p.skip_producer = g_fault_skip_producer & 1;
     return p;
 }
 
@@ -1163,11 +1389,11 @@ cudaError_t ensure_1sm_attr() {
     static bool done[64] = {};
     return ensure_smem_attr(mx_gemm_kernel<FP4>, sm1::smem_alloc(FP4), mu, done);
 }
-template <bool FP4>
+template <bool FP4, int QFMT>
 cudaError_t ensure_2sm_attr() {
     static std::mutex mu;
     static bool done[64] = {};
-    return ensure_smem_attr(mx_gemm_2sm_kernel<FP4>, sm2::smem_alloc(FP4), mu, done);
+    return ensure_smem_attr(mx_gemm_2sm_kernel<FP4, QFMT>, sm2::smem_alloc(FP4), mu, done);
 }
 
 // attr: room for 2 (cluster shape, programmatic serialization)
@@ -1269,23 +1495,44 @@ int max_pair_clusters() {
     static int cached[64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
-    if (ensure_2sm_attr<FP4>() != cudaSuccess) return 1;
+    if (ensure_2sm_attr<FP4, -1>() != cudaSuccess) return 1;
     std::lock_guard<std::mutex> lock(mu);
     if (cached[dev] == 0) {
         cudaLaunchConfig_t cfg;
         cudaLaunchAttribute attr[2];
         pair_launch_config(&cfg, attr, device_sm_count() / 2, FP4, nullptr);
         int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, mx_gemm_2sm_kernel<FP4>, &cfg) != cudaSuccess || n <= 0)
+        if (cudaOccupancyMaxActiveClusters(&n, mx_gemm_2sm_kernel<FP4, -1>, &cfg) != cudaSuccess || n <= 0)
             n = device_sm_count() / 2;
         cached[dev] = n > 0 ? n : 1;
     }
     return cached[dev];
 }
 
-template <bool FP4>
+// A launch tag (40 bits, nonzero): consecutive calls get different tags (a
+// per-process counter), and memory never written by this library is
+// unlikely to hold one (the counter starts at a mixed clock / address seed).
+uint64_t next_tag() {
+    static std::atomic<uint64_t> counter{[] {
+        uint64_t z = static_cast<uint64_t>(std::chrono::steady_clock::now().time_since_epoch().count()) ^
+                     (static_cast<uint64_t>(std::chrono::system_clock::now().time_since_epoch().count()) << 17) ^
+                     reinterpret_cast<uintptr_t>(&g_timeout_ns);
+        // splitmix64 finaliser
+        z = (z ^ (z >> 30)) * 0xbf58476d1ce4e5b9ull;
+        z = (z ^ (z >> 27)) * 0x94d049bb133111ebull;
+        return z ^ (z >> 31);
+    }()};
+    uint64_t e;
+    do e = counter.fetch_add(1, std::memory_order_relaxed) & ((1ull << 40) - 1);
+    while (e == 0);  // never the tag of zeroed memory
+    return e;
+}
+
+int g_fused_lookahead = 1;
+
+template <bool FP4, int QFMT>
 cudaError_t launch_2sm(const GemmArgs& g, cudaStream_t stream) {
-    const cudaError_t attr_err = ensure_2sm_attr<FP4>();
+    const cudaError_t attr_err = ensure_2sm_attr<FP4, QFMT>();
     if (attr_err != cudaSuccess) return attr_err;
     CUtensorMap ma, mb, msa, msb;
     const int64_t sfa_tiles = g.batch * ((g.M + 127) / 128) * ((g.K + 127) / 128);
@@ -1307,11 +1554,26 @@ cudaError_t launch_2sm(const GemmArgs& g, cudaStream_t stream) {
     if (is_fp4(g)) p.idesc_half = make_idesc_mxf4(sm2::BM, sm2::BN / 2);
     const int clusters = p.split_tail ? (full_rounds > 0 ? cap : 2 * tail) : (tiles < cap ? tiles : cap);
     p.split_k = 1;
-    g_last_launch = GemmLaunchInfo{2, 1};
+    if constexpr (QFMT >= 0) {
+        p.q_x = g.x;
+        p.q_ld_x = g.ld_x_bytes;
+        p.q_xq = const_cast<uint8_t*>(g.a);
+        p.q_sf = const_cast<uint8_t*>(g.sfa);
+        p.q_flags = g.q_flags;
+        p.q_tag = next_tag();
+        p.q_f16 = g.x_f16;
+        p.q_panels = static_cast<int>((g.M + 127) / 128);
+        p.q_nkc = static_cast<int>((g.K + kQChunk - 1) / kQChunk);
+        p.q_lookahead = g_fused_lookahead;
+        p.q_emax = QFMT == kE4M3 ? 8 : QFMT == kE5M2 ? 15 : 2;
+        p.q_no_publish = (g_fault_skip_producer & 2) ? 1 : 0;
+        p.skip_producer = g_fault_skip_producer & 1;
+    }
+    g_last_launch = GemmLaunchInfo{QFMT >= 0 ? 3 : 2, 1};
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[2];
     pair_launch_config(&cfg, attr, clusters, FP4, stream);
-    return cudaLaunchKernelEx(&cfg, mx_gemm_2sm_kernel<FP4>, ma, mb, msa, msb, p);
+    return cudaLaunchKernelEx(&cfg, mx_gemm_2sm_kernel<FP4, QFMT>, ma, mb, msa, msb, p);
 }
 
 }  // namespace
@@ -1343,10 +1605,29 @@ bool prefer_pair(const GemmArgs& g) {
 
 cudaError_t launch_scaled_matmul(const GemmArgs& g, cudaStream_t stream) {
     const bool fp4 = is_fp4(g);
-    const bool pair = g_variant == 2 || (g_variant == 0 && (fp4 ? prefer_pair<true>(g) : prefer_pair<false>(g)));
+    const bool automatic = g_variant == 0 || g_variant == 4;
+    const bool pair = g_variant == 2 || (automatic && (fp4 ? prefer_pair<true>(g) : prefer_pair<false>(g)));
     const bool split = g_variant != 3;
-    if (fp4) return pair ? launch_2sm<true>(g, stream) : launch_1sm<true>(g, stream, split);
-    return pair ? launch_2sm<false>(g, stream) : launch_1sm<false>(g, stream, split);
+    if (fp4) return pair ? launch_2sm<true, -1>(g, stream) : launch_1sm<true>(g, stream, split);
+    return pair ? launch_2sm<false, -1>(g, stream) : launch_1sm<false>(g, stream, split);
+}
+
+bool fused_single_launch(const GemmArgs& g) {
+    if (g_variant == 4 || g.batch != 1) return false;
+    const bool x_ok = (reinterpret_cast<uintptr_t>(g.x) & 31u) == 0 && g.ld_x_bytes % 32 == 0 &&
+                      (reinterpret_cast<uintptr_t>(g.a) & 15u) == 0 && (reinterpret_cast<uintptr_t>(g.q_flags) & 7u) == 0;
+    if (!x_ok) return false;
+    if (g_variant == 2) return true;
+    if (g_variant == 1 || g_variant == 3) return false;
+    return is_fp4(g) ? prefer_pair<true>(g) : prefer_pair<false>(g);
+}
+
+cudaError_t launch_fused_matmul(const GemmArgs& g, cudaStream_t stream) {
+    switch (g.elem_fmt) {
+    case kE4M3: return launch_2sm<false, kE4M3>(g, stream);
+    case kE5M2: return launch_2sm<false, kE5M2>(g, stream);
+    default: return launch_2sm<true, kE2M1>(g, stream);
+    }
 }
 
 cudaError_t read_and_clear_device_status(int* status) {

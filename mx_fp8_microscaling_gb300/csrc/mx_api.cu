@@ -485,10 +485,20 @@ mx_status mx_scaled_matmul(const void* a, const void* bt, const uint8_t* a_scale
     return from_cuda(launch_scaled_matmul(g, s));
 }
 
+// Fused workspace: the quantized activation (M*K bytes, enough for FP8 and
+// e2m1), its SF-layout scales, then one 64-bit ready word per quantize item
+// of the single-launch kernel (128 rows x 256 elements).
+static size_t fused_flags_offset(int64_t M, int64_t K) {
+    return align16(static_cast<size_t>(M * K)) + align16(sf_layout_bytes(M, K));
+}
+static size_t fused_flag_bytes(int64_t M, int64_t K) {
+    return static_cast<size_t>((M + 127) / 128) * static_cast<size_t>((K + 255) / 256) * 8u;
+}
+
 mx_status mx_fused_quantize_matmul_workspace(int64_t M, int64_t N, int64_t K, size_t* bytes) {
     if (!bytes || M < 0 || N < 0 || K < 0) return MX_ERR_INVALID_ARG;
     if (K % 32 != 0) return MX_ERR_SHAPE;
-    *bytes = align16(static_cast<size_t>(M * K)) + align16(sf_layout_bytes(M, K));
+    *bytes = fused_flags_offset(M, K) + align16(fused_flag_bytes(M, K));
     return MX_OK;
 }
 
@@ -510,6 +520,31 @@ mx_status mx_fused_quantize_matmul(const void* x, mx_dtype x_dtype, int64_t ld_x
     if (!device_is_sm103()) return MX_ERR_DEVICE;
     uint8_t* xq = static_cast<uint8_t*>(workspace);
     uint8_t* xs = xq + align16(static_cast<size_t>(M * K));
+    {
+        // one launch: the pair kernel quantizes X into the workspace itself
+        GemmArgs g{};
+        g.a = xq;
+        g.bt = static_cast<const uint8_t*>(wt);
+        g.sfa = xs;
+        g.sfb = w_scale_sf;
+        g.M = M;
+        g.N = N;
+        g.K = K;
+        g.c = c;
+        g.ldc = ldc;
+        g.elem_fmt = gemm_fmt(elem_dtype);
+        g.out_bf16 = out_dtype == MX_BF16;
+        g.vec_store = aligned16(c) && (ldc * (out_dtype == MX_F32 ? 4 : 2)) % 16 == 0;
+        g.batch = 1;
+        g.a_batch_stride = M * elem_bytes(elem_dtype, K);
+        g.b_batch_stride = N * elem_bytes(elem_dtype, K);
+        g.c_batch_stride = M * ldc;
+        g.x = static_cast<const uint8_t*>(x);
+        g.ld_x_bytes = ld_x * 2;
+        g.x_f16 = x_dtype == MX_F16;
+        g.q_flags = reinterpret_cast<uint64_t*>(xq + fused_flags_offset(M, K));
+        if (fused_single_launch(g)) return from_cuda(launch_fused_matmul(g, reinterpret_cast<cudaStream_t>(stream)));
+    }
     mx_quant_cfg cfg;
     mx_quant_cfg_default(&cfg);
     cfg.geometry = MX_GEOM_1X32;
@@ -646,7 +681,7 @@ mx_status mx_debug_gemm_fault_injection(int skip_producer, uint64_t timeout_ns) 
 }
 
 mx_status mx_debug_set_gemm_variant(int variant) {
-    if (variant < 0 || variant > 3) return MX_ERR_INVALID_ARG;
+    if (variant < 0 || variant > 4) return MX_ERR_INVALID_ARG;
     set_gemm_variant(variant);
     return MX_OK;
 }

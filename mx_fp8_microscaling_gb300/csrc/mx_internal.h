@@ -93,12 +93,25 @@ struct GemmArgs {
     // to back (sf_layout_bytes(M, K) / (N, K) each).
     int64_t batch;
     int64_t a_batch_stride, b_batch_stride, c_batch_stride;
+    // Fused activation quantize (mx_fused_quantize_matmul): the launch
+    // itself writes A (a: codes, sfa: SF-layout scales) from X [M, K]
+    // bf16/f16, publishing one ready word per 128-row x 256-element item in
+    // q_flags ([ceil(M/128), ceil(K/256)] 64-bit words).
+    const uint8_t* x;
+    int64_t ld_x_bytes;
+    int32_t x_f16;
+    uint64_t* q_flags;
 };
 cudaError_t launch_scaled_matmul(const GemmArgs& g, cudaStream_t stream);
+// Whether the fused call runs as one launch of the pair kernel (else
+// QuantizeMX, then launch_scaled_matmul), and that launch.
+bool fused_single_launch(const GemmArgs& g);
+cudaError_t launch_fused_matmul(const GemmArgs& g, cudaStream_t stream);
 
 // Which kernel the last ScaledMatmul launch on this host used (testing aid).
 struct GemmLaunchInfo {
-    int kernel;   // 1: 1-SM kernel, 2: 2-SM pair kernel, 0: none yet
+    int kernel;   // 1: 1-SM kernel, 2: 2-SM pair kernel, 3: pair kernel with the
+                  // fused activation quantize, 0: none yet
     int split_k;  // CTAs per tile along K (1-SM kernel), else 1
 };
 GemmLaunchInfo last_gemm_launch();

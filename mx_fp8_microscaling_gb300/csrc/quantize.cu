@@ -33,55 +33,17 @@
 #include "mx_device.cuh"
 #include "mx_internal.h"
 #include "pdl.cuh"
+#include "quant_math.cuh"
 
 namespace mx {
 namespace {
 
 using namespace dev;
+using namespace qdev;
 
 constexpr int kThreads = 256;
 
 // --------------------------------------------------------------- helpers
-
-template <bool F16>
-__device__ __forceinline__ float widen_lo(uint32_t w) {
-    if constexpr (F16) return f16_bits_to_f32(w & 0xFFFFu);
-    else return __uint_as_float(w << 16);
-}
-template <bool F16>
-__device__ __forceinline__ float widen_hi(uint32_t w) {
-    if constexpr (F16) return f16_bits_to_f32(w >> 16);
-    else return __uint_as_float(w & 0xFFFF0000u);
-}
-template <bool F16>
-__device__ __forceinline__ float widen1(uint32_t h) {
-    if constexpr (F16) return f16_bits_to_f32(h);
-    else return __uint_as_float(h << 16);
-}
-
-// Binary32 exponent byte of the widened value whose 16-bit magnitude is m16.
-template <bool F16>
-__device__ __forceinline__ uint32_t exp_byte_of_mag(uint32_t m16) {
-    if constexpr (F16) return __float_as_uint(f16_bits_to_f32(m16)) >> 23;
-    else return m16 >> 7;
-}
-
-// E8M0 from the block's max exponent byte: floor at 0, then at 1.
-__device__ __forceinline__ uint32_t e8m0_of(uint32_t max_exp, int bias) {
-    int v = static_cast<int>(max_exp) - bias;
-    return static_cast<uint32_t>(v < 1 ? 1 : v);
-}
-
-// 2^(127 - E): the binary32 with exponent field 254 - E and zero fraction.
-__device__ __forceinline__ float prescale_mul(uint32_t e8m0) {
-    return __uint_as_float((254u - e8m0) << 23);
-}
-
-__device__ __forceinline__ uint32_t mag2(uint32_t w) { return w & 0x7FFF7FFFu; }
-__device__ __forceinline__ uint32_t hmax(uint32_t m) {
-    uint32_t lo = m & 0xFFFFu, hi = m >> 16;
-    return lo > hi ? lo : hi;
-}
 
 // Scale-row placement (plain / interleaved).
 __device__ __forceinline__ int64_t scale_slot(int64_t i, int mode) {
@@ -99,67 +61,6 @@ __device__ __forceinline__ int64_t scale_offset(const QuantArgs& q, int64_t srow
     return scale_slot(srow, q.scale_mode) * q.scale_cols + scol;
 }
 
-template <int FMT>
-__device__ __forceinline__ uint32_t cvt_pair(float hi, float lo) {
-    if constexpr (FMT == kE4M3) return cvt_e4m3x2(hi, lo);
-    else if constexpr (FMT == kE5M2) return cvt_e5m2x2(hi, lo);
-    else return cvt_e2m1x2(hi, lo);
-}
-
-// One element, special values handled explicitly (used where a block holds
-// Inf/NaN, and by the generic kernel).
-template <int FMT>
-__device__ __forceinline__ uint32_t encode1(float y) {
-    const uint32_t sign = __float_as_uint(y) >> 31;
-    if constexpr (FMT == kE2M1) {
-        if (isnan(y)) return sign << 3;
-        if (isinf(y)) return (sign << 3) | 7u;
-        return cvt_e2m1x2(0.0f, y) & 0xFu;
-    } else {
-        constexpr uint32_t kMax = (FMT == kE4M3) ? 0x7Eu : 0x7Bu;
-        if (isnan(y)) return (sign << 7) | 0x7Fu;
-        if (isinf(y)) return (sign << 7) | kMax;
-        return cvt_pair<FMT>(0.0f, y) & 0xFFu;
-    }
-}
-
-// 8 prescaled values of one row -> packed output.
-// FP8: two 32-bit words, byte j = element j.
-// e2m1: one 32-bit word; pair p = elements (2p, 2p+1) forms one byte (the
-// even element in the high nibble for parity 0), and the four pair-bytes are
-// placed by the lane-remap permutation `perm`.
-template <int FMT>
-__device__ __forceinline__ void pack8(const float (&y)[8], bool special, int parity, uint32_t perm,
-                                      uint32_t& w0, uint32_t& w1) {
-    if constexpr (FMT == kE2M1) {
-        uint32_t b[4];
-        if (!special) {
-#pragma unroll
-            for (int p = 0; p < 4; ++p)
-                b[p] = parity ? cvt_pair<FMT>(y[2 * p + 1], y[2 * p]) : cvt_pair<FMT>(y[2 * p], y[2 * p + 1]);
-        } else {
-#pragma unroll
-            for (int p = 0; p < 4; ++p) {
-                uint32_t n0 = encode1<FMT>(y[2 * p]), n1 = encode1<FMT>(y[2 * p + 1]);
-                b[p] = parity ? ((n1 << 4) | n0) : ((n0 << 4) | n1);
-            }
-        }
-        uint32_t src = b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24);
-        w0 = __byte_perm(src, 0u, perm);
-        w1 = 0;
-    } else {
-        if (!special) {
-            w0 = cvt_pair<FMT>(y[1], y[0]) | (cvt_pair<FMT>(y[3], y[2]) << 16);
-            w1 = cvt_pair<FMT>(y[5], y[4]) | (cvt_pair<FMT>(y[7], y[6]) << 16);
-        } else {
-            uint32_t c[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) c[j] = encode1<FMT>(y[j]);
-            w0 = c[0] | (c[1] << 8) | (c[2] << 16) | (c[3] << 24);
-            w1 = c[4] | (c[5] << 8) | (c[6] << 16) | (c[7] << 24);
-        }
-    }
-}
 
 template <int FMT>
 __device__ __forceinline__ void store8(uint8_t* dst, uint32_t w0, uint32_t w1) {
@@ -203,17 +104,9 @@ __global__ void __launch_bounds__(kThreads) quant_g84(QuantArgs q) {
         uint8_t* dst = q.data + (g * 8) * q.ld_data + c * kOutBytes;
 #pragma unroll
         for (int r = 0; r < 8; ++r) {
-            float y[8];
-            y[0] = mul_rn(widen_lo<F16>(v[r].x), sa);
-            y[1] = mul_rn(widen_hi<F16>(v[r].x), sa);
-            y[2] = mul_rn(widen_lo<F16>(v[r].y), sa);
-            y[3] = mul_rn(widen_hi<F16>(v[r].y), sa);
-            y[4] = mul_rn(widen_lo<F16>(v[r].z), sb);
-            y[5] = mul_rn(widen_hi<F16>(v[r].z), sb);
-            y[6] = mul_rn(widen_lo<F16>(v[r].w), sb);
-            y[7] = mul_rn(widen_hi<F16>(v[r].w), sb);
+            const uint32_t w[4] = {v[r].x, v[r].y, v[r].z, v[r].w};
             uint32_t w0, w1;
-            pack8<FMT>(y, special, q.fp4_parity, q.fp4_perm, w0, w1);
+            quantize8<F16, FMT>(w, sa, sb, special, q.fp4_parity, q.fp4_perm, w0, w1);
             store8<FMT>(dst + r * q.ld_data, w0, w1);
         }
         *reinterpret_cast<uint16_t*>(q.scale + scale_slot(g, q.scale_mode) * q.scale_cols + c * 2) =
@@ -269,17 +162,9 @@ __global__ void __launch_bounds__(kThreads) quant_g1x32(QuantArgs q) {
 #pragma unroll
             for (int r = 0; r < TR; ++r) {
                 if (r0 + r >= q.rows) break;
-                float y[8];
-                y[0] = mul_rn(widen_lo<F16>(v[r].x), s[r]);
-                y[1] = mul_rn(widen_hi<F16>(v[r].x), s[r]);
-                y[2] = mul_rn(widen_lo<F16>(v[r].y), s[r]);
-                y[3] = mul_rn(widen_hi<F16>(v[r].y), s[r]);
-                y[4] = mul_rn(widen_lo<F16>(v[r].z), s[r]);
-                y[5] = mul_rn(widen_hi<F16>(v[r].z), s[r]);
-                y[6] = mul_rn(widen_lo<F16>(v[r].w), s[r]);
-                y[7] = mul_rn(widen_hi<F16>(v[r].w), s[r]);
+                const uint32_t w[4] = {v[r].x, v[r].y, v[r].z, v[r].w};
                 uint32_t w0, w1;
-                pack8<FMT>(y, special, q.fp4_parity, q.fp4_perm, w0, w1);
+                quantize8<F16, FMT>(w, s[r], s[r], special, q.fp4_parity, q.fp4_perm, w0, w1);
                 store8<FMT>(q.data + (r0 + r) * q.ld_data + c * kOutBytes, w0, w1);
             }
             // lane t of the 4-lane group writes row t's scale byte
@@ -367,13 +252,8 @@ __global__ void __launch_bounds__(kThreads) quant_g1x32w(QuantArgs q) {
                 uint32_t w[4];
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
-                    float y[8];
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        y[2 * j] = mul_rn(widen_lo<F16>(v[r][4 * h + j]), s[r]);
-                        y[2 * j + 1] = mul_rn(widen_hi<F16>(v[r][4 * h + j]), s[r]);
-                    }
-                    pack8<FMT>(y, special, q.fp4_parity, q.fp4_perm, w[2 * h], w[2 * h + 1]);
+                    const uint32_t hw[4] = {v[r][4 * h], v[r][4 * h + 1], v[r][4 * h + 2], v[r][4 * h + 3]};
+                    quantize8<F16, FMT>(hw, s[r], s[r], special, q.fp4_parity, q.fp4_perm, w[2 * h], w[2 * h + 1]);
                 }
                 if constexpr (FMT == kE2M1) {
                     *reinterpret_cast<uint2*>(q.data + (r0 + r) * q.ld_data + c * 8) = make_uint2(w[0], w[2]);
@@ -427,8 +307,8 @@ __global__ void __launch_bounds__(kThreads) quant_generic(QuantArgs q) {
             for (int cc = 0; cc < ncols; cc += 2) {
                 const uint32_t h0 = ld_u16(q.in + (r * q.ld_in + c0 + cc) * 2);
                 const uint32_t h1 = ld_u16(q.in + (r * q.ld_in + c0 + cc + 1) * 2);
-                const float y0 = mul_rn(widen1<F16>(h0), prescale_mul(e[cc / bc]));
-                const float y1 = mul_rn(widen1<F16>(h1), prescale_mul(e[(cc + 1) / bc]));
+                const float y0 = prescale_keep_nan(widen_keep_nan<F16>(h0), prescale_mul(e[cc / bc]));
+                const float y1 = prescale_keep_nan(widen_keep_nan<F16>(h1), prescale_mul(e[(cc + 1) / bc]));
                 if constexpr (FMT == kE2M1) {
                     uint32_t n0, n1;
                     if (special) { n0 = encode1<FMT>(y0); n1 = encode1<FMT>(y1); }

@@ -58,6 +58,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Non-blocking test of a phase: true iff the phase of parity `parity` has
+// completed (never suspends the thread).
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Bounded wait for the phase of parity `parity` to complete.  Gives up when
 // the shared abort flag is raised by another role, or after `limit_ns` of
 // wall-clock time, in which case it records MX_ERR_TIMEOUT (9) in
@@ -221,6 +235,36 @@ __device__ __forceinline__ bool named_bar_and(uint32_t id, uint32_t threads, boo
         : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(threads)
         : "memory");
     return r != 0;
+}
+
+// OR-reduction form of the named barrier: true in every participant iff
+// `pred` is true in at least one of them.
+__device__ __forceinline__ bool named_bar_or(uint32_t id, uint32_t threads, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(threads)
+        : "memory");
+    return r != 0;
+}
+
+// 64-bit global word with acquire / release semantics at GPU scope (ready
+// words published by one CTA and polled by others).
+__device__ __forceinline__ uint64_t ld_acquire_gpu_u64(const uint64_t* p) {
+    uint64_t v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release_gpu_u64(uint64_t* p, uint64_t v) {
+    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+// Orders this thread's generic-proxy accesses of global memory against its
+// async-proxy (TMA) accesses on either side of the fence.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
 __device__ __forceinline__ void cluster_sync_all() {

@@ -245,13 +245,14 @@ def fp4_input(rows: int = 16384, cols: int = 16384, seed: int = 0,
 def special_values(in_dtype: str = "bf16") -> np.ndarray:
     """A pool of edge-case bit patterns for the input format: signed zeros,
     the smallest and largest subnormals, the smallest normal, +-1, the
-    largest finite value, +-Inf and a quiet NaN."""
+    largest finite value, +-Inf and NaNs of both signs (quiet, and with other
+    payloads)."""
     if in_dtype == "bf16":
         pats = [0x0000, 0x8000, 0x0001, 0x8001, 0x007F, 0x0080, 0x3F80, 0xBF80,
-                0x7F7F, 0xFF7F, 0x7F80, 0xFF80, 0x7FC0, 0x4000, 0x3F00]
+                0x7F7F, 0xFF7F, 0x7F80, 0xFF80, 0x7FC0, 0xFFC0, 0x7F81, 0xFFA4, 0x4000, 0x3F00]
     else:
         pats = [0x0000, 0x8000, 0x0001, 0x8001, 0x03FF, 0x0400, 0x3C00, 0xBC00,
-                0x7BFF, 0xFBFF, 0x7C00, 0xFC00, 0x7E00, 0x4000, 0x3800]
+                0x7BFF, 0xFBFF, 0x7C00, 0xFC00, 0x7E00, 0xFE00, 0x7C01, 0xFD55, 0x4000, 0x3800]
     return np.array(pats, np.uint16)
 
 

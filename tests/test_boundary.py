@@ -143,7 +143,10 @@ def test_matmul_workspace_sizes(mx):
     assert mx.mx_scaled_matmul_workspace(8192, 8192, 8192) == 2 * 64 * 64 * 512
     assert mx.mx_scaled_matmul_workspace(8192, 8192, 8192, True) == 0
     assert mx.mx_sf_layout_bytes(200, 96) == 2 * 1 * 512
-    assert mx.mx_fused_quantize_matmul_workspace(256, 512, 256) == 256 * 256 + 2 * 2 * 512
+    # fused: codes, SF scales, then one 8-byte ready word per 128 x 256 item
+    assert mx.mx_fused_quantize_matmul_workspace(256, 512, 256) == 256 * 256 + 2 * 2 * 512 + 16
+    # 300 * 1056 codes, 3 x 9 scale tiles, 3 x 5 ready words (120 bytes, rounded up to 128)
+    assert mx.mx_fused_quantize_matmul_workspace(300, 512, 1056) == 300 * 1056 + 3 * 9 * 512 + 128
 
 
 def test_fused_argument_errors(lib):
@@ -286,13 +289,13 @@ def test_host_quantize_batch_workspace_and_checks(mx, lib):
 
 
 def test_debug_hooks_check_arguments(mx, lib):
-    # the kernel-choice hook takes 0..3; the last-launch query wants both pointers
-    assert lib.mx_debug_set_gemm_variant(4) == mx.MX_ERR_INVALID_ARG
+    # the kernel-choice hook takes 0..4; the last-launch query wants both pointers
+    assert lib.mx_debug_set_gemm_variant(5) == mx.MX_ERR_INVALID_ARG
     assert lib.mx_debug_set_gemm_variant(-1) == mx.MX_ERR_INVALID_ARG
-    for v in (3, 0):
+    for v in (4, 3, 0):
         assert lib.mx_debug_set_gemm_variant(v) == mx.MX_OK
     one = ctypes.c_int()
     assert lib.mx_debug_last_gemm_launch(None, ctypes.byref(one)) == mx.MX_ERR_INVALID_ARG
     assert lib.mx_debug_last_gemm_launch(ctypes.byref(one), None) == mx.MX_ERR_INVALID_ARG
     kernel, split = mx.mx_debug_last_gemm_launch()
-    assert kernel in (0, 1, 2) and split >= (1 if kernel else 0)
+    assert kernel in (0, 1, 2, 3) and split >= (1 if kernel else 0)
