@@ -5,14 +5,16 @@
 
 A step is one pass of the whole hot path over its synthetic inputs:
   sweep  QuantizeMX on [8192, 8192] for {bf16, f16} x {e4m3fn, e5m2} x
-         {plain, interleaved} scales, 8x4 blocks along dim=-2 (8 launches);
+         {plain, interleaved} scales, 8x4 blocks along dim=-2 (8 launches,
+         repeated 8 times in one timed span);
   gemm   for e4m3fn -> bf16 and e5m2 -> f32: QuantizeMX of A and Bt
          ([8192, 8192] bf16, 1x32 blocks along K), repack of both scale
          tensors to the tensor-core layout, ScaledMatmul 8192^3;
   fp4    QuantizeMX [16384, 16384] bf16 -> e2m1, 8x4, packed, interleaved;
   dequant  MX dequantize of [8192, 8192] e4m3fn codes with 8x4 scales to bf16;
-  fused  activation quantize + ScaledMatmul, X [16384, 8192] bf16 times a
-         pre-quantized e4m3fn weight W [8192, 28672] -> bf16;
+  fused  activation quantize + ScaledMatmul in one launch, X [16384, 8192]
+         bf16 times a pre-quantized e4m3fn weight W [8192, 28672] -> bf16,
+         next to the same product as two launches;
   gemm_fp4  MXFP4 ScaledMatmul 8192^3 (e2m1 operands quantized along K in
          the tensor-core nibble order, repacked scales) -> bf16;
   dot    batched block-scaled dot, 16 problems of 2048^3 e4m3fn -> bf16:
@@ -25,8 +27,9 @@ Inputs are larger than L2 and rotated so no launch re-reads the previous
 launch's input from L2.  Kernel times come from CUDA events on the launching
 stream; the whole step is bracketed by a barrier and a synchronize.
 
---impl reference times the CPU oracle (plain C, one core) on a bounded
-sample of the sweep workload, with the same metric and unit.
+--impl reference times the CPU oracle (plain C, as it stands) on the sweep
+workload, one worker process per host core, with the same metric and unit;
+the main arm's cpu_baseline is the same measurement.
 """
 from __future__ import annotations
 
@@ -281,14 +284,19 @@ class Sweep:
                 s = torch.empty(sr * sc, dtype=torch.uint8, device="cuda")
                 self.out[(layout, in_dtype, fmt)] = (d, s)
                 self.ops.append(("sweep", api.quantize(self.x[(in_dtype, fmt)], fmt, "8x4", -2, layout, d, s)))
-        self.launches = 8
+        self.launches = self.REPEATS * len(self.ops)
+
+    # One event pair around REPEATS x 8 back-to-back launches (per-launch
+    # event records would add their own gaps to 33 us kernels).  A span ends
+    # with its last launch's writes partly still in L2 (about 58 of 69 MB);
+    # over 64 launches that is under 0.5 % of the span's bytes.
+    REPEATS = 8
 
     def step(self, timer):
-        # one event pair around the 8 back-to-back launches: per-launch event
-        # records would add their own gaps to 33 us kernels
         def all_launches():
-            for _, fn in self.ops:
-                fn()
+            for _ in range(self.REPEATS):
+                for _, fn in self.ops:
+                    fn()
         timer.run("sweep", all_launches)
 
 
@@ -326,21 +334,22 @@ class Gemm:
 
 class Fp4:
     """QuantizeMX [16384, 16384] bf16 -> e2m1, 8x4 blocks, interleaved
-    scales: two back-to-back launches a step on two inputs (seeds 0 and 1,
-    512 MiB each), timed as one span like the sweep."""
-    LAUNCHES = 2
+    scales: 16 back-to-back launches a step alternating over two inputs
+    (seeds 0 and 1, 512 MiB each), timed as one span like the sweep."""
+    LAUNCHES = 16
 
     def __init__(self, torch, mx, api):
         cfg = mx.make_cfg("8x4", -2, "interleave")
         db, sr, sc = mx.mx_quantize_sizes(*FP4_SHAPE, "bf16", "e2m1", cfg)
         self.keep = []
-        self.ops = []
-        for seed in range(self.LAUNCHES):
+        calls = []
+        for seed in range(2):
             x = dev_bits(torch, syn.fp4_input(*FP4_SHAPE, seed=seed), "bf16")
             d = torch.empty(db, dtype=torch.uint8, device="cuda")
             s = torch.empty(sr * sc, dtype=torch.uint8, device="cuda")
             self.keep.append((x, d, s))
-            self.ops.append(api.quantize(x, "e2m1", "8x4", -2, "interleave", d, s))
+            calls.append(api.quantize(x, "e2m1", "8x4", -2, "interleave", d, s))
+        self.ops = [calls[i % 2] for i in range(self.LAUNCHES)]
         self.launches = self.LAUNCHES
 
     def step(self, timer):
@@ -352,10 +361,10 @@ class Fp4:
 
 class Dequant:
     """[8192, 8192] e4m3fn codes + plain 8x4 scales -> bf16 (1 + 1/32 B read,
-    2 B written per element): four back-to-back launches a step alternating
+    2 B written per element): 32 back-to-back launches a step alternating
     over two code / output sets (388 MiB, larger than L2), timed as one span
     like the sweep."""
-    LAUNCHES = 4
+    LAUNCHES = 32
 
     def __init__(self, torch, mx, api):
         import ctypes
@@ -410,7 +419,11 @@ class Fused:
         self.unfused = [("fused_split_quantize", api.quantize(self.x, "e4m3fn", "1x32", -1, "sf", self.xq, self.xs)),
                         ("fused_split_gemm", api.matmul_sf(self.xq, self.wq, self.xs, self.ws, "e4m3fn", "bf16",
                                                            self.c, K))]
-        self.launches = 2 + 2
+        self.op()
+        torch.cuda.synchronize()
+        # 3: the pair kernel with the fused quantize, the whole call one launch
+        self.launches_per_call = 1 if mx.mx_debug_last_gemm_launch()[0] == 3 else 2
+        self.launches = self.launches_per_call + 2
 
     def step(self, timer):
         timer.run("fused", self.op)
@@ -644,8 +657,7 @@ def vendor_small_m_reference(torch, g, steps):
                     if it >= 3:
                         ts[which].append(e0.elapsed_time(e1) * 1e3 / SMALL_M_COPIES)
             out[str(m)] = {k: round(statistics.median(v), 2) for k, v in ts.items()}
-        return {"us_per_call": out, "what": f"M x 8192 x 8192 e4m3fn -> bf16, B rotated over {SMALL_M_COPIES} "
-                                            f"copies, CUDA graphs, median of {steps}; cuBLASLt via torch._scaled_mm"}
+        return {"us_per_call": out, "what": "cuBLASLt via torch._scaled_mm, same operands and graphs"}
     except Exception as e:
         return {"unavailable": f"{type(e).__name__}: {str(e)[:160]}"}
 
@@ -680,8 +692,8 @@ def vendor_gemm_reference(torch, g, steps):
                 if it >= 3:
                     times[which].append(e0.elapsed_time(e1))
         out = {k: round(GEMM_FLOP / (statistics.median(v) * 1e-3) / 1e12, 1) for k, v in times.items()}
-        return {"tflops": out, "what": "e4m3fn -> bf16 8192^3, same operands and SF-layout scales, median of "
-                                      f"{steps}; cuBLASLt via torch._scaled_mm"}
+        return {"tflops": out, "what": "8192^3 e4m3fn -> bf16, same operands and scales; cuBLASLt via "
+                                      "torch._scaled_mm"}
     except Exception as e:  # a torch build without block-scaled _scaled_mm
         return {"unavailable": f"{type(e).__name__}: {str(e)[:160]}"}
 
@@ -720,39 +732,87 @@ def vendor_fp4_reference(torch, g, steps):
 
 # ------------------------------------------------------------- CPU oracle
 
-def oracle_sweep_sample(rows=2048, repeats=1):
-    """The oracle on [rows, 8192] slices of the four sweep inputs, plain and
-    interleaved layouts.  Returns (GB/s over algorithmic bytes, seconds,
-    elements, description)."""
+# The oracle runs as it stands (plain C, one call per slice) in a pool of
+# worker processes, one per host core, started with "spawn" (a pool forked
+# after CUDA initialisation can hang).  Each worker makes its inputs, waits
+# on a barrier with the others, and times its own calls; the throughput is
+# all workers' bytes over the span from the first start to the last end.
+
+_POOL_BARRIER = None
+
+
+def _pool_init(barrier):
+    global _POOL_BARRIER
+    _POOL_BARRIER = barrier
+
+
+def _oracle_sweep_task(task):
+    rows, part = task
     import oracle as orc
-    samples = [(i, f, syn.sweep_input(rows, 8192, i, f, seed=0)) for i, f in SWEEP_VARIANTS]
+    samples = [(i, f, syn.sweep_input(rows, 8192, i, f, seed=1000 + part)) for i, f in SWEEP_VARIANTS]
+    _POOL_BARRIER.wait()
     t0 = time.perf_counter()
     nbytes = 0
-    for _ in range(repeats):
-        for layout in ("plain", "interleave"):
-            for in_dtype, fmt, bits in samples:
-                orc.quantize(bits, in_dtype, fmt, geometry="8x4", dim=-2, scale_layout=layout)
-                nbytes += 3 * bits.size + bits.size // 32
-    dt = time.perf_counter() - t0
-    return nbytes / dt / 1e9, dt, 8 * repeats * rows * 8192, \
-        f"8 sweep variants on [{rows}, 8192] slices x {repeats}, single-threaded C oracle"
+    for layout in ("plain", "interleave"):
+        for in_dtype, fmt, bits in samples:
+            orc.quantize(bits, in_dtype, fmt, geometry="8x4", dim=-2, scale_layout=layout)
+            nbytes += 3 * bits.size + bits.size // 32
+    return nbytes, t0, time.perf_counter()
 
 
-def oracle_gemm_sample(rows=2):
-    """The oracle's binary64 scaled dot on `rows` full output rows of the
-    8192^3 ScaledMatmul (k-ordered sums in C).  Returns TFLOP/s."""
+def _oracle_gemm_task(part):
     import oracle as orc
-    rng = np.random.default_rng(0)
+    rng = np.random.default_rng(part)
     K = GEMM_N
-    a = rng.integers(0, 0x7E, size=(rows, K)).astype(np.uint8)
+    a = rng.integers(0, 0x7E, size=(1, K)).astype(np.uint8)
     bt = rng.integers(0, 0x7E, size=(GEMM_N, K)).astype(np.uint8)
-    sa = np.full((rows, K // 32), 127, np.uint8)
+    sa = np.full((1, K // 32), 127, np.uint8)
     sb = np.full((GEMM_N, K // 32), 127, np.uint8)
-    ms, ns = [v.reshape(-1) for v in np.meshgrid(np.arange(rows), np.arange(GEMM_N), indexing="ij")]
+    ms, ns = np.zeros(GEMM_N, np.int64), np.arange(GEMM_N, dtype=np.int64)
+    _POOL_BARRIER.wait()
     t0 = time.perf_counter()
     orc.scaled_matmul_entries(a, bt, sa, sb, "e4m3fn", "e4m3fn", ms, ns)
-    dt = time.perf_counter() - t0
-    return 2.0 * rows * GEMM_N * K / dt / 1e12, dt
+    return 2.0 * GEMM_N * K, t0, time.perf_counter()
+
+
+def _run_pool(fn, tasks):
+    import multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    barrier = ctx.Barrier(len(tasks))
+    with ctx.Pool(len(tasks), initializer=_pool_init, initargs=(barrier,)) as pool:
+        res = pool.map(fn, tasks, chunksize=1)
+    work = sum(r[0] for r in res)
+    span = max(r[2] for r in res) - min(r[1] for r in res)
+    return work, span
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def oracle_sweep_parallel(cores=None):
+    """The oracle on the whole sweep workload: every core quantizes a
+    [rows, 8192] slice (rows = 8192 / cores, rounded down to whole
+    interleave groups) of each of the 4 inputs, both scale layouts.  Returns
+    (GB/s over algorithmic bytes, seconds, cores, description)."""
+    cores = cores or host_cores()
+    rows = max(32, 8192 // cores // 32 * 32)
+    nbytes, dt = _run_pool(_oracle_sweep_task, [(rows, i) for i in range(cores)])
+    return nbytes / dt / 1e9, dt, cores, \
+        f"the sweep's 8 variants over [{rows * cores}, 8192] rows ([{rows}, 8192] a core, own seeds), " \
+        f"plain C oracle, {cores} worker processes"
+
+
+def oracle_gemm_parallel(cores=None):
+    """The oracle's binary64 scaled dot, one full output row of the 8192^3
+    ScaledMatmul per core (k-ordered sums in C).  Returns (TFLOP/s, seconds,
+    cores)."""
+    cores = cores or host_cores()
+    flop, dt = _run_pool(_oracle_gemm_task, list(range(cores)))
+    return flop / dt / 1e12, dt, cores
 
 
 def oracle_pipeline_256(repeats=5):
@@ -814,24 +874,28 @@ def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    rows = args.reference_rows
-    vals = []
+    # each step: the oracle over the whole sweep workload on every host core
+    # (the same sample as the main arm's cpu_baseline)
+    cores = host_cores()
+    vals, spans = [], []
     for _ in range(args.warmup):
-        oracle_sweep_sample(rows=rows)
+        oracle_sweep_parallel(cores)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        v, dt, n, desc = oracle_sweep_sample(rows=rows)
+        v, dt, _, desc = oracle_sweep_parallel(cores)
         vals.append(v)
+        spans.append(dt)
     total = time.perf_counter() - t0
     value = statistics.median(vals)
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * total / args.steps, 3),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "mxfp8/f32",
+        "data": "synthetic",
         "config": {"workload": "QuantizeMX sweep [8192,8192] {bf16,f16}x{e4m3fn,e5m2}x{plain,interleave}, 8x4 "
-                               "blocks, dim=-2", "sample": f"[{rows}, 8192] slice per variant"},
-        "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": desc},
+                               "blocks, dim=-2", "sample": desc},
+        "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": desc, "seconds_median": round(statistics.median(spans), 3)},
         "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -847,8 +911,6 @@ def main():
                     choices=["all", "sweep", "gemm", "fp4", "fused", "dequant", "dot", "gemm_fp4", "gemm_small_m",
                              "pipeline_256"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--reference-rows", type=int, default=1024,
-                    help="rows of each [rows, 8192] sweep slice the reference arm quantizes per step")
     args = ap.parse_args()
     if args.warmup < 3:
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
@@ -907,19 +969,23 @@ def main():
 
     line = {"metric": METRIC, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "u8", "data": "synthetic (seeded; distributions of the workload "
-            "descriptions)", "gpu_launches": launches_per_step * args.steps, "clocks": clocks}
+            "vs_baseline": None, "dtype": "mxfp8/f32",
+            "data": "synthetic (seeded; distributions of the workload descriptions)",
+            "gpu_launches": launches_per_step * args.steps, "clocks": clocks}
+    peak_fp8 = peaks["bf16"] * FP8_OVER_BF16
+    fp8_src = f"{peaks['src']} bf16 burst x {FP8_OVER_BF16} (nominal MXFP8/bf16)"
 
     if "sweep" in parts:
+        per_span = parts["sweep"].launches
         sweep_ms = max_over_ranks(ws, timer.totals["sweep"])
-        n_launch = timer.counts["sweep"] * 8
+        n_launch = timer.counts["sweep"] * per_span
         value = sum_over_ranks(ws, SWEEP_BYTES * n_launch) / (sweep_ms * 1e-3) / 1e9
-        # average launch duration = each step's 8-launch span / 8 (gaps included)
-        achieved = SWEEP_BYTES / (timer.avg_ms("sweep") / 8 * 1e-3) / 1e9
+        # average launch duration = each step's span / its launches (gaps included)
+        achieved = SWEEP_BYTES / (timer.avg_ms("sweep") / per_span * 1e-3) / 1e9
         line.update({"value": round(value, 2), "unit": "GB/s",
                      "config": {"workload": "QuantizeMX sweep [8192,8192] {bf16,f16}x{e4m3fn,e5m2}x"
                                             "{plain,interleave}, 8x4 blocks, dim=-2",
-                                "bytes_per_launch": SWEEP_BYTES, "launches_per_step": 8,
+                                "bytes_per_launch": SWEEP_BYTES, "launches_per_step": per_span,
                                 "l2": "inputs (128 MiB each, 4 distinct) larger than L2 and rotated",
                                 "parallelism": f"replicas x{ws}"},
                      "roofline": {"bound": "hbm", "kernel": "quant_g84", "achieved": round(achieved, 1),
@@ -931,59 +997,60 @@ def main():
 
     if "gemm" in parts:
         g = {}
-        peak_fp8 = peaks["bf16"] * FP8_OVER_BF16
         for fmt, out in Gemm.CASES:
             ms = timer.avg_ms(f"gemm_{fmt}_{out}")
             tf = GEMM_FLOP / (ms * 1e-3) / 1e12
-            g[f"{fmt}_{out}"] = {"tflops": round(tf, 1), "ms": round(ms, 4)}
+            g[f"{fmt}_{out}"] = {"tflops": round(tf, 1), "ms": round(ms, 4), "frac": round(tf / peak_fp8, 4)}
         avg = statistics.mean(v["tflops"] for v in g.values())
         pipe_ms = (timer.totals["gemm_quantize"] + timer.totals["gemm_repack"]
                    + sum(timer.totals[f"gemm_{f}_{o}"] for f, o in Gemm.CASES)) / args.steps / 2
+        line["scaled_matmul_vendor"] = vendor_gemm_reference(torch, parts["gemm"], args.steps)
         line["scaled_matmul"] = {
             "value": round(avg, 1), "unit": "TFLOP/s", "config": "M=N=K=8192, E8M0 per 32 along K",
-            "cases": g, "pipeline_tflops_incl_quantize_repack": round(GEMM_FLOP / (pipe_ms * 1e-3) / 1e12, 1),
-            "quantize_operands_ms": round(timer.totals["gemm_quantize"] / timer.counts["gemm_quantize"], 4),
-            "repack_ms": round(timer.totals["gemm_repack"] / timer.counts["gemm_repack"], 4),
+            "pipeline_tflops_incl_quantize_repack": round(GEMM_FLOP / (pipe_ms * 1e-3) / 1e12, 1),
+            "cases": g,
             "roofline": {"bound": "tensor", "kernel": "mx_gemm_2sm_kernel", "achieved": round(avg, 1),
                          "peak": round(peak_fp8, 1), "unit": "TFLOP/s", "frac": round(avg / peak_fp8, 4),
-                         "peak_source": f"{peaks['src']} bf16 burst x {FP8_OVER_BF16} (nominal MXFP8/bf16)",
+                         "peak_source": fp8_src,
                          "traffic": profiled_traffic("mx_gemm_2sm_kernel", source_hash("gemm.cu"))}}
-    if "gemm" in parts:
-        line["scaled_matmul"]["vendor_reference"] = vendor_gemm_reference(torch, parts["gemm"], args.steps)
     if "fp4" in parts:
         ms = timer.avg_ms("fp4") / Fp4.LAUNCHES   # per launch, from the span of back-to-back launches
         gbs = FP4_BYTES / (ms * 1e-3) / 1e9
         line["fp4_quantize"] = {"value": round(gbs, 1), "unit": "GB/s", "ms": round(ms, 4),
-                                "config": "[16384,16384] bf16 -> e2m1, 8x4, interleaved scales; "
-                                          f"{Fp4.LAUNCHES} back-to-back launches a step on different inputs",
-                                "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm"],
-                                             "unit": "GB/s", "frac": round(gbs / peaks["hbm"], 4),
-                                             "peak_source": peaks["src"]}}
+                                "config": f"[16384,16384] bf16 -> e2m1, 8x4, interleaved; {Fp4.LAUNCHES} launches "
+                                          "a span",
+                                "roofline": {"bound": "hbm", "kernel": "quant_g84<e2m1>", "achieved": round(gbs, 1),
+                                             "peak": peaks["hbm"], "unit": "GB/s",
+                                             "frac": round(gbs / peaks["hbm"], 4), "peak_source": peaks["src"],
+                                             "traffic": profiled_traffic("quant_g84_fp4",
+                                                                         source_hash("quantize.cu"))}}
     if "dequant" in parts:
         ms = timer.avg_ms("dequant") / Dequant.LAUNCHES   # per launch, from the span
         gbs = SWEEP_BYTES / (ms * 1e-3) / 1e9
         line["dequantize"] = {"value": round(gbs, 1), "unit": "GB/s", "ms": round(ms, 4),
-                              "config": "[8192,8192] e4m3fn + 8x4 plain scales -> bf16; "
-                                        f"{Dequant.LAUNCHES} back-to-back launches a step over 2 buffer sets",
+                              "config": f"[8192,8192] e4m3fn + 8x4 scales -> bf16; {Dequant.LAUNCHES} launches a span",
                               "roofline": {"bound": "hbm", "kernel": "dequant_kernel", "achieved": round(gbs, 1),
                                            "peak": peaks["hbm"], "unit": "GB/s",
                                            "frac": round(gbs / peaks["hbm"], 4), "peak_source": peaks["src"],
                                            "traffic": profiled_traffic("dequant_kernel",
                                                                        source_hash("dequantize.cu"))}}
     if "fused" in parts:
+        fu = parts["fused"]
         ms = timer.avg_ms("fused")
         tf = FUSED_FLOP / (ms * 1e-3) / 1e12
-        peak_fp8 = peaks["bf16"] * FP8_OVER_BF16
         q_ms, g_ms = timer.avg_ms("fused_split_quantize"), timer.avg_ms("fused_split_gemm")
         line["fused"] = {"value": round(tf, 1), "unit": "TFLOP/s", "ms": round(ms, 4),
-                         "unfused": {"quantize_x_ms": round(q_ms, 4), "gemm_ms": round(g_ms, 4),
-                                     "total_ms": round(q_ms + g_ms, 4),
-                                     "tflops": round(FUSED_FLOP / ((q_ms + g_ms) * 1e-3) / 1e12, 1),
-                                     "what": "QuantizeMX of X to SF-layout scales, then ScaledMatmul, as two calls"},
-                         "config": "X[16384,8192] bf16 -> e4m3fn (1x32 along K) x W[8192,28672] e4m3fn -> bf16",
-                         "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": round(peak_fp8, 1),
-                                      "unit": "TFLOP/s", "frac": round(tf / peak_fp8, 4),
-                                      "peak_source": f"{peaks['src']} bf16 burst x {FP8_OVER_BF16}"}}
+                         "launches_per_call": fu.launches_per_call,
+                         "two_launches": {"quantize_x_ms": round(q_ms, 4), "gemm_ms": round(g_ms, 4),
+                                          "total_ms": round(q_ms + g_ms, 4),
+                                          "tflops": round(FUSED_FLOP / ((q_ms + g_ms) * 1e-3) / 1e12, 1)},
+                         "config": "X[16384,8192] bf16 quantized along K to e4m3fn in the GEMM launch, "
+                                   "x W[8192,28672] e4m3fn -> bf16",
+                         "roofline": {"bound": "tensor", "kernel": "mx_gemm_2sm_kernel<fused e4m3fn>",
+                                      "achieved": round(tf, 1), "peak": round(peak_fp8, 1), "unit": "TFLOP/s",
+                                      "frac": round(tf / peak_fp8, 4), "peak_source": fp8_src,
+                                      "traffic": profiled_traffic("mx_gemm_2sm_kernel_fused",
+                                                                  source_hash("gemm.cu"))}}
 
     if "gemm_fp4" in parts:
         ms = timer.avg_ms("gemm_fp4")
@@ -997,14 +1064,15 @@ def main():
             "pipeline_tflops_incl_quantize_repack": round(GEMM_FLOP / (pipe_ms * 1e-3) / 1e12, 1),
             "roofline": {"bound": "tensor", "kernel": "mx_gemm_2sm_kernel<true>", "achieved": round(tf, 1),
                          "peak": round(peak_fp4, 1), "unit": "TFLOP/s", "frac": round(tf / peak_fp4, 4),
-                         "peak_source": f"{peaks['src']} bf16 burst x {FP4_OVER_BF16} (nominal FP4/bf16)"}}
+                         "peak_source": f"{peaks['src']} bf16 burst x {FP4_OVER_BF16} (nominal FP4/bf16)",
+                         "traffic": profiled_traffic("mx_gemm_2sm_kernel_fp4", source_hash("gemm.cu"))}}
         line["scaled_matmul_fp4"]["vendor_reference"] = vendor_fp4_reference(torch, parts["gemm_fp4"], args.steps)
     if "pipeline_256" in parts:
         us = timer.avg_ms("pipeline_256") * 1e3
         line["pipeline_256"] = {"us": round(us, 2), "tflops": round(2 * 256 ** 3 / (us * 1e-6) / 1e12, 3),
                                 "us_cuda_graph": round(parts["pipeline_256"].graph_us(), 2),
-                                "config": "M=N=K=256 bf16 -> quantize A, Bt (1x32 along K, e4m3fn) -> repack x2 -> "
-                                          "ScaledMatmul -> f32; 5 launches, latency-bound (no roofline claimed)"}
+                                "config": "M=N=K=256: quantize A, Bt (1x32 along K, e4m3fn), repack x2, "
+                                          "ScaledMatmul -> f32; 5 launches, latency-bound"}
     if "gemm_small_m" in parts:
         sm = parts["gemm_small_m"]
         cases = {}
@@ -1024,7 +1092,6 @@ def main():
                          "note": f"M = {max(SMALL_M)}; bytes = B + A + both scale tensors + C"}}
         line["scaled_matmul_small_m"]["vendor_reference"] = vendor_small_m_reference(torch, sm, args.steps)
     if "dot" in parts:
-        peak_fp8 = peaks["bf16"] * FP8_OVER_BF16
         cases = {}
         for c in Dot.CASES:
             ms = timer.avg_ms(f"dot_{c}")
@@ -1032,13 +1099,12 @@ def main():
         best = cases["rhs_bnk"]["tflops"]
         line["block_scaled_dot"] = {
             "value": best, "unit": "TFLOP/s",
-            "config": "16 x 2048^3 e4m3fn -> bf16, batch dim 0, K innermost on lhs; rhs [B,N,K] in place or "
-                      "[B,K,N] via the transposing copy; whole call (permute + repack + GEMM)",
+            "config": "16 x 2048^3 e4m3fn -> bf16, batch dim 0, K innermost on lhs; rhs [B,N,K] or [B,K,N]; "
+                      "whole call",
             "cases": cases,
             "roofline": {"bound": "tensor", "kernel": "mx_gemm_2sm_kernel", "achieved": best,
                          "peak": round(peak_fp8, 1), "unit": "TFLOP/s", "frac": round(best / peak_fp8, 4),
-                         "peak_source": f"{peaks['src']} bf16 burst x {FP8_OVER_BF16}",
-                         "note": "achieved over the whole call, repack launches included"}}
+                         "peak_source": fp8_src, "note": "whole call, repack launches included"}}
 
     # end to end through the public API with host buffers: one
     # mx_quantize_host_batch call per step takes the 8 pinned host inputs and
@@ -1092,20 +1158,26 @@ def main():
                                "copies in, QuantizeMX, copies out to pinned host, overlapped; one call per step"}
 
     if rank == 0 and not args.no_cpu_baseline:
-        v, dt, n, desc = oracle_sweep_sample(rows=2048)
-        line["cpu_baseline"] = {"value": round(v, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+        v, dt, cores, desc = oracle_sweep_parallel()
+        line["cpu_baseline"] = {"value": round(v, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
                                 "sample": desc, "seconds": round(dt, 2)}
         if "gemm" in parts:
-            tf, dtg = oracle_gemm_sample(rows=2)
-            line["cpu_baseline"]["scaled_matmul"] = {"value": round(tf, 6), "unit": "TFLOP/s", "cores": 1,
-                                                     "sample": "2 full output rows of the 8192^3 product, "
-                                                               "binary64 k-ordered sums",
+            tf, dtg, gcores = oracle_gemm_parallel()
+            line["cpu_baseline"]["scaled_matmul"] = {"value": round(tf, 6), "unit": "TFLOP/s", "cores": gcores,
+                                                     "sample": f"{gcores} full output rows of the 8192^3 product, "
+                                                               "binary64 k-ordered sums, one row a core",
                                                      "seconds": round(dtg, 2)}
         if "pipeline_256" in parts:
             us = oracle_pipeline_256()
             line["cpu_baseline"]["pipeline_256"] = {"us": round(us, 1), "cores": 1,
-                                                    "sample": "the whole 256^3 pipeline: oracle QuantizeMX of A "
-                                                              "and Bt, binary64 dequantize-then-matmul"}
+                                                    "sample": "the whole 256^3 pipeline on one core"}
+    # secondary results first, the headline ones last (readers that keep
+    # only the end of the line still see them)
+    order = ["metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better", "scaling",
+             "vs_baseline", "dtype", "data", "gpu_launches", "config", "roofline", "clocks", "e2e", "cpu_baseline",
+             "scaled_matmul_small_m", "block_scaled_dot", "pipeline_256", "scaled_matmul_vendor", "dequantize",
+             "scaled_matmul_fp4", "fp4_quantize", "fused", "scaled_matmul"]
+    line = {k: line[k] for k in order if k in line} | {k: v for k, v in line.items() if k not in order}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if ws > 1:

@@ -325,7 +325,7 @@ mx_status mx_scaled_matmul_noalloc(const void* a, const void* bt, const uint8_t*
 /*
  * Workspace bytes of mx_fused_quantize_matmul: the quantized activation
  * (M*K bytes, at offset 0), its SF-layout scales (at offset
- * round16(M*K)), then ceil(M/128) * ceil(K/256) 64-bit ready words (at
+ * round16(M*K)), then ceil(M/128) * ceil(K/256) + 1 64-bit ready words (at
  * offset round16(M*K) + round16(ceil(M/128) * ceil(K/128) * 512)), each
  * part 16-byte aligned; round16(x) rounds x up to a multiple of 16.
  */
@@ -349,11 +349,9 @@ mx_status mx_fused_quantize_matmul_workspace(int64_t M, int64_t N, int64_t K, si
  *   the workspace holds QuantizeMX(X) afterwards (codes and SF-layout scales
  *   at the offsets above; scale bytes of rows past M are unspecified).  The
  *   ready words need no clearing: a launch only accepts words it wrote itself
- *   (a per-call tag), and one that completes leaves them all zero, so
+ *   (a per-call tag), and its last CTA sets them all back to zero, so
  *   reusing a workspace, and replaying a captured call, are both safe.
- *   After a call that ended in MX_ERR_TIMEOUT, zero the ready words before
- *   replaying that captured call.  Calls that share a workspace must not
- *   overlap on the GPU.
+ *   Calls that share a workspace must not overlap on the GPU.
  *   x, x_dtype   device [M, ld_x] MX_BF16 | MX_F16
  *   wt, w_scale_sf  device codes [N, K] and SF-layout scales (mx_repack_scales);
  *                for MX_E2M1 X is packed in the tensor-core nibble order

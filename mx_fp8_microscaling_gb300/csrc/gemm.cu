@@ -110,6 +110,7 @@ struct KParams {
     int64_t sfa_batch_tiles;  // 512-byte scale tiles per problem (A / B)
     int64_t sfb_batch_tiles;
     int group_m;
+    int first_group_m;    // M-tiles of the first group (<= group_m; smaller in the fused kernel)
     uint32_t idesc;
     uint32_t idesc_half;  // the same MMA with N = 128 (split tail tiles of the pair kernel)
     int full_rounds;      // pair kernel: rounds of whole tiles before a split tail round
@@ -125,8 +126,8 @@ struct KParams {
     int64_t q_ld_x;       // bytes between rows of X
     uint8_t* q_xq;        // codes [M, K] (FP8) or [M, K / 2] (e2m1)
     uint8_t* q_sf;
-    uint64_t* q_flags;    // one ready word per item, [q_panels, q_nkc]
-    uint64_t q_tag;       // this launch's tag, 40 bits, nonzero (see wait_item_ready)
+    uint64_t* q_flags;    // one ready word per item, [q_panels, q_nkc], then the launch's done word
+    uint64_t q_tag;       // this launch's tag, 40 bits, nonzero (see wait_items_ready)
     int q_f16;            // X is f16 (else bf16)
     int q_panels;         // 128-row panels of X
     int q_nkc;            // items along K per panel
@@ -135,20 +136,35 @@ struct KParams {
     int q_no_publish;     // fault injection: items are never published (the loads' waits time out)
 };
 
-// Tile order: problem by problem; inside one, groups of `group_m` M-tiles,
-// column-major inside a group, so the tiles running at once share A and B
-// panels in L2.
+// Tile order: problem by problem; inside one, groups of M-tiles (the first
+// `first_group_m`, then `group_m` each), column-major inside a group, so the
+// tiles running at once share A and B panels in L2.
 __device__ __forceinline__ void tile_coords(int t, const KParams& p, int& b, int& mt, int& nt) {
     const int per_problem = p.num_m_tiles * p.num_n_tiles;
     b = t / per_problem;
     t -= b * per_problem;
-    const int group = p.group_m * p.num_n_tiles;
-    const int g = t / group;
-    const int first_m = g * p.group_m;
-    const int gm = min(p.num_m_tiles - first_m, p.group_m);
-    const int idx = t - g * group;
+    const int fm = min(p.first_group_m, p.num_m_tiles);
+    int first_m, gm, idx;
+    if (t < fm * p.num_n_tiles) {
+        first_m = 0;
+        gm = fm;
+        idx = t;
+    } else {
+        t -= fm * p.num_n_tiles;
+        const int group = p.group_m * p.num_n_tiles;
+        const int g = t / group;
+        first_m = fm + g * p.group_m;
+        gm = min(p.num_m_tiles - first_m, p.group_m);
+        idx = t - g * group;
+    }
     mt = first_m + idx % gm;
     nt = idx / gm;
+}
+
+// Tile group of M-tile mt (0 for the first group).
+__device__ __forceinline__ int m_tile_group(const KParams& p, int mt) {
+    const int fm = min(p.first_group_m, p.num_m_tiles);
+    return mt < fm ? 0 : 1 + (mt - fm) / p.group_m;
 }
 
 // Work units of the pair kernel's cluster `c` (of `nc`).  Whole 256 x 256
@@ -359,145 +375,177 @@ __device__ __forceinline__ void store_chunk4(const KParams& p, int b, int64_t m,
 // One quantize item: 128 rows (a 128-row panel of A, the rows of one
 // scale-factor tile) x kQChunk elements of X along K, done by the 256 threads
 // of the 8 epilogue warps.  Items are numbered in the order the tiles consume
-// them: tile group by tile group (kQPanelsPerGroup panels each, the group_m
-// pair M-tiles of the tile order), inside a group K chunk by K chunk, panel
-// by panel; CTA c takes items c, c + gridDim.x, ...
-constexpr int kQChunk = 256;            // K elements per item: 2 FP8 stages, 1 FP4 stage
-constexpr int kQPanelsPerGroup = 32;    // 128-row panels in a group of 16 pair M-tiles
+// them: tile group by tile group (two panels per pair M-tile of the group),
+// inside a group K chunk by K chunk, panel by panel; CTA c takes items c,
+// c + gridDim.x, ...
+constexpr int kQChunk = 256;  // K elements per item: 2 FP8 stages, 1 FP4 stage
+// K stages of the current tile that must remain for the epilogue to start
+// an item of a later tile group (an item takes about 8 us, a K stage about
+// 0.33 us).
+constexpr int kQOneStages = 24;
 
 struct QItem {
     int group, panel, kc;
 };
 __device__ __forceinline__ QItem q_item(const KParams& p, int i) {
-    const int per_group = kQPanelsPerGroup * p.q_nkc;
     QItem it;
-    it.group = i / per_group;
-    const int j = i - it.group * per_group;
-    const int gp = min(kQPanelsPerGroup, p.q_panels - it.group * kQPanelsPerGroup);
+    const int fp = min(2 * min(p.first_group_m, p.num_m_tiles), p.q_panels);  // panels of group 0
+    if (i < fp * p.q_nkc) {
+        it.group = 0;
+        it.kc = i / fp;
+        it.panel = i - it.kc * fp;
+        return it;
+    }
+    i -= fp * p.q_nkc;
+    const int per_group = 2 * p.group_m * p.q_nkc;
+    const int g = i / per_group;
+    const int j = i - g * per_group;
+    const int first_panel = fp + g * 2 * p.group_m;
+    const int gp = min(2 * p.group_m, p.q_panels - first_panel);
+    it.group = g + 1;
     it.kc = j / gp;
-    it.panel = it.group * kQPanelsPerGroup + (j - it.kc * gp);
+    it.panel = first_panel + (j - it.kc * gp);
     return it;
 }
 
-// QuantizeMX of one item, 1x32 blocks along K, EMAX (the arithmetic of the
-// standalone quantizer, qdev::): thread t takes 16 consecutive elements of 8
-// rows (rows t/16 + 16 r), so a half-warp reads 512 contiguous bytes of a
-// row and a lane pair holds one block; one xor shuffle finishes the block
-// maximum.  Codes go to q_xq, scales to their SF-layout bytes; scale
-// columns past K inside the last scale tile are written as zero (E8M0 0, so
-// the zero codes the tensor core reads there contribute exactly 0).  All 256
-// threads then fence, meet, and one publishes the item's ready word.
+// QuantizeMX of item i, 1x32 blocks along K, EMAX (the arithmetic of the
+// standalone quantizer, qdev::).  Only the six epilogue warps that do not
+// share a warp scheduler with the MMA-issuing thread (warp 1) do the work:
+// warps 5 and 9 would take issue slots from it, and the MMA issue rate is
+// what bounds the GEMM (with all eight warps quantizing, the fused launch
+// measured 3 % slower).  Their 96 lane pairs take the item's 1024 row blocks
+// (128 rows x 8 blocks of 32) in two batches, a lane pair per block (16
+// elements a lane, one xor shuffle for the block maximum), consecutive pairs
+// along a row so a warp reads 1 KB of two rows per load; all of a batch's
+// loads are issued before any is used.  Codes go to q_xq, scales to their
+// SF-layout bytes; scale columns past K inside the last scale tile are
+// written as zero (E8M0 0, so the zero codes the tensor core reads there
+// contribute exactly 0).  All eight warps then meet, and one thread
+// publishes the item's ready word (release at GPU scope after the barrier,
+// which orders every thread's stores before it).
+constexpr int kQWarps = 6;                          // epilogue warps that quantize
+constexpr int kQPairs = kQWarps * 16;               // lane pairs
+constexpr int kQBlocks = 128 * (kQChunk / 32);      // row blocks of an item
+constexpr int kQPerPair = (kQBlocks + kQPairs - 1) / kQPairs;  // 11
+constexpr int kQBatch = (kQPerPair + 1) / 2;        // 6 blocks a batch
+
+__device__ __forceinline__ int q_warp_slot(int warp) {
+    // epilogue warps 2..9; warps 5 and 9 (warp % 4 == 1, warp 1's scheduler) sit out
+    return (warp & 3) == 1 ? -1 : (warp < 5 ? warp - 2 : warp - 3);
+}
+
 template <bool F16, int QFMT>
-__device__ __noinline__ void quant_item(const KParams& p, int i, int tid) {
+__device__ __forceinline__ void quant_item(const KParams& p, int i, int warp, int lane, int tid) {
     using namespace qdev;
+    const int slot = q_warp_slot(warp);
     const QItem it = q_item(p, i);
-    const int col16 = tid & 15;
-    const int64_t k0 = static_cast<int64_t>(it.kc) * kQChunk + col16 * 16;
-    const bool kin = k0 < p.K;
-    const int64_t row0 = static_cast<int64_t>(it.panel) * 128 + (tid >> 4);
-    uint32_t v[8][8];
+    if (slot >= 0) {
+        const int pair = slot * 16 + (lane >> 1);
+        const int half = lane & 1;
 #pragma unroll
-    for (int r = 0; r < 8; ++r) {
-        const int64_t row = row0 + 16 * r;
-        if (kin && row < p.M) {
-            ld_stream_v8(p.q_x + row * p.q_ld_x + k0 * 2, v[r]);
-        } else {
+        for (int j0 = 0; j0 < kQPerPair; j0 += kQBatch) {
+            uint32_t v[kQBatch][8];
+            int64_t row[kQBatch], k0[kQBatch];
+            bool live[kQBatch], kin[kQBatch];
 #pragma unroll
-            for (int w = 0; w < 8; ++w) v[r][w] = 0;
-        }
-    }
-    uint32_t e[8];
-    float sc[8];
-    bool special = false;
+            for (int jj = 0; jj < kQBatch; ++jj) {
+                const int u = pair + kQPairs * (j0 + jj);
+                live[jj] = j0 + jj < kQPerPair && u < kQBlocks;
+                row[jj] = static_cast<int64_t>(it.panel) * 128 + (u >> 3);
+                k0[jj] = static_cast<int64_t>(it.kc) * kQChunk + (u & 7) * 32 + half * 16;
+                kin[jj] = k0[jj] < p.K;
+                live[jj] = live[jj] && row[jj] < p.M;
+                if (live[jj] && kin[jj]) {
+                    ld_stream_v8(p.q_x + row[jj] * p.q_ld_x + k0[jj] * 2, v[jj]);
+                } else {
 #pragma unroll
-    for (int r = 0; r < 8; ++r) {
-        uint32_t m = vmax_u16x2(vmax_u16x2(vmax_u16x2(mag2(v[r][0]), mag2(v[r][1])),
-                                           vmax_u16x2(mag2(v[r][2]), mag2(v[r][3]))),
-                                vmax_u16x2(vmax_u16x2(mag2(v[r][4]), mag2(v[r][5])),
-                                           vmax_u16x2(mag2(v[r][6]), mag2(v[r][7]))));
-        m = hmax(m);
-        m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
-        const uint32_t x = exp_byte_of_mag<F16>(m);
-        special |= (x == 255u);
-        e[r] = e8m0_of(x, p.q_emax);
-        sc[r] = prescale_mul(e[r]);
-    }
-    const int64_t kb32 = k0 >> 5;  // this lane pair's scale column
-#pragma unroll
-    for (int r = 0; r < 8; ++r) {
-        const int64_t row = row0 + 16 * r;
-        if (row >= p.M) break;
-        if (kin) {
-            uint32_t w[4];
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const uint32_t hw[4] = {v[r][4 * h], v[r][4 * h + 1], v[r][4 * h + 2], v[r][4 * h + 3]};
-                // e2m1: the tensor cores' order, element 2i in the low nibble
-                quantize8<F16, QFMT>(hw, sc[r], sc[r], special, 1, 0x3210u, w[2 * h], w[2 * h + 1]);
+                    for (int w = 0; w < 8; ++w) v[jj][w] = 0;
+                }
             }
-            if constexpr (QFMT == kE2M1) {
-                *reinterpret_cast<uint2*>(p.q_xq + row * (p.K / 2) + k0 / 2) = make_uint2(w[0], w[2]);
-            } else {
-                *reinterpret_cast<uint4*>(p.q_xq + row * p.K + k0) = make_uint4(w[0], w[1], w[2], w[3]);
+#pragma unroll
+            for (int jj = 0; jj < kQBatch; ++jj) {
+                // the block: maximum, E8M0, prescale, and whether it holds Inf/NaN
+                uint32_t m = vmax_u16x2(vmax_u16x2(vmax_u16x2(mag2(v[jj][0]), mag2(v[jj][1])),
+                                                   vmax_u16x2(mag2(v[jj][2]), mag2(v[jj][3]))),
+                                        vmax_u16x2(vmax_u16x2(mag2(v[jj][4]), mag2(v[jj][5])),
+                                                   vmax_u16x2(mag2(v[jj][6]), mag2(v[jj][7]))));
+                m = hmax(m);
+                m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
+                const uint32_t x = exp_byte_of_mag<F16>(m);
+                const bool special = x == 255u;
+                const uint32_t e = e8m0_of(x, p.q_emax);
+                const float sc = prescale_mul(e);
+                if (!live[jj]) continue;
+                if (kin[jj]) {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const uint32_t hw[4] = {v[jj][4 * h], v[jj][4 * h + 1], v[jj][4 * h + 2], v[jj][4 * h + 3]};
+                        // e2m1: the tensor cores' order, element 2i in the low nibble
+                        quantize8<F16, QFMT>(hw, sc, sc, special, 1, 0x3210u, w[2 * h], w[2 * h + 1]);
+                    }
+                    if constexpr (QFMT == kE2M1) {
+                        *reinterpret_cast<uint2*>(p.q_xq + row[jj] * (p.K / 2) + k0[jj] / 2) = make_uint2(w[0], w[2]);
+                    } else {
+                        *reinterpret_cast<uint4*>(p.q_xq + row[jj] * p.K + k0[jj]) =
+                            make_uint4(w[0], w[1], w[2], w[3]);
+                    }
+                }
+                const int64_t kb32 = k0[jj] >> 5;
+                if (half == 0 && kb32 < 4 * static_cast<int64_t>(p.sf_ntk)) {
+                    const int64_t r = row[jj];
+                    const int64_t tile = (r >> 7) * p.sf_ntk + (kb32 >> 2);
+                    p.q_sf[tile * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (kb32 & 3)] =
+                        static_cast<uint8_t>(kin[jj] ? e : 0u);
+                }
             }
         }
-        if ((col16 & 1) == 0 && kb32 < 4 * static_cast<int64_t>(p.sf_ntk)) {
-            const int64_t tile = (row >> 7) * p.sf_ntk + (kb32 >> 2);
-            p.q_sf[tile * 512 + (row & 31) * 16 + ((row >> 5) & 3) * 4 + (kb32 & 3)] =
-                static_cast<uint8_t>(kin ? e[r] : 0u);
-        }
     }
-    // publish: every writer's stores ordered before the ready word, for the
-    // generic and the async (TMA) proxy alike
-    fence_proxy_async_global();
-    __threadfence();
     named_bar_sync(kEpiBarrier, NUM_EPI_WARPS * 32);
-    if (tid == 0 && !p.q_no_publish)
-        st_release_gpu_u64(p.q_flags + static_cast<int64_t>(it.panel) * p.q_nkc + it.kc, p.q_tag << 24);
-}
-
-template <int QFMT>
-__device__ __forceinline__ void quant_item_any(const KParams& p, int i, int tid) {
-    if constexpr (QFMT >= 0) {
-        if (p.q_f16) quant_item<true, QFMT>(p, i, tid);
-        else quant_item<false, QFMT>(p, i, tid);
+    if (tid == 0 && !p.q_no_publish) {
+        // the TMA loads that wait on this word read through the async proxy
+        fence_proxy_async_global();
+        st_release_gpu_u64(p.q_flags + static_cast<int64_t>(it.panel) * p.q_nkc + it.kc, p.q_tag);
     }
 }
 
-// Work units (whole tiles, or the two halves of a split tail tile) whose
-// tile has pair M-tile mt: each loads panel 2 mt + rank once per item.
-__device__ __forceinline__ int units_of_m_tile(const KParams& p, int mt, int num_clusters) {
-    const int g = mt / p.group_m;
-    const int first_m = g * p.group_m;
-    const int gm = min(p.num_m_tiles - first_m, p.group_m);
-    if (!p.split_tail) return p.num_n_tiles;
-    // tiles of this mt are t(nt) = g group_m num_n + nt gm + (mt - first_m);
-    // those at or past full_rounds * clusters run as two halves
-    const int64_t base = static_cast<int64_t>(g) * p.group_m * p.num_n_tiles + (mt - first_m);
-    const int64_t tail_start = static_cast<int64_t>(p.full_rounds) * num_clusters;
-    int64_t nt_min = tail_start <= base ? 0 : (tail_start - base + gm - 1) / gm;
-    if (nt_min > p.num_n_tiles) nt_min = p.num_n_tiles;
-    return p.num_n_tiles + static_cast<int>(p.num_n_tiles - nt_min);
+// Item i, bf16 or f16 input.
+template <int QFMT>
+__device__ __forceinline__ void quant_item_any(const KParams& p, int i, int warp, int lane, int tid) {
+    if constexpr (QFMT >= 0) {
+        if (p.q_f16) quant_item<true, QFMT>(p, i, warp, lane, tid);
+        else quant_item<false, QFMT>(p, i, warp, lane, tid);
+    }
 }
 
-// Ready words.  An item's writer stores (tag << 24): the launch's 40-bit tag
-// with a zero count.  Every work unit that loads the item's panel waits
-// (bounded) until the word carries this launch's tag, then adds 1; the unit
-// that makes the count reach the panel's unit count (units_of_m_tile) sets
-// the word back to 0.  So a launch that completes leaves every word 0 (a
-// replay of the same launch, same tag, waits for its own items), a word from
-// an earlier launch never carries this launch's tag, and a word of fresh
-// memory matches it only by a 2^-40 chance.  After the wait the thread's
-// later TMA loads are ordered after the item's stores.  Gives up like
-// mbar_wait_bounded (MX_ERR_TIMEOUT, abort flag).
-__device__ __forceinline__ bool wait_item_ready(const KParams& p, int panel, int kc, int consumers,
-                                                volatile int* abort_flag) {
-    uint64_t* w = p.q_flags + static_cast<int64_t>(panel) * p.q_nkc + kc;
-    if ((ld_acquire_gpu_u64(w) >> 24) != p.q_tag) {
+// Ready words.  An item's writer stores the launch's tag (40 bits, nonzero,
+// different for every call); a word of an earlier launch never holds it, and
+// a word of fresh memory only by a 2^-40 chance.  At its end every CTA counts
+// itself on the done word that follows the ready words, and the last one sets
+// all of them back to zero (end_of_launch), so a replay of the same launch
+// (same tag) waits for its own items again.
+//
+// Bounded wait (one thread) for items kc0 .. kc1 - 1 (at most 4) of 128-row
+// panel `panel`: the words are loaded together (one round trip), then any not
+// yet written are polled.  Afterwards the thread's later TMA loads are
+// ordered after the items' stores.  Gives up like mbar_wait_bounded
+// (MX_ERR_TIMEOUT, abort flag).
+constexpr int kMaxItemsPerWait = 4;
+constexpr int kReadyBitsMax = 4096;  // 128-row panels the producer's shared-memory bitmap covers
+__device__ __forceinline__ bool wait_items_ready(const KParams& p, int panel, int kc0, int kc1,
+                                                 volatile int* abort_flag) {
+    const uint64_t* w = p.q_flags + static_cast<int64_t>(panel) * p.q_nkc + kc0;
+    const int n = kc1 - kc0;
+    uint64_t v[kMaxItemsPerWait];
+#pragma unroll
+    for (int i = 0; i < kMaxItemsPerWait; ++i) v[i] = i < n ? ld_acquire_gpu_u64(w + i) : p.q_tag;
+#pragma unroll
+    for (int i = 0; i < kMaxItemsPerWait; ++i) {
+        if (v[i] == p.q_tag) continue;
         const uint64_t t0 = globaltimer_ns();
         for (;;) {
             __nanosleep(64);
-            if ((ld_acquire_gpu_u64(w) >> 24) == p.q_tag) break;
+            if (ld_acquire_gpu_u64(w + i) == p.q_tag) break;
             if (*abort_flag) return false;
             if (globaltimer_ns() - t0 > p.timeout_ns) {
                 atomicCAS(&g_mx_status, 0, 9);
@@ -507,9 +555,71 @@ __device__ __forceinline__ bool wait_item_ready(const KParams& p, int panel, int
         }
     }
     fence_proxy_async_global();
-    const unsigned long long seen = atomicAdd(reinterpret_cast<unsigned long long*>(w), 1ull);
-    if (static_cast<int>(seen & 0xFFFFFFull) + 1 == consumers) atomicExch(reinterpret_cast<unsigned long long*>(w), 0ull);
     return true;
+}
+
+// The ready-word warp (fused only): walk this CTA's work units in order
+// and, for each unit's panel, poll all of its ready words together (a lane
+// per word) until every item carries this launch's tag, then raise the
+// panel's bit in `ready_bits` (release, CTA scope).  The TMA-issuing thread
+// skips its own waits for a panel whose bit it reads as set (acquire), so in
+// steady state no global ready word is read on the loads' critical path
+// (polled by the issuing thread itself, the words cost 12 % of the fused
+// call; polled by the producer warp's idle lanes, which share the issuing
+// lane's warp, 25 %).  The warp only ever speeds the loads up: it stops
+// (without an error) on the abort flag or after timeout_ns on one panel, and
+// the issuing thread then waits itself.
+__device__ __forceinline__ void ready_helper(const KParams& p, uint32_t bits_saddr, int num_units, int cluster,
+                                             int num_clusters, uint32_t rank, int lane, volatile int* abort_flag) {
+    const uint32_t mask = 0xFFFFFFFFu;
+    for (int u = 0; u < num_units; ++u) {
+        int b, mt, nt, hf;
+        pair_unit_coords(u, p, cluster, num_clusters, b, mt, nt, hf);
+        const int panel = 2 * mt + static_cast<int>(rank);
+        if (panel >= p.q_panels || panel >= kReadyBitsMax) continue;
+        const uint32_t word = bits_saddr + 4u * static_cast<uint32_t>(panel >> 5);
+        if ((ld_acquire_cta_shared_u32(word) >> (panel & 31)) & 1u) continue;
+        const uint64_t* w = p.q_flags + static_cast<int64_t>(panel) * p.q_nkc;
+        const uint64_t t0 = globaltimer_ns();
+        for (;;) {
+            // relaxed polls; the acquire fence below once all are seen
+            bool mine = true;
+            for (int kc = lane; kc < p.q_nkc; kc += 32) mine &= ld_relaxed_gpu_u64(w + kc) == p.q_tag;
+            if (__all_sync(mask, mine)) break;
+            // every lane leaves together (a lane left alone in __all_sync would wait forever)
+            if (__any_sync(mask, *abort_flag != 0 || globaltimer_ns() - t0 > p.timeout_ns)) return;
+            __nanosleep(1000);
+        }
+        fence_acq_rel_gpu();
+        __syncwarp(mask);
+        if (lane == 0) red_release_cta_shared_or(word, 1u << (panel & 31));
+        __syncwarp(mask);
+    }
+}
+
+// One thread per CTA, after every role of the CTA has finished: count this
+// CTA on the done word ((tag << 24) | CTAs counted).  A plain add counts it
+// when the word already carries this launch's tag (every CTA but the first
+// to arrive); an add that finds another tag (a cleared word, or fresh
+// memory) changed nothing that counts, and the CTA then installs the tag
+// with a count of 1 by compare-and-swap, or adds again once another CTA has.
+// Returns true for the last CTA of the launch, which then clears the ready
+// words and the done word.
+__device__ __forceinline__ bool end_of_launch_is_last(const KParams& p) {
+    unsigned long long* d =
+        reinterpret_cast<unsigned long long*>(p.q_flags + static_cast<int64_t>(p.q_panels) * p.q_nkc);
+    __threadfence();
+    unsigned long long now = atomicAdd(d, 1ull) + 1ull;
+    while ((now >> 24) != p.q_tag) {
+        const unsigned long long cur = atomicAdd(d, 0ull);
+        if ((cur >> 24) == p.q_tag) {
+            now = atomicAdd(d, 1ull) + 1ull;
+        } else if (atomicCAS(d, cur, (p.q_tag << 24) | 1ull) == cur) {
+            now = (p.q_tag << 24) | 1ull;
+        }
+    }
+    __threadfence();
+    return static_cast<unsigned>(now & 0xFFFFFFull) == gridDim.x;
 }
 
 // ====================================================== 1-SM, 128 x 256 tiles
@@ -848,11 +958,15 @@ __host__ __device__ constexpr uint32_t off_bar(bool fp4) { return off_sfb(fp4) +
 // full, empty, sf_full [S]; tmem_full, tmem_empty, mma_done, sf_done; group full, empty [slots]
 __host__ __device__ constexpr int num_bars(bool fp4) { return 3 * STAGES + 4 + 2 * sf_slots(fp4); }
 __host__ __device__ constexpr uint32_t off_misc(bool fp4) { return off_bar(fp4) + num_bars(fp4) * 8; }
-__host__ __device__ constexpr uint32_t smem_alloc(bool fp4) { return off_misc(fp4) + 16 + 1024; }
+// misc: tensor-memory address, abort flag, MMA progress (16 bytes), then the
+// fused producer's bitmap of panels seen ready (kReadyBitsMax bits)
+__host__ __device__ constexpr uint32_t smem_alloc(bool fp4) { return off_misc(fp4) + 16 + kReadyBitsMax / 8 + 1024; }
 constexpr uint32_t PAIR_TX = 2 * (A_STAGE + B_STAGE);  // both CTAs' operand tiles of a stage
 __host__ __device__ constexpr uint32_t pair_sf_tx(bool fp4) { return 2 * 3 * sfa_group(fp4); }
 constexpr int SF_WARP = 10;              // warp that copies scale factors to tensor memory
+constexpr int READY_WARP = 11;           // fused only: polls the activation's ready words
 constexpr int THREADS = NUM_THREADS + 32;
+__host__ __device__ constexpr int threads(bool fused) { return THREADS + (fused ? 32 : 0); }
 // Rank 0's C stores are paced over the first kPaceNum / kPaceDen of the next
 // tile's K stages, when a tile has at least kPaceMinStages of them (A/B at
 // 8192 x 8192, CUDA events: FP8 K = 8192 / 2048 +0.9 / +4.5 %, MXFP4 +2 %;
@@ -865,7 +979,7 @@ constexpr int kPaceNum = 1, kPaceDen = 2, kPaceMinStages = 16;
 // tile t is rows 2t and 2t+1; one box is a scale group's consecutive tiles;
 // tiles past the end read as zeros.
 template <bool FP4, int QFMT>
-__global__ void __launch_bounds__(sm2::THREADS, 1)
+__global__ void __launch_bounds__(sm2::threads(QFMT >= 0), 1)
     mx_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                        const __grid_constant__ CUtensorMap tmap_sfa, const __grid_constant__ CUtensorMap tmap_sfb,
                        const KParams p) {
@@ -914,6 +1028,8 @@ __global__ void __launch_bounds__(sm2::THREADS, 1)
         mbar_init(sf_done, 1);
         *abort_flag = 0;
         *mma_issued = 0;
+        if constexpr (FUSED)
+            for (int i = 0; i < kReadyBitsMax / 32; ++i) reinterpret_cast<uint32_t*>(smem + OFF_MISC + 16)[i] = 0;
         fence_mbar_init();
         prefetch_tmap(&tmap_a);
         prefetch_tmap(&tmap_b);
@@ -932,6 +1048,8 @@ __global__ void __launch_bounds__(sm2::THREADS, 1)
     const int num_units = pair_units(p, cluster, num_clusters);
     pdl_wait_prior();  // set-up done; operands, scales and C belong to earlier kernels until here
 
+    // fused: bitmap of panels whose items are all written (zeroed at set-up)
+    const uint32_t ready_bits = sb + OFF_MISC + 16;
     if (warp == 0) {
         if (lane == 0 && !p.skip_producer) {
             int stage = 0, gslot = 0;
@@ -951,8 +1069,34 @@ __global__ void __launch_bounds__(sm2::THREADS, 1)
                 const int64_t sfa_tile = b * p.sfa_batch_tiles + (2 * mt + static_cast<int>(rank)) * p.sf_ntk;
                 const int64_t sfb_tile0 = b * p.sfb_batch_tiles + (2 * nt + (hf < 0 ? 0 : hf)) * p.sf_ntk;
                 const int64_t sfb_tile1 = hf < 0 ? sfb_tile0 + p.sf_ntk : sfb_tile0;
+                // fused: this unit's panel of A must be quantized before its
+                // loads.  Decided once per unit, before the unit's first
+                // wait for a free stage: the panel's bit (raised by the
+                // ready-word warp) says all its items are written; otherwise
+                // each scale group waits for its own items (FP8: 8 stages =
+                // 4 items; FP4: 1 stage = 1 item), also before that group's
+                // wait for a free stage, off the path from a freed stage to
+                // its next loads.
+                const int panel = 2 * mt + static_cast<int>(rank);
+                bool panel_ready = true;
+                if constexpr (FUSED) {
+                    panel_ready = panel >= p.q_panels;
+                    if (!panel_ready && panel < kReadyBitsMax &&
+                        ((ld_acquire_cta_shared_u32(ready_bits + 4u * (panel >> 5)) >> (panel & 31)) & 1u)) {
+                        fence_proxy_async_global();
+                        panel_ready = true;
+                    }
+                }
                 for (int kb = 0; kb < p.num_kb; ++kb) {
                     const bool group_start = kb % SF_GROUP == 0;
+                    if (FUSED && !panel_ready && group_start) {
+                        const int kc0 = FP4 ? kb : kb / 2;
+                        const int kc1 = min(kc0 + (FP4 ? 1 : SF_GROUP / 2), p.q_nkc);
+                        if (!wait_items_ready(p, panel, kc0, kc1, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                    }
                     // a scale slot is free once its last group's copies into
                     // tensor memory have completed (for one-stage groups the
                     // stage's empty barrier already says so)
@@ -965,20 +1109,6 @@ __global__ void __launch_bounds__(sm2::THREADS, 1)
                     if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, p.timeout_ns, &g_mx_status)) {
                         ok = false;
                         break;
-                    }
-                    if constexpr (FUSED) {
-                        // the A rows and scales of this stage's scale group
-                        // (FP8: 8 stages = 4 items; FP4: 1 stage = 1 item)
-                        // must have been quantized and published
-                        const int panel = 2 * mt + static_cast<int>(rank);
-                        if (group_start && panel < p.q_panels) {
-                            const int kc0 = FP4 ? kb : kb / 2;
-                            const int kc1 = min(kc0 + (FP4 ? 1 : SF_GROUP / 2), p.q_nkc);
-                            const int consumers = units_of_m_tile(p, mt, num_clusters);
-                            for (int kc = kc0; kc < kc1 && ok; ++kc)
-                                ok = wait_item_ready(p, panel, kc, consumers, abort_flag);
-                            if (!ok) break;
-                        }
                     }
                     const uint32_t fb = mapa_shared(full_bar(stage), 0);
                     constexpr bool own_bar = SF_GROUP > 1;  // group bytes on a barrier of their own
@@ -1088,6 +1218,11 @@ __global__ void __launch_bounds__(sm2::THREADS, 1)
             volatile int no_abort = 0;
             (void)mbar_wait_bounded(mma_done, 0, &no_abort, 100000000ull, &g_mx_status);
         }
+    } else if (warp == READY_WARP) {
+        if constexpr (FUSED) {
+            if (!p.skip_producer)
+                ready_helper(p, ready_bits, num_units, cluster, num_clusters, rank, lane, abort_flag);
+        }
     } else if (warp == SF_WARP) {
         // Scale-factor copies, one K block at a time, off the MMA thread: a
         // tcgen05.cp costs the issuing thread as much as the four MMAs of a
@@ -1154,6 +1289,8 @@ __global__ void __launch_bounds__(sm2::THREADS, 1)
         const int half = (warp - 2) >> 2;
         const uint32_t tmem_empty_rank0 = mapa_shared(tmem_empty, 0);
         const int epi_tid = threadIdx.x - 64;  // 0 .. 255
+        // the MMA thread's issued-stage count (rank 0's), read through the cluster window
+        const uint32_t issued_rank0 = mapa_shared(smem_u32(const_cast<uint32_t*>(mma_issued)), 0);
         // fused: this CTA's next quantize item and the item count
         int q_next = static_cast<int>(blockIdx.x);
         const int q_total = FUSED ? p.q_panels * p.q_nkc : 0;
@@ -1164,18 +1301,28 @@ __global__ void __launch_bounds__(sm2::THREADS, 1)
             if constexpr (FUSED) {
                 // Until the accumulator is ready, quantize items of X.  One
                 // thread decides for all eight warps (they meet on named
-                // barriers inside an item), so an accumulator that becomes
-                // ready waits at most one item.  Items more than q_lookahead
-                // tile groups ahead of this tile wait for a later tile.
-                const int cur_group = mt / p.group_m;
+                // barriers inside an item).  Items of this tile's group (or
+                // an earlier one) go at once: tiles running now may wait for
+                // them.  Items of later groups (up to q_lookahead ahead)
+                // start only while at least kQOneStages of this tile's K
+                // stages remain to be issued (the MMA thread's count), so
+                // that they end before the accumulator does: an item still
+                // running when the accumulator is ready holds up the next
+                // tile.  Otherwise the warps wait for the accumulator.
+                const int cur_group = m_tile_group(p, mt);
+                const int G = static_cast<int>(gridDim.x);
+                const uint32_t tile_end = static_cast<uint32_t>(u + 1) * static_cast<uint32_t>(p.num_kb);
                 for (;;) {
-                    bool stop = false;
-                    if (epi_tid == 0)
-                        stop = q_next >= q_total || q_item(p, q_next).group > cur_group + p.q_lookahead ||
-                               *abort_flag || mbar_test(tmem_full, acc_phase);
-                    if (named_bar_or(kEpiBarrier, NUM_EPI_WARPS * 32, stop)) break;
-                    quant_item_any<QFMT>(p, q_next, epi_tid);
-                    q_next += static_cast<int>(gridDim.x);
+                    bool go = false;
+                    if (epi_tid == 0 && q_next < q_total && !*abort_flag && !mbar_test(tmem_full, acc_phase)) {
+                        const int g = q_item(p, q_next).group;
+                        go = g <= cur_group ||
+                             (g <= cur_group + p.q_lookahead &&
+                              static_cast<int>(tile_end - ld_shared_cluster_u32(issued_rank0)) >= kQOneStages);
+                    }
+                    if (!named_bar_or(kEpiBarrier, NUM_EPI_WARPS * 32, go)) break;
+                    quant_item_any<QFMT>(p, q_next, warp, lane, epi_tid);
+                    q_next += G;
                 }
             }
             bool ok = true;
@@ -1258,11 +1405,12 @@ __global__ void __launch_bounds__(sm2::THREADS, 1)
         if constexpr (FUSED) {
             // items other CTAs' tiles still wait for (a CTA with no tiles
             // left, or none at all, still owes its share)
+            const int G = static_cast<int>(gridDim.x);
             for (;;) {
                 const bool stop = epi_tid == 0 && (q_next >= q_total || *abort_flag);
                 if (named_bar_or(kEpiBarrier, NUM_EPI_WARPS * 32, stop)) break;
-                quant_item_any<QFMT>(p, q_next, epi_tid);
-                q_next += static_cast<int>(gridDim.x);
+                quant_item_any<QFMT>(p, q_next, warp, lane, epi_tid);
+                q_next += G;
             }
         }
     }
@@ -1272,6 +1420,16 @@ __global__ void __launch_bounds__(sm2::THREADS, 1)
     cluster_sync_all();  // neither CTA frees its memories while the pair may still use them
     tc_fence_after();
     if (warp == 1) tmem_dealloc_pair(tmem_base, TMEM_COLS);
+    if constexpr (FUSED) {
+        // the last CTA of the launch leaves the ready words zero
+        volatile int* last = abort_flag + 2;  // the misc area's spare word
+        if (threadIdx.x == 0) *last = end_of_launch_is_last(p) ? 1 : 0;
+        __syncthreads();
+        if (*last) {
+            const int64_t n = static_cast<int64_t>(p.q_panels) * p.q_nkc + 1;
+            for (int64_t i = threadIdx.x; i < n; i += blockDim.x) p.q_flags[i] = 0;
+        }
+    }
 }
 
 // ------------------------------------------------------------------- host
@@ -1358,6 +1516,7 @@ KParams base_params(const GemmArgs& g, int bm, int bn) {
     p.sfa_batch_tiles = ((g.M + 127) / 128) * static_cast<int64_t>(p.sf_ntk);
     p.sfb_batch_tiles = ((g.N + 127) / 128) * static_cast<int64_t>(p.sf_ntk);
     p.group_m = 16;
+    p.first_group_m = 16;
     p.idesc = fp4 ? make_idesc_mxf4(bm, bn) : make_idesc_mxf8(g.elem_fmt, g.elem_fmt, bm, bn);
     p.timeout_ns = g_timeout_ns;
     p.skip_producer = g_fault_skip_producer & 1;
@@ -1473,10 +1632,10 @@ cudaError_t launch_1sm(const GemmArgs& g, cudaStream_t stream, bool allow_split)
 
 // attr: room for 2 (cluster shape, programmatic serialization)
 void pair_launch_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, int clusters, bool fp4,
-                        cudaStream_t stream) {
+                        cudaStream_t stream, bool fused = false) {
     *cfg = cudaLaunchConfig_t{};
     cfg->gridDim = dim3(2 * clusters, 1, 1);
-    cfg->blockDim = dim3(sm2::THREADS, 1, 1);
+    cfg->blockDim = dim3(sm2::threads(fused), 1, 1);
     cfg->dynamicSmemBytes = sm2::smem_alloc(fp4);
     cfg->stream = stream;
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1565,6 +1724,9 @@ cudaError_t launch_2sm(const GemmArgs& g, cudaStream_t stream) {
         p.q_panels = static_cast<int>((g.M + 127) / 128);
         p.q_nkc = static_cast<int>((g.K + kQChunk - 1) / kQChunk);
         p.q_lookahead = g_fused_lookahead;
+        // a small first tile group: the first wave of tiles then needs the
+        // items of 8 panels of X, not 32, before it runs at full rate
+        p.first_group_m = 4;
         p.q_emax = QFMT == kE4M3 ? 8 : QFMT == kE5M2 ? 15 : 2;
         p.q_no_publish = (g_fault_skip_producer & 2) ? 1 : 0;
         p.skip_producer = g_fault_skip_producer & 1;
@@ -1572,7 +1734,7 @@ cudaError_t launch_2sm(const GemmArgs& g, cudaStream_t stream) {
     g_last_launch = GemmLaunchInfo{QFMT >= 0 ? 3 : 2, 1};
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[2];
-    pair_launch_config(&cfg, attr, clusters, FP4, stream);
+    pair_launch_config(&cfg, attr, clusters, FP4, stream, QFMT >= 0);
     return cudaLaunchKernelEx(&cfg, mx_gemm_2sm_kernel<FP4, QFMT>, ma, mb, msa, msb, p);
 }
 

@@ -487,12 +487,12 @@ mx_status mx_scaled_matmul(const void* a, const void* bt, const uint8_t* a_scale
 
 // Fused workspace: the quantized activation (M*K bytes, enough for FP8 and
 // e2m1), its SF-layout scales, then one 64-bit ready word per quantize item
-// of the single-launch kernel (128 rows x 256 elements).
+// of the single-launch kernel (128 rows x 256 elements) and one done word.
 static size_t fused_flags_offset(int64_t M, int64_t K) {
     return align16(static_cast<size_t>(M * K)) + align16(sf_layout_bytes(M, K));
 }
 static size_t fused_flag_bytes(int64_t M, int64_t K) {
-    return static_cast<size_t>((M + 127) / 128) * static_cast<size_t>((K + 255) / 256) * 8u;
+    return (static_cast<size_t>((M + 127) / 128) * static_cast<size_t>((K + 255) / 256) + 1) * 8u;
 }
 
 mx_status mx_fused_quantize_matmul_workspace(int64_t M, int64_t N, int64_t K, size_t* bytes) {

@@ -261,6 +261,34 @@ __device__ __forceinline__ void st_release_gpu_u64(uint64_t* p, uint64_t v) {
     asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
+// Relaxed 64-bit global load at GPU scope (polling; pair with
+// fence_acq_rel_gpu once the value is seen, for acquire ordering).
+__device__ __forceinline__ uint64_t ld_relaxed_gpu_u64(const uint64_t* p) {
+    uint64_t v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
+// Plain load of a 32-bit shared-memory word of any CTA of the cluster
+// (`cluster_addr` from mapa_shared).
+__device__ __forceinline__ uint32_t ld_shared_cluster_u32(uint32_t cluster_addr) {
+    uint32_t v;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(cluster_addr) : "memory");
+    return v;
+}
+
+// Shared-memory word with acquire / release semantics at CTA scope (a flag
+// one thread of the CTA raises for another).
+__device__ __forceinline__ uint32_t ld_acquire_cta_shared_u32(uint32_t saddr) {
+    uint32_t v;
+    asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(saddr) : "memory");
+    return v;
+}
+__device__ __forceinline__ void red_release_cta_shared_or(uint32_t saddr, uint32_t bits) {
+    asm volatile("red.release.cta.shared::cta.or.b32 [%0], %1;" ::"r"(saddr), "r"(bits) : "memory");
+}
+
 // Orders this thread's generic-proxy accesses of global memory against its
 // async-proxy (TMA) accesses on either side of the fence.
 __device__ __forceinline__ void fence_proxy_async_global() {

@@ -144,8 +144,9 @@ def test_matmul_workspace_sizes(mx):
     assert mx.mx_scaled_matmul_workspace(8192, 8192, 8192, True) == 0
     assert mx.mx_sf_layout_bytes(200, 96) == 2 * 1 * 512
     # fused: codes, SF scales, then one 8-byte ready word per 128 x 256 item
-    assert mx.mx_fused_quantize_matmul_workspace(256, 512, 256) == 256 * 256 + 2 * 2 * 512 + 16
-    # 300 * 1056 codes, 3 x 9 scale tiles, 3 x 5 ready words (120 bytes, rounded up to 128)
+    # and a done word (2 + 1 words: 24 bytes, rounded up to 32)
+    assert mx.mx_fused_quantize_matmul_workspace(256, 512, 256) == 256 * 256 + 2 * 2 * 512 + 32
+    # 300 * 1056 codes, 3 x 9 scale tiles, 3 x 5 + 1 words (128 bytes)
     assert mx.mx_fused_quantize_matmul_workspace(300, 512, 1056) == 300 * 1056 + 3 * 9 * 512 + 128
 
 
