@@ -399,8 +399,10 @@ class Dequant:
 
 
 class Fused:
+    SHAPE = FUSED  # --fused-shape M,N,K (profiling runs a smaller case)
+
     def __init__(self, torch, mx, api):
-        M, N, K = FUSED
+        M, N, K = self.SHAPE
         x_bits, w_bits = syn.fused_operands(M, N, K, seed=0)
         self.x = dev_bits(torch, x_bits, "bf16")
         wt = dev_bits(torch, w_bits, "bf16")
@@ -911,6 +913,8 @@ def main():
                     choices=["all", "sweep", "gemm", "fp4", "fused", "dequant", "dot", "gemm_fp4", "gemm_small_m",
                              "pipeline_256"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--fused-shape", default=None,
+                    help="M,N,K of the fused workload (default 16384,28672,8192; smaller cases for profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
@@ -918,6 +922,8 @@ def main():
         run_reference(args)
         return
 
+    if args.fused_shape:
+        Fused.SHAPE = tuple(int(v) for v in args.fused_shape.split(","))
     import torch
     ws, rank, local = dist_setup()
     torch.cuda.set_device(local)
@@ -1037,15 +1043,16 @@ def main():
     if "fused" in parts:
         fu = parts["fused"]
         ms = timer.avg_ms("fused")
-        tf = FUSED_FLOP / (ms * 1e-3) / 1e12
+        fused_flop = 2 * Fused.SHAPE[0] * Fused.SHAPE[1] * Fused.SHAPE[2]
+        tf = fused_flop / (ms * 1e-3) / 1e12
         q_ms, g_ms = timer.avg_ms("fused_split_quantize"), timer.avg_ms("fused_split_gemm")
         line["fused"] = {"value": round(tf, 1), "unit": "TFLOP/s", "ms": round(ms, 4),
                          "launches_per_call": fu.launches_per_call,
                          "two_launches": {"quantize_x_ms": round(q_ms, 4), "gemm_ms": round(g_ms, 4),
                                           "total_ms": round(q_ms + g_ms, 4),
-                                          "tflops": round(FUSED_FLOP / ((q_ms + g_ms) * 1e-3) / 1e12, 1)},
-                         "config": "X[16384,8192] bf16 quantized along K to e4m3fn in the GEMM launch, "
-                                   "x W[8192,28672] e4m3fn -> bf16",
+                                          "tflops": round(fused_flop / ((q_ms + g_ms) * 1e-3) / 1e12, 1)},
+                         "config": "X[{0},{2}] bf16 quantized along K to e4m3fn in the GEMM launch, "
+                                   "x W[{2},{1}] e4m3fn -> bf16".format(*Fused.SHAPE),
                          "roofline": {"bound": "tensor", "kernel": "mx_gemm_2sm_kernel<fused e4m3fn>",
                                       "achieved": round(tf, 1), "peak": round(peak_fp8, 1), "unit": "TFLOP/s",
                                       "frac": round(tf / peak_fp8, 4), "peak_source": fp8_src,

@@ -339,8 +339,10 @@ mx_status mx_fused_quantize_matmul_workspace(int64_t M, int64_t N, int64_t K, si
  * Wt [N, K] with SF-layout scales.  The result equals QuantizeMX(X) followed
  * by mx_scaled_matmul bit for bit in the quantized operand.
  *   Where the pair GEMM kernel takes the product (M > 128 and enough 256 x 256
- *   tiles; see mx_debug_set_gemm_variant) and x is 32-byte aligned with a
- *   row pitch of a multiple of 32 bytes, the call is ONE kernel launch: its
+ *   tiles; see mx_debug_set_gemm_variant), the product is long (at least 32
+ *   of its 256 x 256 tiles per pair of SMs: shorter ones run faster as two
+ *   launches), and x is 32-byte aligned with a row pitch of a multiple of
+ *   32 bytes, the call is ONE kernel launch: its
  *   epilogue warps quantize X in items of 128 rows x 256 elements, in the
  *   order the tiles consume them, while the tensor cores run, and publish
  *   each item through a ready word in the workspace that the operand loads

@@ -387,6 +387,11 @@ constexpr int kQOneStages = 24;
 struct QItem {
     int group, panel, kc;
 };
+// Items of the first tile group.
+__device__ __forceinline__ int first_group_items(const KParams& p) {
+    return min(2 * min(p.first_group_m, p.num_m_tiles), p.q_panels) * p.q_nkc;
+}
+
 __device__ __forceinline__ QItem q_item(const KParams& p, int i) {
     QItem it;
     const int fp = min(2 * min(p.first_group_m, p.num_m_tiles), p.q_panels);  // panels of group 0
@@ -423,22 +428,23 @@ __device__ __forceinline__ QItem q_item(const KParams& p, int i) {
 // contribute exactly 0).  All eight warps then meet, and one thread
 // publishes the item's ready word (release at GPU scope after the barrier,
 // which orders every thread's stores before it).
-constexpr int kQWarps = 6;                          // epilogue warps that quantize
-constexpr int kQPairs = kQWarps * 16;               // lane pairs
 constexpr int kQBlocks = 128 * (kQChunk / 32);      // row blocks of an item
-constexpr int kQPerPair = (kQBlocks + kQPairs - 1) / kQPairs;  // 11
-constexpr int kQBatch = (kQPerPair + 1) / 2;        // 6 blocks a batch
+constexpr int kQBatch = 6;                          // blocks a lane pair loads before using any
+constexpr int kQEpiWarps = 6;                       // epilogue warps that quantize between tiles
 
 __device__ __forceinline__ int q_warp_slot(int warp) {
     // epilogue warps 2..9; warps 5 and 9 (warp % 4 == 1, warp 1's scheduler) sit out
     return (warp & 3) == 1 ? -1 : (warp < 5 ? warp - 2 : warp - 3);
 }
 
-template <bool F16, int QFMT>
-__device__ __forceinline__ void quant_item(const KParams& p, int i, int warp, int lane, int tid) {
+// The item's work for the lane pairs of NW warps (this warp's `slot` in
+// 0 .. NW-1; -1 = none); the caller then synchronises its threads and
+// publishes.
+template <bool F16, int QFMT, int NW>
+__device__ __forceinline__ void quant_item_body(const KParams& p, const QItem& it, int slot, int lane) {
     using namespace qdev;
-    const int slot = q_warp_slot(warp);
-    const QItem it = q_item(p, i);
+    constexpr int kQPairs = NW * 16;
+    constexpr int kQPerPair = (kQBlocks + kQPairs - 1) / kQPairs;
     if (slot >= 0) {
         const int pair = slot * 16 + (lane >> 1);
         const int half = lane & 1;
@@ -501,20 +507,41 @@ __device__ __forceinline__ void quant_item(const KParams& p, int i, int warp, in
             }
         }
     }
-    named_bar_sync(kEpiBarrier, NUM_EPI_WARPS * 32);
-    if (tid == 0 && !p.q_no_publish) {
-        // the TMA loads that wait on this word read through the async proxy
-        fence_proxy_async_global();
-        st_release_gpu_u64(p.q_flags + static_cast<int64_t>(it.panel) * p.q_nkc + it.kc, p.q_tag);
-    }
 }
 
-// Item i, bf16 or f16 input.
+// One thread publishes an item once every thread that wrote it has passed a
+// barrier with it (release at GPU scope after the barrier, which orders
+// every thread's stores before it).
+__device__ __forceinline__ void publish_item(const KParams& p, const QItem& it) {
+    if (p.q_no_publish) return;
+    // the TMA loads that wait on this word read through the async proxy
+    fence_proxy_async_global();
+    st_release_gpu_u64(p.q_flags + static_cast<int64_t>(it.panel) * p.q_nkc + it.kc, p.q_tag);
+}
+
+// Item i by the epilogue warps (bf16 or f16 input): the six that do not
+// share warp 1's scheduler work, all eight meet on the epilogue barrier.
 template <int QFMT>
 __device__ __forceinline__ void quant_item_any(const KParams& p, int i, int warp, int lane, int tid) {
     if constexpr (QFMT >= 0) {
-        if (p.q_f16) quant_item<true, QFMT>(p, i, warp, lane, tid);
-        else quant_item<false, QFMT>(p, i, warp, lane, tid);
+        const QItem it = q_item(p, i);
+        if (p.q_f16) quant_item_body<true, QFMT, kQEpiWarps>(p, it, q_warp_slot(warp), lane);
+        else quant_item_body<false, QFMT, kQEpiWarps>(p, it, q_warp_slot(warp), lane);
+        named_bar_sync(kEpiBarrier, NUM_EPI_WARPS * 32);
+        if (tid == 0) publish_item(p, it);
+    }
+}
+
+// Item i by all warps of the CTA, before the roles start (the kernel's
+// prologue: nothing else runs yet, and the first tiles wait for these).
+template <int QFMT, int NW>
+__device__ __forceinline__ void quant_item_all(const KParams& p, int i, int warp, int lane) {
+    if constexpr (QFMT >= 0) {
+        const QItem it = q_item(p, i);
+        if (p.q_f16) quant_item_body<true, QFMT, NW>(p, it, warp, lane);
+        else quant_item_body<false, QFMT, NW>(p, it, warp, lane);
+        __syncthreads();
+        if (threadIdx.x == 0) publish_item(p, it);
     }
 }
 
@@ -966,7 +993,8 @@ __host__ __device__ constexpr uint32_t pair_sf_tx(bool fp4) { return 2 * 3 * sfa
 constexpr int SF_WARP = 10;              // warp that copies scale factors to tensor memory
 constexpr int READY_WARP = 11;           // fused only: polls the activation's ready words
 constexpr int THREADS = NUM_THREADS + 32;
-__host__ __device__ constexpr int threads(bool fused) { return THREADS + (fused ? 32 : 0); }
+constexpr int THREADS_FUSED = THREADS + 32;
+__host__ __device__ constexpr int threads(bool fused) { return fused ? THREADS_FUSED : THREADS; }
 // Rank 0's C stores are paced over the first kPaceNum / kPaceDen of the next
 // tile's K stages, when a tile has at least kPaceMinStages of them (A/B at
 // 8192 x 8192, CUDA events: FP8 K = 8192 / 2048 +0.9 / +4.5 %, MXFP4 +2 %;
@@ -1050,6 +1078,15 @@ __global__ void __launch_bounds__(sm2::threads(QFMT >= 0), 1)
 
     // fused: bitmap of panels whose items are all written (zeroed at set-up)
     const uint32_t ready_bits = sb + OFF_MISC + 16;
+    // fused prologue: every warp quantizes this CTA's items of the first
+    // tile group, which the first wave of tiles needs at once (with the
+    // epilogue warps alone the first tiles ended 17 us later)
+    int q_first = static_cast<int>(blockIdx.x);
+    if constexpr (FUSED) {
+        const int n0 = first_group_items(p);
+        for (; q_first < n0; q_first += static_cast<int>(gridDim.x))
+            quant_item_all<QFMT, THREADS_FUSED / 32>(p, q_first, warp, lane);
+    }
     if (warp == 0) {
         if (lane == 0 && !p.skip_producer) {
             int stage = 0, gslot = 0;
@@ -1090,11 +1127,18 @@ __global__ void __launch_bounds__(sm2::threads(QFMT >= 0), 1)
                 for (int kb = 0; kb < p.num_kb; ++kb) {
                     const bool group_start = kb % SF_GROUP == 0;
                     if (FUSED && !panel_ready && group_start) {
-                        const int kc0 = FP4 ? kb : kb / 2;
-                        const int kc1 = min(kc0 + (FP4 ? 1 : SF_GROUP / 2), p.q_nkc);
-                        if (!wait_items_ready(p, panel, kc0, kc1, abort_flag)) {
-                            ok = false;
-                            break;
+                        // the bit may have been raised since the unit began
+                        if (panel < kReadyBitsMax &&
+                            ((ld_acquire_cta_shared_u32(ready_bits + 4u * (panel >> 5)) >> (panel & 31)) & 1u)) {
+                            fence_proxy_async_global();
+                            panel_ready = true;
+                        } else {
+                            const int kc0 = FP4 ? kb : kb / 2;
+                            const int kc1 = min(kc0 + (FP4 ? 1 : SF_GROUP / 2), p.q_nkc);
+                            if (!wait_items_ready(p, panel, kc0, kc1, abort_flag)) {
+                                ok = false;
+                                break;
+                            }
                         }
                     }
                     // a scale slot is free once its last group's copies into
@@ -1291,8 +1335,8 @@ __global__ void __launch_bounds__(sm2::threads(QFMT >= 0), 1)
         const int epi_tid = threadIdx.x - 64;  // 0 .. 255
         // the MMA thread's issued-stage count (rank 0's), read through the cluster window
         const uint32_t issued_rank0 = mapa_shared(smem_u32(const_cast<uint32_t*>(mma_issued)), 0);
-        // fused: this CTA's next quantize item and the item count
-        int q_next = static_cast<int>(blockIdx.x);
+        // fused: this CTA's next quantize item (after the prologue's) and the item count
+        int q_next = q_first;
         const int q_total = FUSED ? p.q_panels * p.q_nkc : 0;
         uint32_t acc_phase = 0;
         for (int u = 0; u < num_units; ++u) {
@@ -1367,7 +1411,9 @@ __global__ void __launch_bounds__(sm2::threads(QFMT >= 0), 1)
             const int64_t m = static_cast<int64_t>(mt) * BM + rank * 128 + quarter * 32 + lane;
             const int64_t n0 = static_cast<int64_t>(nt) * BN + (hf < 0 ? half : hf) * 128;
             // (fused: only once this CTA's items are all written, so the
-            // wait never stands between another CTA's loads and an item)
+            // wait never stands between a load and an item this CTA owes;
+            // pacing as soon as the next tile's items were written measured
+            // 0.8 % slower)
             const bool paced = rank == 0 && u + 1 < num_units && p.num_kb >= kPaceMinStages &&
                                (!FUSED || q_next >= q_total);
             const uint32_t next_tile = static_cast<uint32_t>(u + 1) * static_cast<uint32_t>(p.num_kb);
@@ -1774,6 +1820,15 @@ cudaError_t launch_scaled_matmul(const GemmArgs& g, cudaStream_t stream) {
     return pair ? launch_2sm<false, -1>(g, stream) : launch_1sm<false>(g, stream, split);
 }
 
+// The fused call runs as one launch when the pair kernel takes the product
+// and the launch is long: the single launch pays a fixed start-up (the first
+// tiles wait for their panels of X, about 15-30 us) where two launches pay
+// QuantizeMX at full bandwidth.  Measured (us, one launch / two launches):
+// 4096 x 8192 x 8192 200 / 173, 8192^3 367 / 338, 8192 x 16384 x 8192
+// 630 / 615; from about 32 pair tiles per cluster on the two are within the
+// run-to-run spread.
+constexpr int kFusedMinTilesPerCluster = 32;
+
 bool fused_single_launch(const GemmArgs& g) {
     if (g_variant == 4 || g.batch != 1) return false;
     const bool x_ok = (reinterpret_cast<uintptr_t>(g.x) & 31u) == 0 && g.ld_x_bytes % 32 == 0 &&
@@ -1781,7 +1836,11 @@ bool fused_single_launch(const GemmArgs& g) {
     if (!x_ok) return false;
     if (g_variant == 2) return true;
     if (g_variant == 1 || g_variant == 3) return false;
-    return is_fp4(g) ? prefer_pair<true>(g) : prefer_pair<false>(g);
+    const bool fp4 = is_fp4(g);
+    if (!(fp4 ? prefer_pair<true>(g) : prefer_pair<false>(g))) return false;
+    const int64_t pair_tiles = ((g.M + 255) / 256) * ((g.N + 255) / 256);
+    const int clusters = fp4 ? max_pair_clusters<true>() : max_pair_clusters<false>();
+    return pair_tiles >= static_cast<int64_t>(kFusedMinTilesPerCluster) * clusters;
 }
 
 cudaError_t launch_fused_matmul(const GemmArgs& g, cudaStream_t stream) {

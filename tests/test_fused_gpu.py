@@ -202,9 +202,11 @@ def test_fused_reused_workspace_takes_no_stale_item(mx, force_pair):
 
 
 def test_fused_automatic_choice(mx):
-    """Without forcing: a product the pair kernel takes runs as one launch;
-    a small-M one as QuantizeMX + the 1-SM GEMM; both against the oracle."""
-    for (M, N, K), want in (((2048, 2048, 512), FUSED_KERNEL), ((64, 512, 512), 1)):
+    """Without forcing: a long product (at least 32 pair tiles per cluster)
+    runs as one launch; a shorter pair-kernel product as QuantizeMX + the
+    pair GEMM; a small-M one as QuantizeMX + the 1-SM GEMM; all against the
+    oracle (sampled rows)."""
+    for (M, N, K), want in (((16384, 12800, 256), FUSED_KERNEL), ((2048, 2048, 512), 2), ((64, 512, 512), 1)):
         x_bits, w_bits = syn.fused_operands(M, N, K, seed=13)
         wq, wsf, wg, ws_plain = _weight(w_bits, "e4m3fn")
         xq_ref, xg, xs = _x_ref(x_bits, "bf16", "e4m3fn", K)
