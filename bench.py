@@ -86,6 +86,14 @@ def source_hash(*names):
     return h.hexdigest()[:16]
 
 
+def _src_hashes():
+    """Hashes of each kernel family's sources (its .cu file and the headers
+    it is built from) that traffic.json entries are keyed on."""
+    return (source_hash("quantize.cu", "quant_math.cuh", "mx_device.cuh", "pdl.cuh"),
+            source_hash("gemm.cu", "tcgen05.cuh", "quant_math.cuh", "mx_device.cuh", "pdl.cuh"),
+            source_hash("dequantize.cu", "mx_device.cuh", "pdl.cuh"))
+
+
 def profiled_traffic(kernel_key, src_hash):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
     on the current kernel source; else None."""
@@ -795,13 +803,14 @@ def host_cores():
         return os.cpu_count() or 1
 
 
-def oracle_sweep_parallel(cores=None):
+def oracle_sweep_parallel(cores=None, rows=None):
     """The oracle on the whole sweep workload: every core quantizes a
     [rows, 8192] slice (rows = 8192 / cores, rounded down to whole
-    interleave groups) of each of the 4 inputs, both scale layouts.  Returns
-    (GB/s over algorithmic bytes, seconds, cores, description)."""
+    interleave groups, unless given) of each of the 4 inputs, both scale
+    layouts.  Returns (GB/s over algorithmic bytes, seconds, cores,
+    description)."""
     cores = cores or host_cores()
-    rows = max(32, 8192 // cores // 32 * 32)
+    rows = rows or max(32, 8192 // cores // 32 * 32)
     nbytes, dt = _run_pool(_oracle_sweep_task, [(rows, i) for i in range(cores)])
     return nbytes / dt / 1e9, dt, cores, \
         f"the sweep's 8 variants over [{rows * cores}, 8192] rows ([{rows}, 8192] a core, own seeds), " \
@@ -881,10 +890,10 @@ def run_reference(args):
     cores = host_cores()
     vals, spans = [], []
     for _ in range(args.warmup):
-        oracle_sweep_parallel(cores)
+        oracle_sweep_parallel(cores, args.reference_rows)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        v, dt, _, desc = oracle_sweep_parallel(cores)
+        v, dt, _, desc = oracle_sweep_parallel(cores, args.reference_rows)
         vals.append(v)
         spans.append(dt)
     total = time.perf_counter() - t0
@@ -913,8 +922,14 @@ def main():
                     choices=["all", "sweep", "gemm", "fp4", "fused", "dequant", "dot", "gemm_fp4", "gemm_small_m",
                              "pipeline_256"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--reference-rows", type=int, default=None,
+                    help="rows of the [rows, 8192] slice each core quantizes in the reference arm (default: the "
+                         "whole sweep workload over all cores; smaller for quick checks)")
     ap.add_argument("--fused-shape", default=None,
                     help="M,N,K of the fused workload (default 16384,28672,8192; smaller cases for profiling)")
+    ap.add_argument("--fused-one-launch", action="store_true",
+                    help="with --workload fused: run the fused call as one launch at any size (profiling small "
+                         "cases; by default shorter products run as two launches)")
     args = ap.parse_args()
     if args.warmup < 3:
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
@@ -930,6 +945,8 @@ def main():
     import mx_fp8_microscaling_gb300 as mx
 
     peaks = load_peaks()
+    global QUANT_SRC, GEMM_SRC, DEQUANT_SRC
+    QUANT_SRC, GEMM_SRC, DEQUANT_SRC = _src_hashes()
     parts = {}
     want = (["sweep", "gemm", "fp4", "dequant", "fused", "dot", "gemm_fp4", "gemm_small_m", "pipeline_256"]
             if args.workload == "all"
@@ -937,6 +954,10 @@ def main():
     builders = {"sweep": Sweep, "gemm": Gemm, "fp4": Fp4, "dequant": Dequant, "fused": Fused, "dot": Dot,
                 "gemm_fp4": GemmFp4, "gemm_small_m": GemmSmallM, "pipeline_256": Pipeline256}
     api = Api(torch, mx)
+    if args.fused_one_launch:
+        if want != ["fused"]:
+            raise SystemExit("--fused-one-launch needs --workload fused")
+        mx.mx_debug_set_gemm_variant(2)
     for name in want:
         parts[name] = builders[name](torch, mx, api)
     torch.cuda.synchronize()
@@ -997,7 +1018,7 @@ def main():
                      "roofline": {"bound": "hbm", "kernel": "quant_g84", "achieved": round(achieved, 1),
                                   "peak": peaks["hbm"], "unit": "GB/s",
                                   "frac": round(achieved / peaks["hbm"], 4), "peak_source": peaks["src"],
-                                  "traffic": profiled_traffic("quant_g84", source_hash("quantize.cu"))}})
+                                  "traffic": profiled_traffic("quant_g84", QUANT_SRC)}})
     else:
         line.update({"value": None, "unit": None, "config": {"workload": args.workload}})
 
@@ -1018,7 +1039,7 @@ def main():
             "roofline": {"bound": "tensor", "kernel": "mx_gemm_2sm_kernel", "achieved": round(avg, 1),
                          "peak": round(peak_fp8, 1), "unit": "TFLOP/s", "frac": round(avg / peak_fp8, 4),
                          "peak_source": fp8_src,
-                         "traffic": profiled_traffic("mx_gemm_2sm_kernel", source_hash("gemm.cu"))}}
+                         "traffic": profiled_traffic("mx_gemm_2sm_kernel", GEMM_SRC)}}
     if "fp4" in parts:
         ms = timer.avg_ms("fp4") / Fp4.LAUNCHES   # per launch, from the span of back-to-back launches
         gbs = FP4_BYTES / (ms * 1e-3) / 1e9
@@ -1029,7 +1050,7 @@ def main():
                                              "peak": peaks["hbm"], "unit": "GB/s",
                                              "frac": round(gbs / peaks["hbm"], 4), "peak_source": peaks["src"],
                                              "traffic": profiled_traffic("quant_g84_fp4",
-                                                                         source_hash("quantize.cu"))}}
+                                                                         QUANT_SRC)}}
     if "dequant" in parts:
         ms = timer.avg_ms("dequant") / Dequant.LAUNCHES   # per launch, from the span
         gbs = SWEEP_BYTES / (ms * 1e-3) / 1e9
@@ -1039,7 +1060,7 @@ def main():
                                            "peak": peaks["hbm"], "unit": "GB/s",
                                            "frac": round(gbs / peaks["hbm"], 4), "peak_source": peaks["src"],
                                            "traffic": profiled_traffic("dequant_kernel",
-                                                                       source_hash("dequantize.cu"))}}
+                                                                       DEQUANT_SRC)}}
     if "fused" in parts:
         fu = parts["fused"]
         ms = timer.avg_ms("fused")
@@ -1057,7 +1078,7 @@ def main():
                                       "achieved": round(tf, 1), "peak": round(peak_fp8, 1), "unit": "TFLOP/s",
                                       "frac": round(tf / peak_fp8, 4), "peak_source": fp8_src,
                                       "traffic": profiled_traffic("mx_gemm_2sm_kernel_fused",
-                                                                  source_hash("gemm.cu"))}}
+                                                                  GEMM_SRC)}}
 
     if "gemm_fp4" in parts:
         ms = timer.avg_ms("gemm_fp4")
@@ -1072,7 +1093,7 @@ def main():
             "roofline": {"bound": "tensor", "kernel": "mx_gemm_2sm_kernel<true>", "achieved": round(tf, 1),
                          "peak": round(peak_fp4, 1), "unit": "TFLOP/s", "frac": round(tf / peak_fp4, 4),
                          "peak_source": f"{peaks['src']} bf16 burst x {FP4_OVER_BF16} (nominal FP4/bf16)",
-                         "traffic": profiled_traffic("mx_gemm_2sm_kernel_fp4", source_hash("gemm.cu"))}}
+                         "traffic": profiled_traffic("mx_gemm_2sm_kernel_fp4", GEMM_SRC)}}
         line["scaled_matmul_fp4"]["vendor_reference"] = vendor_fp4_reference(torch, parts["gemm_fp4"], args.steps)
     if "pipeline_256" in parts:
         us = timer.avg_ms("pipeline_256") * 1e3
@@ -1095,7 +1116,7 @@ def main():
             "cases": cases,
             "roofline": {"bound": "hbm", "kernel": "mx_gemm_kernel (split-K)", "achieved": top["gbs"],
                          "peak": peaks["hbm"], "unit": "GB/s", "frac": top["frac"], "peak_source": peaks["src"],
-                         "traffic": profiled_traffic("mx_gemm_kernel_small_m", source_hash("gemm.cu")),
+                         "traffic": profiled_traffic("mx_gemm_kernel_small_m", GEMM_SRC),
                          "note": f"M = {max(SMALL_M)}; bytes = B + A + both scale tensors + C"}}
         line["scaled_matmul_small_m"]["vendor_reference"] = vendor_small_m_reference(torch, sm, args.steps)
     if "dot" in parts:
