@@ -99,6 +99,7 @@ def _load():
         "mx_debug_gemm_fault_injection": [I, ctypes.c_uint64],
         "mx_debug_set_gemm_variant": [I],
         "mx_debug_last_gemm_launch": [P, P],
+        "mx_debug_last_gemm_operands": [P, P],
     }
     for name, args in sigs.items():
         fn = getattr(lib, name)
@@ -481,6 +482,15 @@ def mx_debug_last_gemm_launch():
     kernel, split = ctypes.c_int(0), ctypes.c_int(0)
     _check(_lib.mx_debug_last_gemm_launch(ctypes.byref(kernel), ctypes.byref(split)), "mx_debug_last_gemm_launch")
     return kernel.value, split.value
+
+
+def mx_debug_last_gemm_operands():
+    """(a_mn_major, b_mn_major) of the last ScaledMatmul launch: 1 where the
+    operand was read in place as MN-major tiles (a dot operand stored
+    [batch..., K, rows...]), 0 for K-major rows."""
+    a, b = ctypes.c_int(0), ctypes.c_int(0)
+    _check(_lib.mx_debug_last_gemm_operands(ctypes.byref(a), ctypes.byref(b)), "mx_debug_last_gemm_operands")
+    return a.value, b.value
 
 
 def raw_library() -> ctypes.CDLL:

@@ -134,6 +134,9 @@ struct KParams {
     int q_lookahead;      // tile groups past the CTA's current one whose items it may quantize
     int q_emax;           // EMAX of the element format
     int q_no_publish;     // fault injection: items are never published (the loads' waits time out)
+    // Pair kernel, FP8 only: A (B) is stored [batch, K, M] ([batch, K, N]),
+    // M (N) innermost; its tiles are loaded and fed to the MMA MN-major.
+    int a_mn, b_mn;
 };
 
 // Tile order: problem by problem; inside one, groups of M-tiles (the first
@@ -1176,8 +1179,15 @@ __global__ void __launch_bounds__(sm2::threads(QFMT >= 0), 1)
                             gphase ^= 1u;
                         }
                     }
-                    tma_load_3d_pair(sb + OFF_A + stage * A_STAGE, &tmap_a, fb, kb * BK, a_row, b);
-                    tma_load_3d_pair(sb + OFF_B + stage * B_STAGE, &tmap_b, fb, kb * BK, b_row, b);
+                    // K-major tiles: (K bytes, rows); MN-major: (rows, K rows)
+                    if (p.a_mn)
+                        tma_load_3d_pair(sb + OFF_A + stage * A_STAGE, &tmap_a, fb, a_row, kb * BK, b);
+                    else
+                        tma_load_3d_pair(sb + OFF_A + stage * A_STAGE, &tmap_a, fb, kb * BK, a_row, b);
+                    if (p.b_mn)
+                        tma_load_3d_pair(sb + OFF_B + stage * B_STAGE, &tmap_b, fb, b_row, kb * BK, b);
+                    else
+                        tma_load_3d_pair(sb + OFF_B + stage * B_STAGE, &tmap_b, fb, kb * BK, b_row, b);
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
@@ -1242,9 +1252,13 @@ __global__ void __launch_bounds__(sm2::threads(QFMT >= 0), 1)
                         for (int kk = 0; kk < BK / 32; ++kk) {
                             const uint32_t idesc = unit_idesc | (static_cast<uint32_t>(kk) << 4) |
                                                    (static_cast<uint32_t>(kk) << 29);
-                            tc_mma_mxf8_pair(tmem_base, sdesc_kmajor_sw128(sa + kk * 32),
-                                             sdesc_kmajor_sw128(sbb + kk * 32), idesc, sf_t, sf_t + 4u,
-                                             (kb | kk) != 0);
+                            // 32 K elements: 32 bytes into a K-major row, 32
+                            // rows of 128 bytes into an MN-major tile
+                            const uint64_t da = p.a_mn ? sdesc_mnmajor_sw128(sa + kk * 32 * 128)
+                                                       : sdesc_kmajor_sw128(sa + kk * 32);
+                            const uint64_t db = p.b_mn ? sdesc_mnmajor_sw128(sbb + kk * 32 * 128)
+                                                       : sdesc_kmajor_sw128(sbb + kk * 32);
+                            tc_mma_mxf8_pair(tmem_base, da, db, idesc, sf_t, sf_t + 4u, (kb | kk) != 0);
                         }
                     }
                     tc_commit_pair_mc(empty_bar(stage), 3);
@@ -1511,6 +1525,25 @@ bool make_operand_map(CUtensorMap* map, const void* base, int64_t rows, int64_t 
     return r == CUDA_SUCCESS;
 }
 
+// MN-major FP8 operands [batch, k, mn] (rows of `mn` bytes, one per K index;
+// problem stride `batch_stride` bytes) with a (128 B x 128 K rows x 1) box,
+// 128B swizzle: a K stage of 128 rows along MN.  `mn` must be a multiple of
+// 16 (the row pitch of a tensor map).  Rows past K and columns past mn read
+// as zeros inside each problem.
+bool make_operand_map_mn(CUtensorMap* map, const void* base, int64_t mn, int64_t k, int64_t batch,
+                         int64_t batch_stride) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(mn), static_cast<cuuint64_t>(k), static_cast<cuuint64_t>(batch)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(mn), static_cast<cuuint64_t>(batch_stride)};
+    cuuint32_t box[3] = {128, static_cast<cuuint32_t>(BK), 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 // A scale-factor buffer of `tiles` 512-byte tiles as [2 * tiles, 256] bytes.
 // Tiles past the end read as zeros.  A box is `box_tiles` consecutive tiles
 // (one scale group: SF_GROUP stages of 1 (FP8) or 2 (FP4) tiles).
@@ -1654,6 +1687,7 @@ int choose_split_k(int tiles, int num_kb) {
 
 template <bool FP4>
 cudaError_t launch_1sm(const GemmArgs& g, cudaStream_t stream, bool allow_split) {
+    if (g.a_mn_major || g.b_mn_major) return cudaErrorInvalidValue;  // K-major operands only
     const cudaError_t attr_err = ensure_1sm_attr<FP4>();
     if (attr_err != cudaSuccess) return attr_err;
     CUtensorMap ma, mb;
@@ -1742,9 +1776,12 @@ cudaError_t launch_2sm(const GemmArgs& g, cudaStream_t stream) {
     CUtensorMap ma, mb, msa, msb;
     const int64_t sfa_tiles = g.batch * ((g.M + 127) / 128) * ((g.K + 127) / 128);
     const int64_t sfb_tiles = g.batch * ((g.N + 127) / 128) * ((g.K + 127) / 128);
-    if (!make_operand_map(&ma, g.a, g.M, row_bytes(g), 128, g.batch, g.a_batch_stride) ||
-        !make_operand_map(&mb, g.bt, g.N, row_bytes(g), 128, g.batch, g.b_batch_stride) ||
-        !make_sf_map(&msa, g.sfa, sfa_tiles, sm2::sf_group(FP4) * (FP4 ? 2 : 1)) ||
+    if ((FP4 || QFMT >= 0) && (g.a_mn_major || g.b_mn_major)) return cudaErrorInvalidValue;
+    const bool map_a = g.a_mn_major ? make_operand_map_mn(&ma, g.a, g.M, g.K, g.batch, g.a_batch_stride)
+                                    : make_operand_map(&ma, g.a, g.M, row_bytes(g), 128, g.batch, g.a_batch_stride);
+    const bool map_b = g.b_mn_major ? make_operand_map_mn(&mb, g.bt, g.N, g.K, g.batch, g.b_batch_stride)
+                                    : make_operand_map(&mb, g.bt, g.N, row_bytes(g), 128, g.batch, g.b_batch_stride);
+    if (!map_a || !map_b || !make_sf_map(&msa, g.sfa, sfa_tiles, sm2::sf_group(FP4) * (FP4 ? 2 : 1)) ||
         !make_sf_map(&msb, g.sfb, sfb_tiles, sm2::sf_group(FP4) * (FP4 ? 2 : 1)))
         return cudaErrorInvalidValue;
     KParams p = base_params(g, sm2::BM, sm2::BN);
@@ -1757,6 +1794,11 @@ cudaError_t launch_2sm(const GemmArgs& g, cudaStream_t stream) {
     p.full_rounds = full_rounds;
     p.idesc_half = make_idesc_mxf8(g.elem_fmt, g.elem_fmt, sm2::BM, sm2::BN / 2);
     if (is_fp4(g)) p.idesc_half = make_idesc_mxf4(sm2::BM, sm2::BN / 2);
+    p.a_mn = g.a_mn_major ? 1 : 0;
+    p.b_mn = g.b_mn_major ? 1 : 0;
+    const uint32_t major_bits = (p.a_mn ? kIdescAMnMajor : 0u) | (p.b_mn ? kIdescBMnMajor : 0u);
+    p.idesc |= major_bits;
+    p.idesc_half |= major_bits;
     const int clusters = p.split_tail ? (full_rounds > 0 ? cap : 2 * tail) : (tiles < cap ? tiles : cap);
     p.split_k = 1;
     if constexpr (QFMT >= 0) {
@@ -1777,7 +1819,7 @@ cudaError_t launch_2sm(const GemmArgs& g, cudaStream_t stream) {
         p.q_no_publish = (g_fault_skip_producer & 2) ? 1 : 0;
         p.skip_producer = g_fault_skip_producer & 1;
     }
-    g_last_launch = GemmLaunchInfo{QFMT >= 0 ? 3 : 2, 1};
+    g_last_launch = GemmLaunchInfo{QFMT >= 0 ? 3 : 2, 1, p.a_mn, p.b_mn};
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[2];
     pair_launch_config(&cfg, attr, clusters, FP4, stream, QFMT >= 0);
@@ -1811,10 +1853,17 @@ bool prefer_pair(const GemmArgs& g) {
     return choose_split_k<FP4>(static_cast<int>(tiles_1sm), static_cast<int>((g.K + stage_k - 1) / stage_k)) < 2;
 }
 
-cudaError_t launch_scaled_matmul(const GemmArgs& g, cudaStream_t stream) {
+bool scaled_matmul_takes_pair(const GemmArgs& g) {
     const bool fp4 = is_fp4(g);
     const bool automatic = g_variant == 0 || g_variant == 4;
-    const bool pair = g_variant == 2 || (automatic && (fp4 ? prefer_pair<true>(g) : prefer_pair<false>(g)));
+    return g_variant == 2 || (automatic && (fp4 ? prefer_pair<true>(g) : prefer_pair<false>(g)));
+}
+
+cudaError_t launch_scaled_matmul(const GemmArgs& g, cudaStream_t stream) {
+    const bool fp4 = is_fp4(g);
+    // MN-major operands: the pair kernel reads them (callers check
+    // scaled_matmul_takes_pair first)
+    const bool pair = g.a_mn_major || g.b_mn_major || scaled_matmul_takes_pair(g);
     const bool split = g_variant != 3;
     if (fp4) return pair ? launch_2sm<true, -1>(g, stream) : launch_1sm<true>(g, stream, split);
     return pair ? launch_2sm<false, -1>(g, stream) : launch_1sm<false>(g, stream, split);

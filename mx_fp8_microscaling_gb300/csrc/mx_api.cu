@@ -161,6 +161,9 @@ struct DotPlan {
     int lperm[MX_MAX_RANK] = {}, rperm[MX_MAX_RANK] = {};
     int lc = 0, rc = 0;
     bool lcanon = true, rcanon = true;
+    // stored [batch..., K, free...] (batch axes in order, then the
+    // contracting one): an MN-major operand the pair kernel reads in place
+    bool lmn = false, rmn = false;
     size_t off_lq = 0, off_ls = 0, off_rq = 0, off_rs = 0, off_sfa = 0, off_sfb = 0, total = 0;
 };
 
@@ -220,6 +223,16 @@ mx_status plan_dot(const int64_t* ldims, int lrank, const int64_t* rdims, int rr
     p.rperm[n] = rc;
     for (int i = 0; i < lrank; ++i) p.lcanon = p.lcanon && p.lperm[i] == i;
     for (int i = 0; i < rrank; ++i) p.rcanon = p.rcanon && p.rperm[i] == i;
+    auto mn_order = [nb](const int* perm, int rank) {
+        if (perm[rank - 1] != nb) return false;
+        for (int i = 0; i < nb; ++i)
+            if (perm[i] != i) return false;
+        for (int i = nb; i < rank - 1; ++i)
+            if (perm[i] != i + 1) return false;
+        return true;
+    };
+    p.lmn = !p.lcanon && mn_order(p.lperm, lrank);
+    p.rmn = !p.rcanon && mn_order(p.rperm, rrank);
     if (M > (int64_t(1) << 30) || N > (int64_t(1) << 30) || K > (int64_t(1) << 30)) return MX_ERR_SHAPE;
     // tiles of all problems are counted in 32-bit integers by the kernels
     if (batch * ((M + 127) / 128) * ((N + 127) / 128) > (int64_t(1) << 30)) return MX_ERR_SHAPE;
@@ -605,33 +618,7 @@ mx_status mx_block_scaled_dot(const void* lhs, const int64_t* lhs_dims, int lhs_
     if (!device_is_sm103()) return MX_ERR_DEVICE;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
-    const uint8_t* a = static_cast<const uint8_t*>(lhs);
-    const uint8_t* sa = static_cast<const uint8_t*>(lhs_scale);
-    const uint8_t* bt = static_cast<const uint8_t*>(rhs);
-    const uint8_t* sb = static_cast<const uint8_t*>(rhs_scale);
-    cudaError_t e = cudaSuccess;
-    const int64_t code_div = fp4 ? 2 : 1;  // elements per byte along the contracting axis
-    if (!P.lcanon) {
-        e = permute_operand(lhs, lhs_dims, lhs_rank, P.lperm, P.lc, code_div, ws + P.off_lq, s);
-        if (e == cudaSuccess) e = permute_operand(lhs_scale, lhs_dims, lhs_rank, P.lperm, P.lc, 32, ws + P.off_ls, s);
-        a = ws + P.off_lq;
-        sa = ws + P.off_ls;
-    }
-    if (e == cudaSuccess && !P.rcanon) {
-        e = permute_operand(rhs, rhs_dims, rhs_rank, P.rperm, P.rc, code_div, ws + P.off_rq, s);
-        if (e == cudaSuccess) e = permute_operand(rhs_scale, rhs_dims, rhs_rank, P.rperm, P.rc, 32, ws + P.off_rs, s);
-        bt = ws + P.off_rq;
-        sb = ws + P.off_rs;
-    }
-    const int64_t kb = P.K / 32;
-    if (e == cudaSuccess)
-        e = launch_repack_scales_batched(sa, P.M, P.K, kb, P.M * kb, P.batch, ws + P.off_sfa, s);
-    if (e == cudaSuccess)
-        e = launch_repack_scales_batched(sb, P.N, P.K, kb, P.N * kb, P.batch, ws + P.off_sfb, s);
-    if (e != cudaSuccess) return MX_ERR_CUDA;
     GemmArgs g{};
-    g.a = a;
-    g.bt = bt;
     g.sfa = ws + P.off_sfa;
     g.sfb = ws + P.off_sfb;
     g.M = P.M;
@@ -646,6 +633,40 @@ mx_status mx_block_scaled_dot(const void* lhs, const int64_t* lhs_dims, int lhs_
     g.a_batch_stride = P.M * elem_bytes(elem_dtype, P.K);
     g.b_batch_stride = P.N * elem_bytes(elem_dtype, P.K);
     g.c_batch_stride = P.M * P.N;
+    // An FP8 operand stored [batch, K, rows] is read in place, MN-major, when
+    // the pair kernel takes the product and its rows are whole 16-byte
+    // multiples; otherwise it is copied into [batch, rows, K] first.
+    const bool pair = !fp4 && scaled_matmul_takes_pair(g);
+    g.a_mn_major = pair && P.lmn && P.M % 16 == 0 && aligned16(lhs);
+    g.b_mn_major = pair && P.rmn && P.N % 16 == 0 && aligned16(rhs);
+    const uint8_t* a = static_cast<const uint8_t*>(lhs);
+    const uint8_t* sa = static_cast<const uint8_t*>(lhs_scale);
+    const uint8_t* bt = static_cast<const uint8_t*>(rhs);
+    const uint8_t* sb = static_cast<const uint8_t*>(rhs_scale);
+    cudaError_t e = cudaSuccess;
+    const int64_t code_div = fp4 ? 2 : 1;  // elements per byte along the contracting axis
+    if (!P.lcanon && !g.a_mn_major) {
+        e = permute_operand(lhs, lhs_dims, lhs_rank, P.lperm, P.lc, code_div, ws + P.off_lq, s);
+        if (e == cudaSuccess) e = permute_operand(lhs_scale, lhs_dims, lhs_rank, P.lperm, P.lc, 32, ws + P.off_ls, s);
+        a = ws + P.off_lq;
+        sa = ws + P.off_ls;
+    }
+    if (e == cudaSuccess && !P.rcanon && !g.b_mn_major) {
+        e = permute_operand(rhs, rhs_dims, rhs_rank, P.rperm, P.rc, code_div, ws + P.off_rq, s);
+        if (e == cudaSuccess) e = permute_operand(rhs_scale, rhs_dims, rhs_rank, P.rperm, P.rc, 32, ws + P.off_rs, s);
+        bt = ws + P.off_rq;
+        sb = ws + P.off_rs;
+    }
+    const int64_t kb = P.K / 32;
+    if (e == cudaSuccess)
+        e = g.a_mn_major ? launch_repack_scales_mn_inner(sa, P.M, P.K, P.M, P.M * kb, P.batch, ws + P.off_sfa, s)
+                         : launch_repack_scales_batched(sa, P.M, P.K, kb, P.M * kb, P.batch, ws + P.off_sfa, s);
+    if (e == cudaSuccess)
+        e = g.b_mn_major ? launch_repack_scales_mn_inner(sb, P.N, P.K, P.N, P.N * kb, P.batch, ws + P.off_sfb, s)
+                         : launch_repack_scales_batched(sb, P.N, P.K, kb, P.N * kb, P.batch, ws + P.off_sfb, s);
+    if (e != cudaSuccess) return MX_ERR_CUDA;
+    g.a = a;
+    g.bt = bt;
     return from_cuda(launch_scaled_matmul(g, s));
 }
 
@@ -691,6 +712,14 @@ mx_status mx_debug_last_gemm_launch(int* kernel, int* split_k) {
     const GemmLaunchInfo info = last_gemm_launch();
     *kernel = info.kernel;
     *split_k = info.split_k;
+    return MX_OK;
+}
+
+mx_status mx_debug_last_gemm_operands(int* a_mn_major, int* b_mn_major) {
+    if (!a_mn_major || !b_mn_major) return MX_ERR_INVALID_ARG;
+    const GemmLaunchInfo info = last_gemm_launch();
+    *a_mn_major = info.a_mn_major;
+    *b_mn_major = info.b_mn_major;
     return MX_OK;
 }
 

@@ -62,6 +62,10 @@ cudaError_t launch_repack_scales(const uint8_t* plain, int64_t mn, int64_t k, in
 cudaError_t launch_repack_scales_batched(const uint8_t* plain, int64_t mn, int64_t k, int64_t ld_plain,
                                          int64_t plain_batch_stride, int64_t batch, uint8_t* sf,
                                          cudaStream_t stream);
+// The same from scales stored [k/32, mn] (mn innermost, rows ld_plain bytes).
+cudaError_t launch_repack_scales_mn_inner(const uint8_t* plain, int64_t mn, int64_t k, int64_t ld_plain,
+                                          int64_t plain_batch_stride, int64_t batch, uint8_t* sf,
+                                          cudaStream_t stream);
 
 // Byte-tensor permutation: dst (dense, `rank` axes of extents dst_dims,
 // outermost first) takes dst[i_0, .., i_{r-1}] = src[sum_a i_a * src_stride[a]].
@@ -101,8 +105,14 @@ struct GemmArgs {
     int64_t ld_x_bytes;
     int32_t x_f16;
     uint64_t* q_flags;
+    // FP8, not fused: A stored [batch, K, M] / Bt stored [batch, K, N] (M / N
+    // innermost, rows M / N bytes, a multiple of 16; the batch strides still
+    // count the whole problem); read MN-major by the pair kernel.
+    int32_t a_mn_major, b_mn_major;
 };
 cudaError_t launch_scaled_matmul(const GemmArgs& g, cudaStream_t stream);
+// Whether launch_scaled_matmul runs `g` (its K-major form) on the pair kernel.
+bool scaled_matmul_takes_pair(const GemmArgs& g);
 // Whether the fused call runs as one launch of the pair kernel (else
 // QuantizeMX, then launch_scaled_matmul), and that launch.
 bool fused_single_launch(const GemmArgs& g);
@@ -113,6 +123,7 @@ struct GemmLaunchInfo {
     int kernel;   // 1: 1-SM kernel, 2: 2-SM pair kernel, 3: pair kernel with the
                   // fused activation quantize, 0: none yet
     int split_k;  // CTAs per tile along K (1-SM kernel), else 1
+    int a_mn_major, b_mn_major;  // operands read MN-major
 };
 GemmLaunchInfo last_gemm_launch();
 

@@ -13,9 +13,12 @@
 // rows' contiguous 64-byte segments (16-byte loads where aligned) into shared
 // memory and writes the 16 tiles, which are contiguous in the output, with
 // 16-byte stores.  A batch of problems is one launch: their SF layouts are
-// written back to back.
+// written back to back.  Scales stored the other way round, [k/32, mn] with
+// mn innermost (the scales of an operand stored [K, MN]), are read as 128-row
+// segments per scale column and transposed through the same shared tile.
 
 #include <cstdint>
+#include <cstring>
 
 #include "mx_internal.h"
 #include "pdl.cuh"
@@ -30,7 +33,8 @@ constexpr int kCols = 4 * kTilesPerBlock;
 __global__ void __launch_bounds__(kRepackThreads) repack_sf_kernel(const uint8_t* __restrict__ plain, int64_t mn,
                                                                   int64_t kb, int64_t ld, int64_t ntm, int64_t ntk,
                                                                   int64_t plain_batch_stride, int64_t batch,
-                                                                  uint8_t* __restrict__ sf, int vec_ok) {
+                                                                  uint8_t* __restrict__ sf, int vec_ok,
+                                                                  int mn_inner) {
     dev::pdl_allow_next();
     dev::pdl_wait_prior();
     __shared__ __align__(16) uint8_t rows[128][kCols + 16];
@@ -48,6 +52,21 @@ __global__ void __launch_bounds__(kRepackThreads) repack_sf_kernel(const uint8_t
                                                : kTilesPerBlock);
         __syncthreads();  // the previous unit's reads of `rows` are done
         // rows tm*128 .. +127, columns c0 .. c0+63 (0 past the matrix)
+        if (mn_inner) {
+            // scale (r, c) at src[c * ld + r]: 16 rows of one column per step
+            for (int i = threadIdx.x; i < kCols * 8; i += kRepackThreads) {
+                const int cc = i >> 3, seg = i & 7;
+                const int64_t c = c0 + cc, r = tm * 128 + 16 * seg;
+                uint8_t v[16];
+                if (c < kb && vec_ok && r + 16 <= mn) {
+                    const uint4 w = *reinterpret_cast<const uint4*>(src + c * ld + r);
+                    memcpy(v, &w, 16);
+                } else {
+                    for (int j = 0; j < 16; ++j) v[j] = (c < kb && r + j < mn) ? src[c * ld + r + j] : uint8_t(0);
+                }
+                for (int j = 0; j < 16; ++j) rows[16 * seg + j][cc] = v[j];
+            }
+        } else
         for (int i = threadIdx.x; i < 128 * (kCols / 16); i += kRepackThreads) {
             const int rr = i / (kCols / 16), seg = i % (kCols / 16);
             const int64_t r = tm * 128 + rr, c = c0 + 16 * seg;
@@ -94,7 +113,23 @@ cudaError_t launch_repack_scales_batched(const uint8_t* plain, int64_t mn, int64
     const int vec_ok = (reinterpret_cast<uintptr_t>(plain) & 15u) == 0 && ld_plain % 16 == 0 &&
                        plain_batch_stride % 16 == 0;
     return launch_pdl(repack_sf_kernel, static_cast<unsigned>(blocks), kRepackThreads, 0, stream, plain, mn, kb,
-                      ld_plain, ntm, ntk, plain_batch_stride, batch, sf, vec_ok);
+                      ld_plain, ntm, ntk, plain_batch_stride, batch, sf, vec_ok, 0);
+}
+
+cudaError_t launch_repack_scales_mn_inner(const uint8_t* plain, int64_t mn, int64_t k, int64_t ld_plain,
+                                          int64_t plain_batch_stride, int64_t batch, uint8_t* sf,
+                                          cudaStream_t stream) {
+    const int64_t kb = k / 32;
+    const int64_t ntm = (mn + 127) / 128;
+    const int64_t ntk = (kb + 3) / 4;
+    if (ntm == 0 || ntk == 0 || batch == 0) return cudaSuccess;
+    const int64_t units = batch * ntm * ((ntk + kTilesPerBlock - 1) / kTilesPerBlock);
+    const int64_t cap = static_cast<int64_t>(device_sm_count()) * 8;
+    const int64_t blocks = units < cap ? units : cap;
+    const int vec_ok = (reinterpret_cast<uintptr_t>(plain) & 15u) == 0 && ld_plain % 16 == 0 &&
+                       plain_batch_stride % 16 == 0;
+    return launch_pdl(repack_sf_kernel, static_cast<unsigned>(blocks), kRepackThreads, 0, stream, plain, mn, kb,
+                      ld_plain, ntm, ntk, plain_batch_stride, batch, sf, vec_ok, 1);
 }
 
 cudaError_t launch_repack_scales(const uint8_t* plain, int64_t mn, int64_t k, int64_t ld_plain,

@@ -430,6 +430,20 @@ __device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t saddr) {
            (static_cast<uint64_t>(2) << 61);
 }
 
+// Shared-memory matrix descriptor, MN-major 8-bit operand tile: TMA wrote
+// rows of 128 bytes along M (or N), one row per K index, with the 128-byte
+// swizzle, so the tile is a single swizzle atom wide along MN (128
+// elements) and its 8-row K groups are 1024 bytes apart (SBO).  The leading
+// byte offset steps between atoms along MN; with one atom per tile no MMA
+// uses it, and it is set equal to the SBO so that no reading of the two
+// fields reaches outside the tile.  A K offset of k rows adds k * 128 bytes
+// to the start address (multiples of 32 rows keep it 1024-byte aligned).
+__device__ __forceinline__ uint64_t sdesc_mnmajor_sw128(uint32_t saddr) {
+    return static_cast<uint64_t>((saddr >> 4) & 0x3FFFu) | (static_cast<uint64_t>(1024 >> 4) << 16) |
+           (static_cast<uint64_t>(1024 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) |
+           (static_cast<uint64_t>(2) << 61);
+}
+
 // Descriptor of a 512-byte scale-factor tile (32 rows x 16 bytes, no swizzle,
 // 8-row groups 128 bytes apart) as the source of tcgen05.cp.32x128b.
 __device__ __forceinline__ uint64_t sdesc_sf_tile(uint32_t saddr) {
@@ -443,7 +457,10 @@ __device__ __forceinline__ uint64_t sdesc_sf_tile(uint32_t saddr) {
 // A/B formats (0 = E4M3, 1 = E5M2) at bits 7..9 / 10..12, both K-major,
 // N >> 3 at bits 17..22, scale type UE8M0 (bit 23 = 1), M >> 4 at bits 24..28.
 // The scale-factor byte selectors (bits 4..5 for B, 29..30 for A) are OR-ed in
-// per MMA.
+// per MMA, and so are the operands' major bits (kIdescAMnMajor /
+// kIdescBMnMajor) for MN-major 8-bit tiles.
+constexpr uint32_t kIdescAMnMajor = 1u << 15;  // A tile MN-major (the "transpose A" bit)
+constexpr uint32_t kIdescBMnMajor = 1u << 16;  // B tile MN-major
 __host__ __device__ constexpr uint32_t make_idesc_mxf8(int a_fmt, int b_fmt, int m, int n) {
     return (static_cast<uint32_t>(a_fmt) << 7) | (static_cast<uint32_t>(b_fmt) << 10) |
            (static_cast<uint32_t>(n >> 3) << 17) | (1u << 23) | (static_cast<uint32_t>(m >> 4) << 24);

@@ -300,3 +300,7 @@ def test_debug_hooks_check_arguments(mx, lib):
     assert lib.mx_debug_last_gemm_launch(ctypes.byref(one), None) == mx.MX_ERR_INVALID_ARG
     kernel, split = mx.mx_debug_last_gemm_launch()
     assert kernel in (0, 1, 2, 3) and split >= (1 if kernel else 0)
+    assert lib.mx_debug_last_gemm_operands(None, ctypes.byref(one)) == mx.MX_ERR_INVALID_ARG
+    assert lib.mx_debug_last_gemm_operands(ctypes.byref(one), None) == mx.MX_ERR_INVALID_ARG
+    a_mn, b_mn = mx.mx_debug_last_gemm_operands()
+    assert a_mn in (0, 1) and b_mn in (0, 1)

@@ -134,3 +134,122 @@ def test_large_batched_sampled(mx):
         check_gemm(got[bb][rows], C, S, "bf16")
         C, S = orc.scaled_matmul(a[bb], bt, sa[bb], sbt, "e4m3fn", cols=cols)
         check_gemm(got[bb][:, cols], C, S, "bf16")
+
+
+# ---------------------------------------------------------------- MN-major operands
+#
+# An FP8 operand stored [batch, K, rows] (the contracting axis before the free
+# axes) is read in place by the pair kernel as MN-major tiles, with no
+# transposing copy, when its rows are a multiple of 16 bytes.  Each case runs
+# under the forced pair kernel (small shapes) or automatic choice (large
+# ones), checks which operands were read in place, and compares every element
+# with the oracle.
+
+def run_major(mx, lshape, rshape, lb, rb, lc, rc, fmt, out_dtype, seed, variant=2):
+    import torch
+    rng = np.random.default_rng(seed)
+    lhs, ls = operand(rng, lshape, lc, fmt)
+    rhs, rs = operand(rng, rshape, rc, fmt)
+    want, s = orc.block_scaled_dot(lhs, rhs, ls, rs, fmt, lhs_batch=lb, rhs_batch=rb, lhs_contract=(lc,),
+                                   rhs_contract=(rc,))
+    mx.mx_debug_set_gemm_variant(variant)
+    try:
+        got = mx.mx_block_scaled_dot(to_device_u8(lhs), to_device_u8(rhs), to_device_u8(ls), to_device_u8(rs), fmt,
+                                     out_dtype, lhs_batch=lb, rhs_batch=rb, lhs_contract=(lc,), rhs_contract=(rc,))
+        torch.cuda.synchronize()
+    finally:
+        mx.mx_debug_set_gemm_variant(0)
+    check_gemm(got.float().cpu().numpy(), want, s, out_dtype)
+    return got, mx.mx_debug_last_gemm_launch(), mx.mx_debug_last_gemm_operands()
+
+
+MAJOR_CASES = {
+    # name: (lhs shape, rhs shape, lb, rb, lc, rc, expected (a_mn, b_mn))
+    "rhs_kn": ((2, 256, 512), (2, 512, 384), (0,), (0,), 2, 1, (0, 1)),
+    # N = 208 = 128 + 80 and K = 160 = 128 + 32: both edges of the MN-major
+    # tile read zeros past the operand
+    "rhs_kn_ragged": ((2, 200, 160), (2, 160, 208), (0,), (0,), 2, 1, (0, 1)),
+    "rhs_kn_short_k": ((1, 300, 96), (1, 96, 48), (0,), (0,), 2, 1, (0, 1)),
+    "lhs_km": ((3, 512, 272), (3, 136, 512), (0,), (0,), 1, 2, (1, 0)),
+    "both_mn": ((2, 384, 400), (2, 384, 144), (0,), (0,), 1, 1, (1, 1)),
+    "no_batch_both_mn": ((288, 336), (288, 528), (), (), 0, 0, (1, 1)),
+    "two_batch_dims_both_mn": ((2, 3, 256, 160), (2, 3, 256, 96), (0, 1), (0, 1), 2, 2, (1, 1)),
+    "two_batch_dims_rhs_kn": ((2, 3, 160, 256), (2, 3, 256, 96), (0, 1), (0, 1), 3, 2, (0, 1)),
+    "two_free_dims_rhs_kn": ((2, 160, 256), (2, 256, 3, 32), (0,), (0,), 2, 1, (0, 1)),
+    # rows not a multiple of 16 bytes: copied into [batch, rows, K] instead
+    "rhs_kn_odd_rows": ((2, 256, 256), (2, 256, 200), (0,), (0,), 2, 1, (0, 0)),
+    "rhs_kn_rows_8": ((2, 256, 256), (2, 256, 8), (0,), (0,), 2, 1, (0, 0)),
+}
+
+
+@pytest.mark.parametrize("out_dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("fmt", ["e4m3fn", "e5m2"])
+@pytest.mark.parametrize("name", sorted(MAJOR_CASES))
+def test_mn_major_operands_match_oracle(mx, name, fmt, out_dtype):
+    lshape, rshape, lb, rb, lc, rc, majors = MAJOR_CASES[name]
+    _, launch, got_majors = run_major(mx, lshape, rshape, lb, rb, lc, rc, fmt, out_dtype,
+                                      seed=100 + sorted(MAJOR_CASES).index(name))
+    assert launch[0] == 2
+    assert got_majors == majors
+
+
+def test_mn_major_equals_copied_operand_bitwise(mx):
+    # the same products from the same codes and scales: reading [B, K, N] in
+    # place gives the bits of the [B, N, K] copy
+    import torch
+    rng = np.random.default_rng(41)
+    B, M, N, K = 3, 384, 272, 640
+    a, sa = operand(rng, (B, M, K), 2, "e4m3fn")
+    b_kn, sb_kn = operand(rng, (B, K, N), 1, "e4m3fn")
+    b_nk = np.ascontiguousarray(b_kn.transpose(0, 2, 1))
+    sb_nk = np.ascontiguousarray(sb_kn.transpose(0, 2, 1))
+    mx.mx_debug_set_gemm_variant(2)
+    try:
+        in_place = mx.mx_block_scaled_dot(to_device_u8(a), to_device_u8(b_kn), to_device_u8(sa), to_device_u8(sb_kn),
+                                          "e4m3fn", "f32", lhs_batch=(0,), rhs_batch=(0,), rhs_contract=(1,))
+        assert mx.mx_debug_last_gemm_operands() == (0, 1)
+        copied = mx.mx_block_scaled_dot(to_device_u8(a), to_device_u8(b_nk), to_device_u8(sa), to_device_u8(sb_nk),
+                                        "e4m3fn", "f32", lhs_batch=(0,), rhs_batch=(0,))
+        assert mx.mx_debug_last_gemm_operands() == (0, 0)
+        torch.cuda.synchronize()
+    finally:
+        mx.mx_debug_set_gemm_variant(0)
+    assert torch.equal(in_place.view(torch.int32), copied.view(torch.int32))
+
+
+def test_mn_major_not_used_by_the_one_sm_kernel(mx):
+    # M <= 128 runs on the 1-SM kernel, which reads K-major rows only: the
+    # [B, K, N] operand is copied, and the result still matches the oracle
+    _, launch, majors = run_major(mx, (2, 64, 256), (2, 256, 512), (0,), (0,), 2, 1, "e4m3fn", "bf16", seed=7,
+                                  variant=0)
+    assert launch[0] == 1
+    assert majors == (0, 0)
+
+
+def test_mn_major_full_tiles_sampled(mx):
+    # 8 x 1024^3 with rhs [B, K, N] and lhs [B, K, M]: enough 256 x 256 tiles
+    # for whole rounds (no split tail) on the automatic choice; sampled rows
+    # and columns of three problems against the oracle
+    import torch
+    rng = np.random.default_rng(19)
+    B, M, N, K = 8, 1024, 1024, 1024
+    a_km, sa_km = operand(rng, (B, K, M), 1, "e4m3fn")
+    b_kn, sb_kn = operand(rng, (B, K, N), 1, "e4m3fn")
+    got = mx.mx_block_scaled_dot(to_device_u8(a_km), to_device_u8(b_kn), to_device_u8(sa_km), to_device_u8(sb_kn),
+                                 "e4m3fn", "bf16", lhs_batch=(0,), rhs_batch=(0,), lhs_contract=(1,),
+                                 rhs_contract=(1,))
+    torch.cuda.synchronize()
+    assert mx.mx_debug_last_gemm_launch()[0] == 2
+    assert mx.mx_debug_last_gemm_operands() == (1, 1)
+    got = got.float().cpu().numpy()
+    rows = np.unique(np.concatenate([[0, 127, 128, 255, 256, M - 1], rng.choice(M, 18, replace=False)]))
+    cols = np.unique(np.concatenate([[0, 127, 128, 255, 256, N - 1], rng.choice(N, 18, replace=False)]))
+    for bb in (0, 5, 7):
+        a = np.ascontiguousarray(a_km[bb].T)
+        sa = np.ascontiguousarray(sa_km[bb].T)
+        bt = np.ascontiguousarray(b_kn[bb].T)
+        sbt = np.ascontiguousarray(sb_kn[bb].T)
+        C, S = orc.scaled_matmul(a, bt, sa, sbt, "e4m3fn", rows=rows)
+        check_gemm(got[bb][rows], C, S, "bf16")
+        C, S = orc.scaled_matmul(a, bt, sa, sbt, "e4m3fn", cols=cols)
+        check_gemm(got[bb][:, cols], C, S, "bf16")
