@@ -82,6 +82,24 @@ def test_matmul_split_tail_round(mx, out_dtype, M, N, K):
     check_gemm(c, c_ref, s_ref, out_dtype, TOL)
 
 
+@pytest.mark.parametrize("out_dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("M,N,K", [(4096, 4096, 128), (4096, 8192, 256)])
+def test_matmul_accumulator_handoff_many_short_tiles(mx, out_dtype, M, N, K):
+    """Many pair tiles per cluster (3.5 and 7) of one or two K stages, so
+    rank 0's stores are not paced and the accumulator changes hands every
+    few microseconds: an MMA that overwrote the accumulator before rank 1's
+    epilogue had read it would show in some tile.  Every element against
+    the oracle."""
+    mx.mx_debug_set_gemm_variant(2)
+    try:
+        a, bt, sa, sb = _random_operands(M, N, K, "e4m3fn", seed=M + N + K + 1)
+        c = _gpu_matmul(mx, a, bt, sa, sb, "e4m3fn", out_dtype)
+    finally:
+        mx.mx_debug_set_gemm_variant(0)
+    c_ref, s_ref = orc.scaled_matmul(a, bt, sa, sb, "e4m3fn")
+    check_gemm(c, c_ref, s_ref, out_dtype, TOL)
+
+
 @pytest.mark.parametrize("fmt", ["e4m3fn", "e5m2"])
 def test_matmul_sf_layout_scales(mx, variant, fmt):
     M, N, K = 256, 512, 384
