@@ -1008,11 +1008,11 @@ constexpr int kPaceNum = 1, kPaceDen = 2, kPaceMinStages = 16;
 
 // Scale-factor buffers are read by TMA as [2 * tiles, 256] bytes: a 512-byte
 // tile t is rows 2t and 2t+1; one box is a scale group's consecutive tiles;
-// tiles past the end read as zeros.  MN: the instantiation that may read A
-// and / or B as MN-major tiles (KParams::a_mn / b_mn); the others read
-// K-major rows only and carry no per-MMA test of the operands' layout (the
-// MMA-issuing thread is on the critical path: that test cost 2 % at 8192^3).
-template <bool FP4, int QFMT, bool MN = false>
+// tiles past the end read as zeros.  MN: which operands this instantiation
+// reads as MN-major tiles (bit 0: B, bit 1: A; 0 = both K-major), fixed at
+// compile time: the MMA-issuing thread is on the critical path, and a
+// runtime test of the operands' layout per MMA cost 2 % at 8192^3.
+template <bool FP4, int QFMT, int MN = 0>
 __global__ void __launch_bounds__(sm2::threads(QFMT >= 0), 1)
     mx_gemm_2sm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                        const __grid_constant__ CUtensorMap tmap_sfa, const __grid_constant__ CUtensorMap tmap_sfb,
@@ -1025,7 +1025,7 @@ __global__ void __launch_bounds__(sm2::threads(QFMT >= 0), 1)
     constexpr int SF_TILES_PER_STAGE = FP4 ? 2 : 1;
     constexpr int SF_GROUP = sf_group(FP4), SF_SLOTS = sf_slots(FP4);
     constexpr bool FUSED = QFMT >= 0;  // quantize X into the A operand inside this launch
-    const bool a_mn = MN && p.a_mn, b_mn = MN && p.b_mn;
+    constexpr bool a_mn = (MN & 2) != 0, b_mn = (MN & 1) != 0;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sb = smem_u32(smem);
@@ -1184,11 +1184,11 @@ __global__ void __launch_bounds__(sm2::threads(QFMT >= 0), 1)
                         }
                     }
                     // K-major tiles: (K bytes, rows); MN-major: (rows, K rows)
-                    if (a_mn)
+                    if constexpr (a_mn)
                         tma_load_3d_pair(sb + OFF_A + stage * A_STAGE, &tmap_a, fb, a_row, kb * BK, b);
                     else
                         tma_load_3d_pair(sb + OFF_A + stage * A_STAGE, &tmap_a, fb, kb * BK, a_row, b);
-                    if (b_mn)
+                    if constexpr (b_mn)
                         tma_load_3d_pair(sb + OFF_B + stage * B_STAGE, &tmap_b, fb, b_row, kb * BK, b);
                     else
                         tma_load_3d_pair(sb + OFF_B + stage * B_STAGE, &tmap_b, fb, kb * BK, b_row, b);
@@ -1631,7 +1631,7 @@ cudaError_t ensure_1sm_attr() {
     static bool done[64] = {};
     return ensure_smem_attr(mx_gemm_kernel<FP4>, sm1::smem_alloc(FP4), mu, done);
 }
-template <bool FP4, int QFMT, bool MN = false>
+template <bool FP4, int QFMT, int MN = 0>
 cudaError_t ensure_2sm_attr() {
     static std::mutex mu;
     static bool done[64] = {};
@@ -1773,14 +1773,15 @@ uint64_t next_tag() {
 
 int g_fused_lookahead = 1;
 
-template <bool FP4, int QFMT, bool MN = false>
+template <bool FP4, int QFMT, int MN = 0>
 cudaError_t launch_2sm(const GemmArgs& g, cudaStream_t stream) {
     const cudaError_t attr_err = ensure_2sm_attr<FP4, QFMT, MN>();
     if (attr_err != cudaSuccess) return attr_err;
     CUtensorMap ma, mb, msa, msb;
     const int64_t sfa_tiles = g.batch * ((g.M + 127) / 128) * ((g.K + 127) / 128);
     const int64_t sfb_tiles = g.batch * ((g.N + 127) / 128) * ((g.K + 127) / 128);
-    if ((FP4 || QFMT >= 0 || !MN) && (g.a_mn_major || g.b_mn_major)) return cudaErrorInvalidValue;
+    if ((g.a_mn_major ? 2 : 0) + (g.b_mn_major ? 1 : 0) != MN || (MN && (FP4 || QFMT >= 0)))
+        return cudaErrorInvalidValue;
     const bool map_a = g.a_mn_major ? make_operand_map_mn(&ma, g.a, g.M, g.K, g.batch, g.a_batch_stride)
                                     : make_operand_map(&ma, g.a, g.M, row_bytes(g), 128, g.batch, g.a_batch_stride);
     const bool map_b = g.b_mn_major ? make_operand_map_mn(&mb, g.bt, g.N, g.K, g.batch, g.b_batch_stride)
@@ -1870,7 +1871,9 @@ cudaError_t launch_scaled_matmul(const GemmArgs& g, cudaStream_t stream) {
     const bool pair = g.a_mn_major || g.b_mn_major || scaled_matmul_takes_pair(g);
     const bool split = g_variant != 3;
     if (fp4) return pair ? launch_2sm<true, -1>(g, stream) : launch_1sm<true>(g, stream, split);
-    if (g.a_mn_major || g.b_mn_major) return launch_2sm<false, -1, true>(g, stream);
+    if (g.a_mn_major && g.b_mn_major) return launch_2sm<false, -1, 3>(g, stream);
+    if (g.a_mn_major) return launch_2sm<false, -1, 2>(g, stream);
+    if (g.b_mn_major) return launch_2sm<false, -1, 1>(g, stream);
     return pair ? launch_2sm<false, -1>(g, stream) : launch_1sm<false>(g, stream, split);
 }
 
