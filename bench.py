@@ -735,8 +735,7 @@ def vendor_fp4_reference(torch, g, steps):
                 if it >= 3:
                     times[which].append(e0.elapsed_time(e1))
         out = {k: round(GEMM_FLOP / (statistics.median(v) * 1e-3) / 1e12, 1) for k, v in times.items()}
-        return {"tflops": out, "what": "8192^3 -> bf16 on the same packed e2m1 operands; cuBLASLt runs NVFP4 "
-                                      "(1x16 blocks, e4m3 scales: the only block-scaled FP4 form torch exposes)"}
+        return {"tflops": out, "what": "same packed e2m1 codes; cuBLASLt runs NVFP4 (1x16, e4m3 scales)"}
     except Exception as e:
         return {"unavailable": f"{type(e).__name__}: {str(e)[:160]}"}
 
@@ -1204,8 +1203,8 @@ def main():
     # only the end of the line still see them)
     order = ["metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better", "scaling",
              "vs_baseline", "dtype", "data", "gpu_launches", "config", "roofline", "clocks", "e2e", "cpu_baseline",
-             "scaled_matmul_small_m", "block_scaled_dot", "pipeline_256", "scaled_matmul_vendor", "dequantize",
-             "scaled_matmul_fp4", "fp4_quantize", "fused", "scaled_matmul"]
+             "scaled_matmul_small_m", "block_scaled_dot", "pipeline_256", "scaled_matmul_fp4", "scaled_matmul_vendor",
+             "dequantize", "fp4_quantize", "fused", "scaled_matmul"]
     line = {k: line[k] for k in order if k in line} | {k: v for k, v in line.items() if k not in order}
     if rank == 0:
         print(json.dumps(line), flush=True)
