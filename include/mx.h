@@ -488,9 +488,9 @@ mx_status mx_debug_last_gemm_launch(int* kernel, int* split_k);
  * launch read A (*a_mn_major) and B (*b_mn_major) in place as MN-major tiles
  * (1) or as K-major rows (0).  mx_block_scaled_dot reads an FP8 operand
  * stored [batch..., K, rows...] (batch axes in order, then the contracting
- * axis, then the free axes) in place when the pair kernel takes the product
- * and the operand's rows are a multiple of 16 bytes on a 16-byte aligned
- * base; otherwise it copies the operand into [batch, rows, K] first.
+ * axis, then the free axes) in place when the operand's rows are a
+ * multiple of 16 bytes on a 16-byte aligned base (either GEMM kernel);
+ * otherwise it copies the operand into [batch, rows, K] first.
  * MX_ERR_INVALID_ARG if a pointer is NULL.  Host only.
  */
 mx_status mx_debug_last_gemm_operands(int* a_mn_major, int* b_mn_major);

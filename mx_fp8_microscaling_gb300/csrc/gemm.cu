@@ -675,11 +675,19 @@ constexpr int SF_WARP = 10;              // warp that copies scale factors to te
 constexpr int THREADS = NUM_THREADS + 32;
 }  // namespace sm1
 
-template <bool FP4>
+// MN: operands read as MN-major tiles (bit 0: B, bit 1: A; FP8 only).  An
+// MN-major B stage is two 128-row atom columns 16 KB apart (two TMA boxes);
+// its B stages then come first in shared memory, so that every address its
+// descriptors can name stays inside the CTA's allocation.
+template <bool FP4, int MN = 0>
 __global__ void __launch_bounds__(sm1::THREADS, 1)
     mx_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                    const KParams p) {
     using namespace sm1;
+    constexpr bool a_mn = (MN & 2) != 0, b_mn = (MN & 1) != 0;
+    constexpr uint32_t S_OFF_A = b_mn ? STAGES * B_STAGE : OFF_A;  // operand stages
+    constexpr uint32_t S_OFF_B = b_mn ? 0u : OFF_B;
+    constexpr uint32_t OFF_PARTIAL = 0;  // split-K partials reuse the drained operand stages
     constexpr uint32_t SFA_STAGE = sfa_stage(FP4), SFB_STAGE = sfb_stage(FP4);
     constexpr uint32_t OFF_SFB = off_sfb(FP4), OFF_BAR = off_bar(FP4), OFF_MISC = off_misc(FP4);
     constexpr uint32_t SF_COLS = sf_cols(FP4);
@@ -749,8 +757,18 @@ __global__ void __launch_bounds__(sm1::THREADS, 1)
                     const int t0 = FP4 ? 2 * kb : kb;
                     const uint32_t sf_bytes = (FP4 && t0 + 1 < p.sf_ntk) ? 1024u : 512u;
                     mbar_arrive_expect_tx(fb, A_STAGE + B_STAGE + 3u * sf_bytes);
-                    tma_load_3d(sb + OFF_A + stage * A_STAGE, &tmap_a, fb, kb * BK, mt * BM, b);
-                    tma_load_3d(sb + OFF_B + stage * B_STAGE, &tmap_b, fb, kb * BK, nt * BN, b);
+                    // K-major tiles: (K bytes, rows); MN-major: (rows, K rows)
+                    if constexpr (a_mn)
+                        tma_load_3d(sb + S_OFF_A + stage * A_STAGE, &tmap_a, fb, mt * BM, kb * BK, b);
+                    else
+                        tma_load_3d(sb + S_OFF_A + stage * A_STAGE, &tmap_a, fb, kb * BK, mt * BM, b);
+                    if constexpr (b_mn) {
+                        tma_load_3d(sb + S_OFF_B + stage * B_STAGE, &tmap_b, fb, nt * BN, kb * BK, b);
+                        tma_load_3d(sb + S_OFF_B + stage * B_STAGE + B_STAGE / 2, &tmap_b, fb, nt * BN + 128, kb * BK,
+                                    b);
+                    } else {
+                        tma_load_3d(sb + S_OFF_B + stage * B_STAGE, &tmap_b, fb, kb * BK, nt * BN, b);
+                    }
                     bulk_load(sb + OFF_SFA + stage * SFA_STAGE,
                               sfa + (static_cast<size_t>(mt) * p.sf_ntk + t0) * 512u, sf_bytes, fb);
                     bulk_load(sb + OFF_SFB + stage * SFB_STAGE,
@@ -791,8 +809,8 @@ __global__ void __launch_bounds__(sm1::THREADS, 1)
                     }
                     tc_fence_after();
                     const uint32_t sf_t = tmem_base + TMEM_SF + SF_COLS * stage;
-                    const uint32_t sa = sb + OFF_A + stage * A_STAGE;
-                    const uint32_t sbb = sb + OFF_B + stage * B_STAGE;
+                    const uint32_t sa = sb + S_OFF_A + stage * A_STAGE;
+                    const uint32_t sbb = sb + S_OFF_B + stage * B_STAGE;
                     if constexpr (FP4) {
                         // 4 MMAs of K = 64; K group g = kk / 2 has its own scale
                         // columns, bytes {0,1} / {2,3} of them by scale data ID
@@ -810,9 +828,13 @@ __global__ void __launch_bounds__(sm1::THREADS, 1)
                         for (int kk = 0; kk < BK / 32; ++kk) {
                             const uint32_t idesc = p.idesc | (static_cast<uint32_t>(kk) << 4) |
                                                    (static_cast<uint32_t>(kk) << 29);
-                            tc_mma_mxf8(tmem_base, sdesc_kmajor_sw128(sa + kk * 32),
-                                        sdesc_kmajor_sw128(sbb + kk * 32), idesc, sf_t, sf_t + 4u,
-                                        !first_kb || kk != 0);
+                            // 32 K elements: 32 bytes into a K-major row, 32
+                            // rows of 128 bytes into an MN-major atom column
+                            const uint64_t da = a_mn ? sdesc_mnmajor_sw128(sa + kk * 32 * 128)
+                                                     : sdesc_kmajor_sw128(sa + kk * 32);
+                            const uint64_t db = b_mn ? sdesc_mnmajor_sw128(sbb + kk * 32 * 128, B_STAGE / 2)
+                                                     : sdesc_kmajor_sw128(sbb + kk * 32);
+                            tc_mma_mxf8(tmem_base, da, db, idesc, sf_t, sf_t + 4u, !first_kb || kk != 0);
                         }
                     }
                     tc_commit(empty_bar(stage));
@@ -909,7 +931,7 @@ __global__ void __launch_bounds__(sm1::THREADS, 1)
 #pragma unroll
                     for (int c = 0; c < 32; ++c) {
                         const uint32_t* x = &v[c >> 3][4 * (c & 7)];
-                        st_shared_v4(sb + OFF_A + partial_off(row, half * 32 + c), x[0], x[1], x[2], x[3]);
+                        st_shared_v4(sb + OFF_PARTIAL + partial_off(row, half * 32 + c), x[0], x[1], x[2], x[3]);
                     }
                 }
             } else {
@@ -935,7 +957,7 @@ __global__ void __launch_bounds__(sm1::THREADS, 1)
         const int e_end = (s + 1) * total / S;
         for (int e = s * total / S + static_cast<int>(threadIdx.x); e < e_end; e += blockDim.x) {
             const int r = e / chunks, j = e - r * chunks;
-            const float4* own = reinterpret_cast<const float4*>(generic_shared(sb + OFF_A + partial_off(r, j)));
+            const float4* own = reinterpret_cast<const float4*>(generic_shared(sb + OFF_PARTIAL + partial_off(r, j)));
             float4 acc = *map_cluster(own, 0);
             // CTA q's partial, through the cluster window, 4 loads in flight
 #pragma unroll
@@ -1625,11 +1647,11 @@ cudaError_t ensure_smem_attr(Kernel kernel, uint32_t bytes, std::mutex& mu, bool
     }
     return cudaSuccess;
 }
-template <bool FP4>
+template <bool FP4, int MN = 0>
 cudaError_t ensure_1sm_attr() {
     static std::mutex mu;
     static bool done[64] = {};
-    return ensure_smem_attr(mx_gemm_kernel<FP4>, sm1::smem_alloc(FP4), mu, done);
+    return ensure_smem_attr(mx_gemm_kernel<FP4, MN>, sm1::smem_alloc(FP4), mu, done);
 }
 template <bool FP4, int QFMT, int MN = 0>
 cudaError_t ensure_2sm_attr() {
@@ -1689,29 +1711,36 @@ int choose_split_k(int tiles, int num_kb) {
     return 1;
 }
 
-template <bool FP4>
+template <bool FP4, int MN = 0>
 cudaError_t launch_1sm(const GemmArgs& g, cudaStream_t stream, bool allow_split) {
-    if (g.a_mn_major || g.b_mn_major) return cudaErrorInvalidValue;  // K-major operands only
-    const cudaError_t attr_err = ensure_1sm_attr<FP4>();
+    if ((g.a_mn_major ? 2 : 0) + (g.b_mn_major ? 1 : 0) != MN || (MN && FP4)) return cudaErrorInvalidValue;
+    const cudaError_t attr_err = ensure_1sm_attr<FP4, MN>();
     if (attr_err != cudaSuccess) return attr_err;
     CUtensorMap ma, mb;
-    if (!make_operand_map(&ma, g.a, g.M, row_bytes(g), sm1::BM, g.batch, g.a_batch_stride) ||
-        !make_operand_map(&mb, g.bt, g.N, row_bytes(g), sm1::BN, g.batch, g.b_batch_stride))
-        return cudaErrorInvalidValue;
+    // MN-major maps load 128-row boxes: A's 128-row tile is one box, B's
+    // 256-row tile two
+    const bool map_a = g.a_mn_major ? make_operand_map_mn(&ma, g.a, g.M, g.K, g.batch, g.a_batch_stride)
+                                    : make_operand_map(&ma, g.a, g.M, row_bytes(g), sm1::BM, g.batch, g.a_batch_stride);
+    const bool map_b = g.b_mn_major ? make_operand_map_mn(&mb, g.bt, g.N, g.K, g.batch, g.b_batch_stride)
+                                    : make_operand_map(&mb, g.bt, g.N, row_bytes(g), sm1::BN, g.batch, g.b_batch_stride);
+    if (!map_a || !map_b) return cudaErrorInvalidValue;
     KParams p = base_params(g, sm1::BM, sm1::BN);
+    p.a_mn = g.a_mn_major ? 1 : 0;
+    p.b_mn = g.b_mn_major ? 1 : 0;
+    p.idesc |= (p.a_mn ? kIdescAMnMajor : 0u) | (p.b_mn ? kIdescBMnMajor : 0u);
     const int tiles = p.batch * p.num_m_tiles * p.num_n_tiles;
     p.split_k = allow_split ? choose_split_k<FP4>(tiles, p.num_kb) : 1;
-    g_last_launch = GemmLaunchInfo{1, p.split_k};
+    g_last_launch = GemmLaunchInfo{1, p.split_k, p.a_mn, p.b_mn};
     if (p.split_k > 1) {
         cudaLaunchConfig_t cfg;
         cudaLaunchAttribute attr[2];
         split_launch_config(&cfg, attr, tiles, p.split_k, FP4, stream);
-        return cudaLaunchKernelEx(&cfg, mx_gemm_kernel<FP4>, ma, mb, p);
+        return cudaLaunchKernelEx(&cfg, mx_gemm_kernel<FP4, MN>, ma, mb, p);
     }
     const int sms = device_sm_count();
     const int grid = tiles < sms ? tiles : sms;
-    return launch_pdl(mx_gemm_kernel<FP4>, static_cast<unsigned>(grid), sm1::THREADS, sm1::smem_alloc(FP4), stream,
-                      ma, mb, p);
+    return launch_pdl(mx_gemm_kernel<FP4, MN>, static_cast<unsigned>(grid), sm1::THREADS, sm1::smem_alloc(FP4),
+                      stream, ma, mb, p);
 }
 
 // attr: room for 2 (cluster shape, programmatic serialization)
@@ -1866,15 +1895,17 @@ bool scaled_matmul_takes_pair(const GemmArgs& g) {
 
 cudaError_t launch_scaled_matmul(const GemmArgs& g, cudaStream_t stream) {
     const bool fp4 = is_fp4(g);
-    // MN-major operands: the pair kernel reads them (callers check
-    // scaled_matmul_takes_pair first)
-    const bool pair = g.a_mn_major || g.b_mn_major || scaled_matmul_takes_pair(g);
+    const bool pair = scaled_matmul_takes_pair(g);
     const bool split = g_variant != 3;
     if (fp4) return pair ? launch_2sm<true, -1>(g, stream) : launch_1sm<true>(g, stream, split);
-    if (g.a_mn_major && g.b_mn_major) return launch_2sm<false, -1, 3>(g, stream);
-    if (g.a_mn_major) return launch_2sm<false, -1, 2>(g, stream);
-    if (g.b_mn_major) return launch_2sm<false, -1, 1>(g, stream);
-    return pair ? launch_2sm<false, -1>(g, stream) : launch_1sm<false>(g, stream, split);
+    // FP8 operands read MN-major (a dot operand stored [batch, K, rows]):
+    // one instantiation of each kernel per combination
+    switch ((g.a_mn_major ? 2 : 0) + (g.b_mn_major ? 1 : 0)) {
+    case 1: return pair ? launch_2sm<false, -1, 1>(g, stream) : launch_1sm<false, 1>(g, stream, split);
+    case 2: return pair ? launch_2sm<false, -1, 2>(g, stream) : launch_1sm<false, 2>(g, stream, split);
+    case 3: return pair ? launch_2sm<false, -1, 3>(g, stream) : launch_1sm<false, 3>(g, stream, split);
+    default: return pair ? launch_2sm<false, -1>(g, stream) : launch_1sm<false>(g, stream, split);
+    }
 }
 
 // The fused call runs as one launch when the pair kernel takes the product

@@ -634,11 +634,10 @@ mx_status mx_block_scaled_dot(const void* lhs, const int64_t* lhs_dims, int lhs_
     g.b_batch_stride = P.N * elem_bytes(elem_dtype, P.K);
     g.c_batch_stride = P.M * P.N;
     // An FP8 operand stored [batch, K, rows] is read in place, MN-major, when
-    // the pair kernel takes the product and its rows are whole 16-byte
-    // multiples; otherwise it is copied into [batch, rows, K] first.
-    const bool pair = !fp4 && scaled_matmul_takes_pair(g);
-    g.a_mn_major = pair && P.lmn && P.M % 16 == 0 && aligned16(lhs);
-    g.b_mn_major = pair && P.rmn && P.N % 16 == 0 && aligned16(rhs);
+    // its rows are whole 16-byte multiples; otherwise it is copied into
+    // [batch, rows, K] first.
+    g.a_mn_major = !fp4 && P.lmn && P.M % 16 == 0 && aligned16(lhs);
+    g.b_mn_major = !fp4 && P.rmn && P.N % 16 == 0 && aligned16(rhs);
     const uint8_t* a = static_cast<const uint8_t*>(lhs);
     const uint8_t* sa = static_cast<const uint8_t*>(lhs_scale);
     const uint8_t* bt = static_cast<const uint8_t*>(rhs);

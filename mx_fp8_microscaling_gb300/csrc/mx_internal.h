@@ -107,11 +107,11 @@ struct GemmArgs {
     uint64_t* q_flags;
     // FP8, not fused: A stored [batch, K, M] / Bt stored [batch, K, N] (M / N
     // innermost, rows M / N bytes, a multiple of 16; the batch strides still
-    // count the whole problem); read MN-major by the pair kernel.
+    // count the whole problem); read as MN-major tiles by either kernel.
     int32_t a_mn_major, b_mn_major;
 };
 cudaError_t launch_scaled_matmul(const GemmArgs& g, cudaStream_t stream);
-// Whether launch_scaled_matmul runs `g` (its K-major form) on the pair kernel.
+// Whether launch_scaled_matmul runs `g` on the pair kernel (else the 1-SM one).
 bool scaled_matmul_takes_pair(const GemmArgs& g);
 // Whether the fused call runs as one launch of the pair kernel (else
 // QuantizeMX, then launch_scaled_matmul), and that launch.

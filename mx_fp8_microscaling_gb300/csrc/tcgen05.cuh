@@ -432,14 +432,16 @@ __device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t saddr) {
 
 // Shared-memory matrix descriptor, MN-major 8-bit operand tile: TMA wrote
 // rows of 128 bytes along M (or N), one row per K index, with the 128-byte
-// swizzle, so the tile is a single swizzle atom wide along MN (128
-// elements) and its 8-row K groups are 1024 bytes apart (SBO).  The leading
-// byte offset steps between atoms along MN; with one atom per tile no MMA
-// uses it, and it is set equal to the SBO so that no reading of the two
-// fields reaches outside the tile.  A K offset of k rows adds k * 128 bytes
-// to the start address (multiples of 32 rows keep it 1024-byte aligned).
-__device__ __forceinline__ uint64_t sdesc_mnmajor_sw128(uint32_t saddr) {
-    return static_cast<uint64_t>((saddr >> 4) & 0x3FFFu) | (static_cast<uint64_t>(1024 >> 4) << 16) |
+// swizzle, so each swizzle atom is 128 elements wide along MN and its 8-row
+// K groups are 1024 bytes apart (SBO).  The leading byte offset (LBO) steps
+// from one 128-element atom column to the next along MN: a tile one atom
+// wide never uses it (it is then set equal to the SBO, so that no reading
+// of the two fields reaches outside the tile); a 256-row tile loaded as two
+// atom columns `lbo` bytes apart passes that distance.  A K offset of k rows
+// adds k * 128 bytes to the start address (multiples of 32 rows keep it
+// 1024-byte aligned).
+__device__ __forceinline__ uint64_t sdesc_mnmajor_sw128(uint32_t saddr, uint32_t lbo = 1024) {
+    return static_cast<uint64_t>((saddr >> 4) & 0x3FFFu) | (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
            (static_cast<uint64_t>(1024 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) |
            (static_cast<uint64_t>(2) << 61);
 }

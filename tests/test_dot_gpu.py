@@ -139,11 +139,11 @@ def test_large_batched_sampled(mx):
 # ---------------------------------------------------------------- MN-major operands
 #
 # An FP8 operand stored [batch, K, rows] (the contracting axis before the free
-# axes) is read in place by the pair kernel as MN-major tiles, with no
-# transposing copy, when its rows are a multiple of 16 bytes.  Each case runs
-# under the forced pair kernel (small shapes) or automatic choice (large
-# ones), checks which operands were read in place, and compares every element
-# with the oracle.
+# axes) is read in place as MN-major tiles, with no transposing copy, when its
+# rows are a multiple of 16 bytes, by either GEMM kernel.  Each case runs
+# under a forced kernel (small shapes) or the automatic choice (large ones),
+# checks which operands were read in place, and compares every element with
+# the oracle.
 
 def run_major(mx, lshape, rshape, lb, rb, lc, rc, fmt, out_dtype, seed, variant=2):
     import torch
@@ -217,13 +217,50 @@ def test_mn_major_equals_copied_operand_bitwise(mx):
     assert torch.equal(in_place.view(torch.int32), copied.view(torch.int32))
 
 
-def test_mn_major_not_used_by_the_one_sm_kernel(mx):
-    # M <= 128 runs on the 1-SM kernel, which reads K-major rows only: the
-    # [B, K, N] operand is copied, and the result still matches the oracle
-    _, launch, majors = run_major(mx, (2, 64, 256), (2, 256, 512), (0,), (0,), 2, 1, "e4m3fn", "bf16", seed=7,
-                                  variant=0)
+ONE_SM_CASES = {
+    # M <= 128: the 1-SM kernel, split K over a cluster where the shape
+    # calls for it; its MN-major B tile is two 128-row atom columns
+    "rhs_kn_split": ((2, 64, 2048), (2, 2048, 512), (0,), (0,), 2, 1, (0, 1)),
+    "rhs_kn_ragged_n": ((3, 100, 1024), (3, 1024, 208), (0,), (0,), 2, 1, (0, 1)),
+    "lhs_km": ((2, 1024, 48), (2, 300, 1024), (0,), (0,), 1, 2, (1, 0)),
+    "both_mn_k_tail": ((1, 160, 128), (1, 160, 400), (0,), (0,), 1, 1, (1, 1)),
+}
+
+
+@pytest.mark.parametrize("out_dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("variant", [0, 3], ids=["auto", "no_split"])
+@pytest.mark.parametrize("name", sorted(ONE_SM_CASES))
+def test_mn_major_on_the_one_sm_kernel(mx, name, variant, out_dtype):
+    lshape, rshape, lb, rb, lc, rc, majors = ONE_SM_CASES[name]
+    _, launch, got = run_major(mx, lshape, rshape, lb, rb, lc, rc, "e4m3fn", out_dtype,
+                               seed=200 + sorted(ONE_SM_CASES).index(name), variant=variant)
     assert launch[0] == 1
-    assert majors == (0, 0)
+    assert launch[1] == 1 if variant == 3 else launch[1] >= 1
+    assert got == majors
+
+
+def test_mn_major_one_sm_split_equals_copied_operand_bitwise(mx):
+    # the split-K slices add the same partial products in the same order
+    # whichever way B is stored
+    import torch
+    rng = np.random.default_rng(43)
+    B, M, N, K = 2, 96, 768, 4096
+    a, sa = operand(rng, (B, M, K), 2, "e5m2")
+    b_kn, sb_kn = operand(rng, (B, K, N), 1, "e5m2")
+    b_nk = np.ascontiguousarray(b_kn.transpose(0, 2, 1))
+    sb_nk = np.ascontiguousarray(sb_kn.transpose(0, 2, 1))
+    in_place = mx.mx_block_scaled_dot(to_device_u8(a), to_device_u8(b_kn), to_device_u8(sa), to_device_u8(sb_kn),
+                                      "e5m2", "f32", lhs_batch=(0,), rhs_batch=(0,), rhs_contract=(1,))
+    assert mx.mx_debug_last_gemm_operands() == (0, 1)
+    kernel, split = mx.mx_debug_last_gemm_launch()
+    assert kernel == 1 and split > 1
+    copied = mx.mx_block_scaled_dot(to_device_u8(a), to_device_u8(b_nk), to_device_u8(sa), to_device_u8(sb_nk),
+                                    "e5m2", "f32", lhs_batch=(0,), rhs_batch=(0,))
+    assert mx.mx_debug_last_gemm_operands() == (0, 0)
+    torch.cuda.synchronize()
+    assert torch.equal(in_place.view(torch.int32), copied.view(torch.int32))
+    want, s = orc.block_scaled_dot(a, b_kn, sa, sb_kn, "e5m2", lhs_batch=(0,), rhs_batch=(0,), rhs_contract=(1,))
+    check_gemm(in_place.cpu().numpy(), want, s, "f32")
 
 
 def test_mn_major_full_tiles_sampled(mx):
