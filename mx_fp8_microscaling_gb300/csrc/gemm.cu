@@ -134,8 +134,9 @@ struct KParams {
     int q_lookahead;      // tile groups past the CTA's current one whose items it may quantize
     int q_emax;           // EMAX of the element format
     int q_no_publish;     // fault injection: items are never published (the loads' waits time out)
-    // Pair kernel, FP8 only: A (B) is stored [batch, K, M] ([batch, K, N]),
-    // M (N) innermost; its tiles are loaded and fed to the MMA MN-major.
+    // FP8 only: A (B) is stored [batch, K, M] ([batch, K, N]), M (N)
+    // innermost, and read as MN-major tiles.  The kernels take the layout
+    // from their MN template bits; these record it for the launch's caller.
     int a_mn, b_mn;
 };
 
