@@ -35,6 +35,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import os
 import statistics
@@ -78,11 +79,19 @@ def load_peaks():
     return {"hbm": 6800.0, "bf16": 1900.0, "bf16_sust": 1700.0, "src": "of fallback"}
 
 
+def code_text(src):
+    """Source text without C/C++ comments and with whitespace runs collapsed:
+    what the compiler sees, so that editing a comment keeps the hash."""
+    src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", " ", src)
+    return " ".join(src.split())
+
+
 def source_hash(*names):
     h = hashlib.sha256()
     for n in names:
-        with open(os.path.join(ROOT, "mx_fp8_microscaling_gb300", "csrc", n), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "mx_fp8_microscaling_gb300", "csrc", n), encoding="utf-8") as f:
+            h.update(code_text(f.read()).encode())
     return h.hexdigest()[:16]
 
 
