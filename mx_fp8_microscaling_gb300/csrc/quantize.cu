@@ -71,9 +71,12 @@ __device__ __forceinline__ void store8(uint8_t* dst, uint32_t w0, uint32_t w1) {
 // ------------------------------------------------------ 8x4 blocks, dim=-2
 
 // Thread unit: row group g (8 rows) x column chunk c (8 columns) = 2 blocks.
-// Consecutive threads take consecutive chunks of the same rows.
+// Consecutive threads take consecutive chunks of the same rows.  Held to 64
+// registers so that four blocks (32 warps of loads in flight) fit on an SM:
+// the FP8 instantiations take 59 anyway; the e2m1 one took 80 and three
+// blocks, and went 6318 -> 6483 GB/s on [16384, 16384] bf16 with the bound.
 template <bool F16, int FMT>
-__global__ void __launch_bounds__(kThreads) quant_g84(QuantArgs q) {
+__global__ void __launch_bounds__(kThreads, 4) quant_g84(QuantArgs q) {
     dev::pdl_allow_next();
     dev::pdl_wait_prior();
     const int64_t nchunk = q.cols >> 3;
