@@ -416,11 +416,15 @@ mx_status mx_block_scaled_dot_workspace(const int64_t* lhs_dims, int lhs_rank, c
  *   out_dtype   MX_F32 | MX_BF16 (round to nearest even); `out` is dense in
  *               the order of mx_block_scaled_dot_shape, caller-owned
  *   workspace   device, 16-byte aligned, mx_block_scaled_dot_workspace bytes
- *               (canonical copies of operands that are not already
- *               [batch.., free.., K] in memory, and the scales in the
- *               tensor-core layout)
+ *               (room for canonical copies of operands that are not
+ *               already [batch.., free.., K] in memory, and the scales in
+ *               the tensor-core layout)
  * Operands already in [batch.., free.., K] order are read in place and must
- * be 16-byte aligned.  Accumulation is f32 on the tensor cores.
+ * be 16-byte aligned.  FP8 operands stored [batch.., K, free..] (the batch
+ * axes in order, then the contracting axis) are read in place too, as
+ * MN-major tiles, when their rows (the product of the free extents) are a
+ * multiple of 16 bytes on a 16-byte aligned base; other layouts are copied
+ * into [batch, rows, K] first.  Accumulation is f32 on the tensor cores.
  * Errors (nothing launched): MX_ERR_SHAPE (rank < 2 or > MX_MAX_RANK, batch
  * or contracting extents differ, K not a multiple of 32 or < 32, extents
  * over 2^30), MX_ERR_DIM (batch counts differ, an index out of bounds or
