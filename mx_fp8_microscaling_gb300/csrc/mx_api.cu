@@ -162,7 +162,7 @@ struct DotPlan {
     int lc = 0, rc = 0;
     bool lcanon = true, rcanon = true;
     // stored [batch..., K, free...] (batch axes in order, then the
-    // contracting one): an MN-major operand the pair kernel reads in place
+    // contracting one): an MN-major operand the GEMM kernels read in place
     bool lmn = false, rmn = false;
     size_t off_lq = 0, off_ls = 0, off_rq = 0, off_rs = 0, off_sfa = 0, off_sfb = 0, total = 0;
 };
