@@ -49,3 +49,16 @@ def test_reference_arm_prints_contract_line():
         assert key in line, key
     assert line["impl"] == "reference" and line["unit"] == "GB/s" and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle" and line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_kernel_source_hash_ignores_comments_only():
+    """traffic.json entries are keyed on the kernels' code: editing a comment
+    or whitespace keeps the key, editing code changes it."""
+    sys.path.insert(0, ROOT)
+    import bench
+    base = "int f(int x) {\n    return x + 1;  // one more\n}\n/* block\n comment */\n"
+    assert bench.code_text(base) == bench.code_text(base.replace("// one more", "// another note"))
+    assert bench.code_text(base) == bench.code_text(base.replace("    return", "\treturn"))
+    assert bench.code_text(base) == bench.code_text(base.replace("/* block\n comment */", ""))
+    assert bench.code_text(base) != bench.code_text(base.replace("x + 1", "x + 2"))
+    assert bench.code_text(base) == "int f(int x) { return x + 1; }"
